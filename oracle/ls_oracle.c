@@ -1,0 +1,326 @@
+/*
+ * ls_oracle.c -- FP64 CPU oracle (test infrastructure only; see ls_oracle.h).
+ *
+ * Each function writes out the plain definition of what the fused operator
+ * computes, element by element, in double precision.  Where the fast method
+ * reaches the same result by a rewrite (the single-sync LayerNorm statistics,
+ * the two-sum LayerNorm backward) this file does NOT follow the rewrite: it
+ * computes the textbook two-pass definition, so that the rewrite is checked
+ * against the definition rather than against itself.
+ *
+ * Sources (page title, section):
+ *  [L10]  "CMU 11-868 L10: accelerating the Transformer on GPUs (LightSeq)",
+ *         section "Technique 1: kernel fusion" (the fused bias+dropout+residual,
+ *         bias+ReLU+dropout, LayerNorm and softmax operators, slide p.12) and
+ *         section "Technique 2: rewrite the formula" (LayerNorm statistics,
+ *         slide p.21; LayerNorm backward, slide p.22; softmax, slides p.23-26).
+ *  [LS2]  "LightSeq2: Accelerated Training for Transformer-based Models on GPUs",
+ *         section 2.1.1 (Transformer-layer operator taxonomy and the fused
+ *         bias+dropout+residual example) and section 2.1.2 (dropout with a
+ *         saved mask m reused in the backward pass).
+ *  [CS336] "CS336 Lecture 5: GPU", section 6.1 (row softmax of the attention
+ *         score matrix) and section 6.2 (the max-subtracted softmax).
+ *  Philox-4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
+ *         Easy as 1, 2, 3", SC'11 (the pages name no generator).
+ */
+#include "ls_oracle.h"
+
+#include <math.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+/* ------------------------------------------------------------------------- */
+/* Philox-4x32-10 (SC'11, section 3.3 "Philox"; constants from its table of   */
+/* multipliers and Weyl key increments).                                      */
+/* ------------------------------------------------------------------------- */
+#define PHILOX_M0 0xD2511F53u
+#define PHILOX_M1 0xCD9E8D57u
+#define PHILOX_W0 0x9E3779B9u
+#define PHILOX_W1 0xBB67AE85u
+
+void or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]) {
+    uint32_t c0 = ctr[0], c1 = ctr[1], c2 = ctr[2], c3 = ctr[3];
+    uint32_t k0 = key[0], k1 = key[1];
+    for (int round = 0; round < 10; ++round) {
+        if (round > 0) { /* key schedule: add the Weyl constants between rounds */
+            k0 += PHILOX_W0;
+            k1 += PHILOX_W1;
+        }
+        uint64_t p0 = (uint64_t)PHILOX_M0 * (uint64_t)c0;
+        uint64_t p1 = (uint64_t)PHILOX_M1 * (uint64_t)c2;
+        uint32_t n0 = (uint32_t)(p1 >> 32) ^ c1 ^ k0;
+        uint32_t n1 = (uint32_t)p1;
+        uint32_t n2 = (uint32_t)(p0 >> 32) ^ c3 ^ k1;
+        uint32_t n3 = (uint32_t)p0;
+        c0 = n0; c1 = n1; c2 = n2; c3 = n3;
+    }
+    out[0] = c0; out[1] = c1; out[2] = c2; out[3] = c3;
+}
+
+/* Reading (the pages name no generator): the key is the 64-bit seed, the
+ * counter's low half is the 128-bit block number i>>2 and its high half is the
+ * call's 64-bit offset; element i takes 32-bit word i&3 of its block. */
+uint32_t or_dropout_word(uint64_t seed, uint64_t offset, uint64_t i) {
+    uint64_t block = i >> 2;
+    uint32_t ctr[4] = {(uint32_t)block, (uint32_t)(block >> 32), (uint32_t)offset,
+                       (uint32_t)(offset >> 32)};
+    uint32_t key[2] = {(uint32_t)seed, (uint32_t)(seed >> 32)};
+    uint32_t out[4];
+    or_philox4x32_10(ctr, key, out);
+    return out[i & 3];
+}
+
+/* Keep with probability 1 - p: a uniform 32-bit word u keeps the element iff
+ * u >= floor(p * 2^32) (clamped to 2^32 - 1).  p is the FP32 value the caller
+ * passes; p = 0 keeps everything. */
+uint32_t or_dropout_threshold(float p) {
+    double t = floor((double)p * 4294967296.0);
+    if (t <= 0.0) return 0u;
+    if (t >= 4294967295.0) return 4294967295u;
+    return (uint32_t)t;
+}
+
+static int keep_bit(uint64_t seed, uint64_t offset, uint64_t i, uint32_t thr) {
+    return or_dropout_word(seed, offset, i) >= thr;
+}
+
+static int64_t mask_word_count(int64_t n) { return (n + 31) / 32; }
+
+static int get_bit(const uint32_t* words, int64_t i) {
+    return (int)((words[i >> 5] >> (i & 31)) & 1u);
+}
+
+void or_dropout_keep_bits(int64_t n, float p, uint64_t seed, uint64_t offset, uint32_t* words) {
+    uint32_t thr = or_dropout_threshold(p);
+    memset(words, 0, (size_t)mask_word_count(n) * sizeof(uint32_t));
+    for (int64_t i = 0; i < n; ++i)
+        if (keep_bit(seed, offset, (uint64_t)i, thr)) words[i >> 5] |= 1u << (i & 31);
+}
+
+/* ------------------------------------------------------------------------- */
+/* bias + dropout + residual  ([L10] technique 1; [LS2] 2.1.1)                */
+/* ------------------------------------------------------------------------- */
+void or_bdr_fwd(int64_t rows, int64_t cols, const double* x, const double* bias,
+                const double* residual, float p, uint64_t seed, uint64_t offset,
+                double* out, uint32_t* mask_words) {
+    const uint32_t thr = or_dropout_threshold(p);
+    const double scale = 1.0 / (1.0 - (double)p);
+    const int64_t n = rows * cols;
+    if (mask_words) memset(mask_words, 0, (size_t)mask_word_count(n) * sizeof(uint32_t));
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            int64_t i = r * cols + c;
+            int keep = keep_bit(seed, offset, (uint64_t)i, thr);
+            double z = x[i] + bias[c];
+            out[i] = residual[i] + (keep ? z * scale : 0.0);
+        }
+    }
+    if (mask_words)
+        for (int64_t i = 0; i < n; ++i)
+            if (keep_bit(seed, offset, (uint64_t)i, thr)) mask_words[i >> 5] |= 1u << (i & 31);
+}
+
+/* Shared by both dropout backward passes: dx = bit * dout / (1 - p), and the
+ * bias gradient is the column sum of dx (the bias is broadcast over rows). */
+static void dropout_bwd_core(int64_t rows, int64_t cols, const double* dout,
+                             const uint32_t* mask_words, int regen, uint32_t thr,
+                             uint64_t seed, uint64_t offset, float p, double* dx,
+                             double* dbias) {
+    const double scale = 1.0 / (1.0 - (double)p);
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            int64_t i = r * cols + c;
+            int bit = regen ? keep_bit(seed, offset, (uint64_t)i, thr) : get_bit(mask_words, i);
+            dx[i] = bit ? dout[i] * scale : 0.0;
+        }
+    }
+    if (dbias) {
+        for (int64_t c = 0; c < cols; ++c) {
+            double s = 0.0;
+            for (int64_t r = 0; r < rows; ++r) s += dx[r * cols + c];
+            dbias[c] = s;
+        }
+    }
+}
+
+void or_bdr_bwd(int64_t rows, int64_t cols, const double* dout, const uint32_t* mask_words,
+                float p, uint64_t seed, uint64_t offset, double* dx, double* dbias) {
+    dropout_bwd_core(rows, cols, dout, mask_words, mask_words == NULL, or_dropout_threshold(p),
+                     seed, offset, p, dx, dbias);
+}
+
+/* ------------------------------------------------------------------------- */
+/* bias + ReLU + dropout  ([L10] technique 1).  ReLU(0) = 0 and its slope at  */
+/* 0 is taken as 0, so the saved bit is (z > 0) and keep.                     */
+/* ------------------------------------------------------------------------- */
+void or_brd_fwd(int64_t rows, int64_t cols, const double* x, const double* bias,
+                float p, uint64_t seed, uint64_t offset, double* out, uint32_t* mask_words) {
+    const uint32_t thr = or_dropout_threshold(p);
+    const double scale = 1.0 / (1.0 - (double)p);
+    const int64_t n = rows * cols;
+    if (mask_words) memset(mask_words, 0, (size_t)mask_word_count(n) * sizeof(uint32_t));
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        for (int64_t c = 0; c < cols; ++c) {
+            int64_t i = r * cols + c;
+            double z = x[i] + bias[c];
+            int bit = (z > 0.0) && keep_bit(seed, offset, (uint64_t)i, thr);
+            out[i] = bit ? z * scale : 0.0;
+        }
+    }
+    if (mask_words)
+        for (int64_t r = 0; r < rows; ++r)
+            for (int64_t c = 0; c < cols; ++c) {
+                int64_t i = r * cols + c;
+                double z = x[i] + bias[c];
+                if ((z > 0.0) && keep_bit(seed, offset, (uint64_t)i, thr))
+                    mask_words[i >> 5] |= 1u << (i & 31);
+            }
+}
+
+void or_brd_bwd(int64_t rows, int64_t cols, const double* dout, const uint32_t* mask_words,
+                float p, double* dx, double* dbias) {
+    dropout_bwd_core(rows, cols, dout, mask_words, 0, 0u, 0u, 0u, p, dx, dbias);
+}
+
+/* ------------------------------------------------------------------------- */
+/* LayerNorm ([L10] technique 2, slides p.21-22).  Definition, two passes:    */
+/*   mu = mean(x);  var = mean((x - mu)^2);  rstd = 1 / sqrt(var + eps)       */
+/*   y  = gamma * (x - mu) * rstd + beta                                       */
+/* ------------------------------------------------------------------------- */
+static void row_stats(const double* xr, int64_t cols, double eps, double* mu_out,
+                      double* rstd_out) {
+    double s = 0.0;
+    for (int64_t c = 0; c < cols; ++c) s += xr[c];
+    double mu = s / (double)cols;
+    double v = 0.0;
+    for (int64_t c = 0; c < cols; ++c) v += (xr[c] - mu) * (xr[c] - mu);
+    v /= (double)cols;
+    *mu_out = mu;
+    *rstd_out = 1.0 / sqrt(v + eps);
+}
+
+void or_layernorm_fwd(int64_t rows, int64_t cols, const double* x, const double* gamma,
+                      const double* beta, double eps, double* y, double* mean, double* rstd) {
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * cols;
+        double mu, rs;
+        row_stats(xr, cols, eps, &mu, &rs);
+        for (int64_t c = 0; c < cols; ++c) y[r * cols + c] = gamma[c] * (xr[c] - mu) * rs + beta[c];
+        if (mean) mean[r] = mu;
+        if (rstd) rstd[r] = rs;
+    }
+}
+
+/* Textbook LayerNorm gradient with xhat = (x - mu) * rstd and g = gamma * dy:
+ *   dx     = rstd * (g - mean(g) - xhat * mean(g * xhat))
+ *   dgamma = sum over rows of dy * xhat,   dbeta = sum over rows of dy.
+ * The statistics are recomputed here from x by the definition above. */
+void or_layernorm_bwd(int64_t rows, int64_t cols, const double* dy, const double* x,
+                      const double* gamma, double eps, double* dx, double* dgamma,
+                      double* dbeta) {
+    double* xhat = (double*)malloc((size_t)(rows * cols) * sizeof(double));
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const double* xr = x + r * cols;
+        const double* dyr = dy + r * cols;
+        double mu, rs;
+        row_stats(xr, cols, eps, &mu, &rs);
+        double mean_g = 0.0, mean_gx = 0.0;
+        for (int64_t c = 0; c < cols; ++c) {
+            double xh = (xr[c] - mu) * rs;
+            xhat[r * cols + c] = xh;
+            double g = gamma[c] * dyr[c];
+            mean_g += g;
+            mean_gx += g * xh;
+        }
+        mean_g /= (double)cols;
+        mean_gx /= (double)cols;
+        for (int64_t c = 0; c < cols; ++c) {
+            double xh = xhat[r * cols + c];
+            double g = gamma[c] * dyr[c];
+            dx[r * cols + c] = rs * (g - mean_g - xh * mean_gx);
+        }
+    }
+    for (int64_t c = 0; c < cols; ++c) {
+        double sg = 0.0, sb = 0.0;
+        for (int64_t r = 0; r < rows; ++r) {
+            sg += dy[r * cols + c] * xhat[r * cols + c];
+            sb += dy[r * cols + c];
+        }
+        if (dgamma) dgamma[c] = sg;
+        if (dbeta) dbeta[c] = sb;
+    }
+    free(xhat);
+}
+
+/* ------------------------------------------------------------------------- */
+/* Masked softmax over the key axis ([L10] slides p.23-26; [CS336] 6.1-6.2).  */
+/* ------------------------------------------------------------------------- */
+static int64_t valid_len(int64_t b, int64_t q, int64_t q_len, int64_t k_len,
+                         const int32_t* key_len, int causal) {
+    int64_t v = k_len;
+    if (key_len) {
+        int64_t kl = key_len[b];
+        if (kl < 0) kl = 0;
+        if (kl < v) v = kl;
+    }
+    if (causal) {
+        int64_t last = q + k_len - q_len; /* last key the query may see */
+        if (last + 1 < v) v = last + 1;
+    }
+    return v < 0 ? 0 : v;
+}
+
+void or_softmax_fwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
+                    const double* x, const int32_t* key_len, int causal, double* y) {
+    const int64_t nrows = batch * heads * q_len;
+#pragma omp parallel for schedule(static)
+    for (int64_t row = 0; row < nrows; ++row) {
+        int64_t b = row / (heads * q_len);
+        int64_t q = row % q_len;
+        const double* xr = x + row * k_len;
+        double* yr = y + row * k_len;
+        int64_t v = valid_len(b, q, q_len, k_len, key_len, causal);
+        double m = -INFINITY;
+        for (int64_t j = 0; j < v; ++j)
+            if (xr[j] > m) m = xr[j];
+        double s = 0.0;
+        for (int64_t j = 0; j < v; ++j) s += exp(xr[j] - m);
+        for (int64_t j = 0; j < k_len; ++j) yr[j] = (j < v) ? exp(xr[j] - m) / s : 0.0;
+    }
+}
+
+/* dx = y * (dy - <y, dy>) over the valid keys, 0 on masked keys (the
+ * Jacobian-vector product of the row softmax). */
+void or_softmax_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
+                    const double* y, const double* dy, const int32_t* key_len, int causal,
+                    double* dx) {
+    const int64_t nrows = batch * heads * q_len;
+#pragma omp parallel for schedule(static)
+    for (int64_t row = 0; row < nrows; ++row) {
+        int64_t b = row / (heads * q_len);
+        int64_t q = row % q_len;
+        const double* yr = y + row * k_len;
+        const double* dyr = dy + row * k_len;
+        double* dxr = dx + row * k_len;
+        int64_t v = valid_len(b, q, q_len, k_len, key_len, causal);
+        double dot = 0.0;
+        for (int64_t j = 0; j < v; ++j) dot += yr[j] * dyr[j];
+        for (int64_t j = 0; j < k_len; ++j) dxr[j] = (j < v) ? yr[j] * (dyr[j] - dot) : 0.0;
+    }
+}
+
+int or_num_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

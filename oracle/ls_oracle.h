@@ -1,0 +1,80 @@
+/*
+ * ls_oracle.h -- FP64 CPU oracle for the fused non-GEMM Transformer-layer
+ * operators (bias+dropout+residual, bias+ReLU+dropout, LayerNorm, masked
+ * attention softmax; forward and backward).
+ *
+ * TEST INFRASTRUCTURE ONLY.  This is the plain, slow, obviously correct
+ * definition that the CUDA path is checked against.  Only the tests, the
+ * smoke check and the benchmark's CPU-baseline leg may call it.  It shares no
+ * code, header, table or constant with the CUDA library.
+ *
+ * Every floating-point input is an FP64 array holding exactly the values the
+ * GPU receives (FP16/FP32 storage values widen to FP64 without rounding).
+ * Every result is FP64.  Layouts are row-major:
+ *   activations  [rows, cols]            (rows = tokens, cols = hidden or FFN)
+ *   scores       [batch, heads, q_len, k_len]
+ *   dropout mask ceil(rows*cols/32) uint32 words; element i is bit (i & 31)
+ *                of word (i >> 5); bits past the last element are 0.
+ */
+#ifndef LS_ORACLE_H
+#define LS_ORACLE_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Philox-4x32 with 10 rounds (Salmon, Moraes, Dror, Shaw, "Parallel Random
+ * Numbers: As Easy as 1, 2, 3", SC'11): out = Philox(ctr, key). */
+void or_philox4x32_10(const uint32_t ctr[4], const uint32_t key[2], uint32_t out[4]);
+
+/* The 32-bit uniform word that element i of a dropout call (seed, offset)
+ * draws: block i>>2 of the counter stream, word i&3 of that block. */
+uint32_t or_dropout_word(uint64_t seed, uint64_t offset, uint64_t i);
+
+/* Keep threshold for drop probability p: element kept iff word >= threshold. */
+uint32_t or_dropout_threshold(float p);
+
+/* Keep bits of n elements (ceil(n/32) words). */
+void or_dropout_keep_bits(int64_t n, float p, uint64_t seed, uint64_t offset, uint32_t* words);
+
+/* bias + dropout + residual:  out = residual + keep * (x + bias[c]) / (1 - p) */
+void or_bdr_fwd(int64_t rows, int64_t cols, const double* x, const double* bias,
+                const double* residual, float p, uint64_t seed, uint64_t offset,
+                double* out, uint32_t* mask_words);
+/* dx = keep * dout / (1 - p);  dbias[c] = sum_r dx[r, c].  mask_words may be
+ * NULL, in which case the keep bits are drawn again from (seed, offset). */
+void or_bdr_bwd(int64_t rows, int64_t cols, const double* dout, const uint32_t* mask_words,
+                float p, uint64_t seed, uint64_t offset, double* dx, double* dbias);
+
+/* bias + ReLU + dropout:  z = x + bias[c];  bit = (z > 0) and keep;
+ * out = bit * z / (1 - p). */
+void or_brd_fwd(int64_t rows, int64_t cols, const double* x, const double* bias,
+                float p, uint64_t seed, uint64_t offset, double* out, uint32_t* mask_words);
+void or_brd_bwd(int64_t rows, int64_t cols, const double* dout, const uint32_t* mask_words,
+                float p, double* dx, double* dbias);
+
+/* LayerNorm over each row (biased variance, eps inside the square root). */
+void or_layernorm_fwd(int64_t rows, int64_t cols, const double* x, const double* gamma,
+                      const double* beta, double eps, double* y, double* mean, double* rstd);
+void or_layernorm_bwd(int64_t rows, int64_t cols, const double* dy, const double* x,
+                      const double* gamma, double eps, double* dx, double* dgamma,
+                      double* dbeta);
+
+/* Masked softmax along the last axis of [batch, heads, q_len, k_len].
+ * key_len may be NULL (no padding mask).  Entry (b, h, q, j) is valid iff
+ * j < clamp(key_len[b], 0, k_len) and, when causal, j <= q + k_len - q_len. */
+void or_softmax_fwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
+                    const double* x, const int32_t* key_len, int causal, double* y);
+void or_softmax_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
+                    const double* y, const double* dy, const int32_t* key_len, int causal,
+                    double* dx);
+
+/* OpenMP threads the row loops use. */
+int or_num_threads(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif

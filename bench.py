@@ -1,0 +1,546 @@
+#!/usr/bin/env python3
+"""Benchmark of the fused non-GEMM Transformer-layer operators on GB300.
+
+One step = the forward and backward pass of every fused operator of one
+Transformer layer (softmax, bias+dropout+residual after attention, LayerNorm,
+bias+ReLU+dropout after FFN1, bias+dropout+residual after FFN2, LayerNorm;
+then the backward of each in reverse order) over one batch of synthetic,
+device-resident inputs.  The step is captured once in a CUDA graph and
+replayed.  The metric is achieved HBM bandwidth: algorithmic bytes of the step
+(every input read once, every output written once) per second of step time;
+tokens/s and per-operator bandwidth are reported beside it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload bert-base]
+    python bench.py --impl reference ...     # the FP64 CPU oracle on the host
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own replica
+of the workload (weak scaling; the path has no exchange step).
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "achieved HBM GB/s and % of GB300 peak per fused op (fwd+bwd), tokens/s"
+UNIT = "GB/s"
+DEFAULT_WORKLOAD = "bert-base"
+L2_BYTES = 129e6
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
+                    choices=["transformer-base", "bert-base", "gpt2-large", "tiny"])
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle work for the cpu_baseline sample")
+    ap.add_argument("--details", default=None, help="also write a per-op JSON report here")
+    a = ap.parse_args()
+    if a.warmup < 3:
+        ap.error("--warmup must be >= 3")
+    return a
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def dist_env():
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+# ---------------------------------------------------------------------------
+# Clock sampling (nvidia-smi, 100 ms) during the GPU-busy window.
+# ---------------------------------------------------------------------------
+class ClockSampler:
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.samples = []
+        self._stop = threading.Event()
+        self._proc = None
+        self._thread = None
+
+    def start(self):
+        try:
+            self._proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except (OSError, FileNotFoundError):
+            self._proc = None
+            return
+        self._thread = threading.Thread(target=self._read, daemon=True)
+        self._thread.start()
+
+    def _read(self):
+        for line in self._proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[1]), float(parts[2]),
+                                     parts[5], parts[6], parts[7], parts[8]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self._proc is not None:
+            self._proc.terminate()
+            try:
+                self._proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self._proc.kill()
+        if self._thread is not None:
+            self._thread.join(timeout=5)
+
+    def summary(self, t0, t1):
+        win = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not win:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"], "samples": 0}
+        reasons = set()
+        for s in win:
+            for name, v in zip(("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown",
+                                "sw_power_cap"), s[3:7]):
+                if v.lower() == "active":
+                    reasons.add(name)
+        return {"sm_mhz": statistics.median(s[1] for s in win),
+                "sm_max_mhz": max(s[2] for s in win), "reasons": sorted(reasons),
+                "samples": len(win)}
+
+
+# ---------------------------------------------------------------------------
+# The layer step on the GPU.
+# ---------------------------------------------------------------------------
+class LayerStep:
+    """Device buffers of one layer and the ordered list of operator calls."""
+
+    def __init__(self, layer, seed, device):
+        import numpy as np
+        import torch
+
+        from transformer_layer_non_gb300 import accounting, ls_ops, synth
+
+        self.layer = layer
+        self.torch = torch
+        self.ls = ls_ops
+        L = layer
+        T, H, F = L.tokens, L.hidden, L.ffn
+        dt = {"f16": torch.float16, "f32": torch.float32}[L.dtype]
+        self.esize = 2 if L.dtype == "f16" else 4
+        host = synth.layer_inputs(L, seed)
+        self.key_len_np = host.get("key_len")
+        dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
+        self.inp = {k: dev(v) for k, v in host.items()}
+        e = lambda *s, d=dt: torch.empty(s, dtype=d, device=device)  # noqa: E731
+        nw = lambda n: (n + 31) // 32  # noqa: E731
+        self.out = {
+            "attn_out": e(T, H), "attn_mask": e(nw(T * H), d=torch.int32),
+            "ln1_y": e(T, H), "ln1_mean": e(T, d=torch.float32), "ln1_rstd": e(T, d=torch.float32),
+            "ffn1_out": e(T, F), "ffn1_mask": e(nw(T * F), d=torch.int32),
+            "ffn2_out": e(T, H), "ffn2_mask": e(nw(T * H), d=torch.int32),
+            "ln2_y": e(T, H), "ln2_mean": e(T, d=torch.float32), "ln2_rstd": e(T, d=torch.float32),
+            "probs": e(L.batch, L.heads, L.seq, L.seq),
+            "ln2_dx": e(T, H), "ln2_dgamma": e(H), "ln2_dbeta": e(H),
+            "ffn2_dx": e(T, H), "ffn2_dbias": e(H),
+            "ffn1_dx": e(T, F), "ffn1_dbias": e(F),
+            "ln1_dx": e(T, H), "ln1_dgamma": e(H), "ln1_dbeta": e(H),
+            "attn_dx": e(T, H), "attn_dbias": e(H),
+            "scores_dx": e(L.batch, L.heads, L.seq, L.seq),
+        }
+        ws = max(ls_ops.colreduce_workspace_bytes(T, F), ls_ops.colreduce_workspace_bytes(T, H))
+        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.bytes = accounting.layer_step_bytes(T, H, F, L.batch, L.heads, L.seq, self.esize,
+                                                 self.key_len_np, L.causal)
+        self.launches = {k: 1 for k in self.bytes}
+        for k in ("ln2_bwd", "ffn2_bdr_bwd", "ffn1_brd_bwd", "ln1_bwd", "attn_bdr_bwd"):
+            self.launches[k] = 2  # main kernel + deterministic column reduction
+
+    def ops(self):
+        """(name, thunk) in layer order: forward, then backward in reverse."""
+        ls, i, o, L, ws = self.ls, self.inp, self.out, self.layer, self.workspace
+        kl = i.get("key_len")
+        p = L.p
+        return [
+            ("softmax_fwd", lambda: ls.ls_softmax_fwd(o["probs"], i["scores"], kl, L.causal)),
+            ("attn_bdr_fwd", lambda: ls.ls_bias_dropout_residual_fwd(
+                o["attn_out"], o["attn_mask"], i["attn_x"], i["attn_bias"], i["attn_res"], p, 0, 1)),
+            ("ln1_fwd", lambda: ls.ls_layernorm_fwd(o["ln1_y"], o["ln1_mean"], o["ln1_rstd"],
+                                                    i["ln1_x"], i["ln1_gamma"], i["ln1_beta"], 1e-5)),
+            ("ffn1_brd_fwd", lambda: ls.ls_bias_relu_dropout_fwd(
+                o["ffn1_out"], o["ffn1_mask"], i["ffn1_x"], i["ffn1_bias"], p, 0, 2)),
+            ("ffn2_bdr_fwd", lambda: ls.ls_bias_dropout_residual_fwd(
+                o["ffn2_out"], o["ffn2_mask"], i["ffn2_x"], i["ffn2_bias"], i["ffn2_res"], p, 0, 3)),
+            ("ln2_fwd", lambda: ls.ls_layernorm_fwd(o["ln2_y"], o["ln2_mean"], o["ln2_rstd"],
+                                                    i["ln2_x"], i["ln2_gamma"], i["ln2_beta"], 1e-5)),
+            ("ln2_bwd", lambda: ls.ls_layernorm_bwd(
+                o["ln2_dx"], o["ln2_dgamma"], o["ln2_dbeta"], i["ln2_dy"], i["ln2_x"],
+                i["ln2_gamma"], o["ln2_mean"], o["ln2_rstd"], workspace=ws)),
+            ("ffn2_bdr_bwd", lambda: ls.ls_bias_dropout_residual_bwd(
+                o["ffn2_dx"], o["ffn2_dbias"], i["ffn2_dout"], o["ffn2_mask"], p, workspace=ws)),
+            ("ffn1_brd_bwd", lambda: ls.ls_bias_relu_dropout_bwd(
+                o["ffn1_dx"], o["ffn1_dbias"], i["ffn1_dout"], o["ffn1_mask"], p, workspace=ws)),
+            ("ln1_bwd", lambda: ls.ls_layernorm_bwd(
+                o["ln1_dx"], o["ln1_dgamma"], o["ln1_dbeta"], i["ln1_dy"], i["ln1_x"],
+                i["ln1_gamma"], o["ln1_mean"], o["ln1_rstd"], workspace=ws)),
+            ("attn_bdr_bwd", lambda: ls.ls_bias_dropout_residual_bwd(
+                o["attn_dx"], o["attn_dbias"], i["attn_dout"], o["attn_mask"], p, workspace=ws)),
+            ("softmax_bwd", lambda: ls.ls_softmax_bwd(o["scores_dx"], o["probs"], i["scores_dy"],
+                                                      kl, L.causal)),
+        ]
+
+    def footprint_bytes(self):
+        t = self.torch
+        tot = sum(v.numel() * v.element_size() for v in self.inp.values())
+        tot += sum(v.numel() * v.element_size() for v in self.out.values())
+        return tot
+
+
+def capture(step, with_events):
+    """Capture one step in a CUDA graph; optionally with an external timing
+    event before the first and after every operator."""
+    torch = step.torch
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    events = []
+    with torch.cuda.stream(s):
+        for _, fn in step.ops():  # eager warm-up outside capture (loads modules)
+            fn()
+    torch.cuda.current_stream().wait_stream(s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    if with_events:
+        events = [torch.cuda.Event(enable_timing=True, external=True)
+                  for _ in range(len(step.ops()) + 1)]
+    with torch.cuda.graph(g):
+        if with_events:
+            events[0].record()
+        for k, (_, fn) in enumerate(step.ops()):
+            fn()
+            if with_events:
+                events[k + 1].record()
+    torch.cuda.synchronize()
+    return g, events
+
+
+def kernels_sha():
+    h = hashlib.sha256()
+    csrc = os.path.join(ROOT, "transformer_layer_non_gb300", "csrc")
+    for f in sorted(os.listdir(csrc)):
+        h.update(f.encode())
+        h.update(open(os.path.join(csrc, f), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def ncu_traffic(kernel_key, workload):
+    """DRAM bytes per launch from a committed ncu summary, if it was taken on
+    the current kernel sources; else None."""
+    p = os.path.join(ROOT, "profiles", "ncu_traffic.json")
+    if not os.path.exists(p):
+        return None
+    try:
+        d = json.load(open(p))
+    except ValueError:
+        return None
+    if d.get("kernels_sha") != kernels_sha():
+        return None
+    e = d.get("ops", {}).get(workload, {}).get(kernel_key)
+    return None if e is None else e.get("dram_bytes_per_launch")
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle (cpu_baseline leg and the reference arm).
+# ---------------------------------------------------------------------------
+def oracle_sample_step(layer, frac, seed=0):
+    """Build a bounded sample of the layer (a fraction of its rows and of its
+    (batch, head) score slices) and return (run, algorithmic_bytes)."""
+    import numpy as np
+
+    import oracle
+    from transformer_layer_non_gb300 import accounting, synth
+
+    L = layer
+    T, H, F = L.tokens, L.hidden, L.ffn
+    d = synth.layer_inputs(L, seed)
+    rows = max(8, int(round(T * frac)))
+    nb = max(1, int(round(L.batch * frac)))
+    es = 2 if L.dtype == "f16" else 4
+    f64 = lambda a: np.ascontiguousarray(a, dtype=np.float64)  # noqa: E731
+    s = {k: f64(v) for k, v in d.items() if k not in ("scores", "scores_dy", "key_len")}
+    s = {k: (v[:rows] if v.ndim == 2 else v) for k, v in s.items()}
+    sc = f64(d["scores"][:nb])
+    sdy = f64(d["scores_dy"][:nb])
+    kl = d.get("key_len")
+    kl = None if kl is None else kl[:nb]
+    p, eps = L.p, 1e-5
+
+    def run():
+        out, m1 = oracle.bias_dropout_residual_fwd(s["attn_x"], s["attn_bias"], s["attn_res"], p, 0, 1)
+        y1, _, _ = oracle.layernorm_fwd(s["ln1_x"], s["ln1_gamma"], s["ln1_beta"], eps)
+        o2, m2 = oracle.bias_relu_dropout_fwd(s["ffn1_x"], s["ffn1_bias"], p, 0, 2)
+        o3, m3 = oracle.bias_dropout_residual_fwd(s["ffn2_x"], s["ffn2_bias"], s["ffn2_res"], p, 0, 3)
+        y2, _, _ = oracle.layernorm_fwd(s["ln2_x"], s["ln2_gamma"], s["ln2_beta"], eps)
+        pr = oracle.softmax_fwd(sc, kl, L.causal)
+        oracle.layernorm_bwd(s["ln2_dy"], s["ln2_x"], s["ln2_gamma"], eps)
+        oracle.bias_dropout_residual_bwd(s["ffn2_dout"], m3, p)
+        oracle.bias_relu_dropout_bwd(s["ffn1_dout"], m2, p)
+        oracle.layernorm_bwd(s["ln1_dy"], s["ln1_x"], s["ln1_gamma"], eps)
+        oracle.bias_dropout_residual_bwd(s["attn_dout"], m1, p)
+        oracle.softmax_bwd(pr, sdy, kl, L.causal)
+
+    b = accounting.layer_step_bytes(rows, H, F, nb, L.heads, L.seq, es, kl, L.causal)
+    sample = (f"{rows} of {T} token rows and {nb} of {L.batch} batch elements' score "
+              f"tensors of {L.name}, every operator forward and backward")
+    return run, sum(b.values()), rows / T, sample
+
+
+def calibrated_oracle(layer, budget_s, seed=0):
+    """Pick a sample fraction whose single pass takes about budget_s seconds."""
+    frac = 1.0 / 64
+    run, nbytes, _, _ = oracle_sample_step(layer, frac, seed)
+    t0 = time.perf_counter()
+    run()
+    dt = max(time.perf_counter() - t0, 1e-3)
+    frac = min(1.0, frac * budget_s / dt)
+    return oracle_sample_step(layer, frac, seed)
+
+
+def cpu_baseline(layer, budget_s):
+    import oracle
+
+    run, nbytes, frac, sample = calibrated_oracle(layer, budget_s)
+    t0 = time.perf_counter()
+    run()
+    dt = time.perf_counter() - t0
+    return {"value": round(nbytes / dt / 1e9, 3), "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    import oracle
+    from transformer_layer_non_gb300 import synth
+
+    layer = synth.LAYERS[args.workload]
+    per_step = max(0.5, min(2.0, 90.0 / (args.steps + args.warmup)))
+    run, nbytes, frac, sample = calibrated_oracle(layer, per_step, args.seed)
+    for _ in range(args.warmup):
+        run()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        run()
+    dt = time.perf_counter() - t0
+    value = nbytes * args.steps / dt / 1e9
+    tokens = layer.tokens * frac * args.steps / dt
+    line = {
+        "impl": "reference", "metric": METRIC, "value": round(value, 3), "unit": UNIT,
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": layer.name, "tokens": layer.tokens, "hidden": layer.hidden,
+                   "ffn": layer.ffn, "heads": layer.heads, "seq_len": layer.seq,
+                   "storage": layer.dtype, "sample_fraction": round(frac, 5)},
+        "tokens_per_s": round(tokens, 1),
+        "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return 0
+
+
+# ---------------------------------------------------------------------------
+# Our arm.
+# ---------------------------------------------------------------------------
+def run_ours(args):
+    import torch
+
+    from transformer_layer_non_gb300 import ls_ops, synth
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+    ls_ops.load()
+    layer = synth.LAYERS[args.workload]
+    step = LayerStep(layer, args.seed, device)
+    step_bytes = sum(step.bytes.values())
+    names = [n for n, _ in step.ops()]
+    graph, _ = capture(step, with_events=False)
+    try:
+        igraph, events = capture(step, with_events=True)
+    except TypeError:
+        igraph, events = None, None
+
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    t_busy0 = time.time()
+    for _ in range(args.warmup):
+        graph.replay()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(args.steps):
+        graph.replay()
+    e1.record()
+    torch.cuda.synchronize()
+    if pg:
+        pg.barrier()
+    ms = e0.elapsed_time(e1)
+    if pg:
+        t = torch.tensor([ms], device=device)
+        pg.all_reduce(t, op=pg.ReduceOp.MAX)
+        ms = float(t.item())
+    ms_step = ms / args.steps
+
+    # Per-operator device time: external event nodes inside the step graph,
+    # one replay at a time (the events of a replay bracket each operator).
+    per_op = {n: 0.0 for n in names}
+    n_inst = min(args.steps, 500)
+    if igraph is not None:
+        for _ in range(n_inst):
+            igraph.replay()
+            torch.cuda.synchronize()
+            for k, n in enumerate(names):
+                per_op[n] += events[k].elapsed_time(events[k + 1])
+        per_op = {n: v / n_inst for n, v in per_op.items()}
+    t_busy1 = time.time()
+
+    # End to end through the public API with host buffers: per step, copy every
+    # input from pinned host memory, run the step, copy every output back.
+    e2e_steps = min(args.steps, 50)
+    host_in = {k: v.cpu().pin_memory() for k, v in step.inp.items()}
+    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in step.out.items()}
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(v.numel() * v.element_size() for v in host_out.values())
+    for _ in range(3):
+        for k, v in host_in.items():
+            step.inp[k].copy_(v, non_blocking=True)
+        graph.replay()
+        for k, v in host_out.items():
+            v.copy_(step.out[k], non_blocking=True)
+    torch.cuda.synchronize()
+    f0 = torch.cuda.Event(enable_timing=True)
+    f1 = torch.cuda.Event(enable_timing=True)
+    f0.record()
+    for _ in range(e2e_steps):
+        for k, v in host_in.items():
+            step.inp[k].copy_(v, non_blocking=True)
+        graph.replay()
+        for k, v in host_out.items():
+            v.copy_(step.out[k], non_blocking=True)
+    f1.record()
+    torch.cuda.synchronize()
+    e2e_ms = f0.elapsed_time(f1) / e2e_steps
+    sampler.stop()
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    peak, peak_kind = load_peaks()
+    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    ops_report = {}
+    for n in names:
+        t_us = per_op[n] * 1e3 if igraph is not None else None
+        gbs = step.bytes[n] / (per_op[n] * 1e-3) / 1e9 if igraph is not None and per_op[n] > 0 else None
+        ops_report[n] = {"us": None if t_us is None else round(t_us, 2),
+                         "bytes": int(step.bytes[n]),
+                         "GB/s": None if gbs is None else round(gbs, 1),
+                         "frac": None if gbs is None else round(gbs / peak, 4)}
+    dominant = max(names, key=lambda n: per_op[n]) if igraph is not None else "softmax_bwd"
+    dom = ops_report[dominant]
+    roofline = {"bound": "hbm", "kernel": dominant,
+                "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
+                "frac": dom["frac"], "traffic": ncu_traffic(dominant, layer.name),
+                "algorithmic_bytes": dom["bytes"], "peak_source": f"{peak_kind} hbm_gbs (copy)"}
+    clocks = sampler.summary(t_busy0, t_busy1)
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16-storage/fp32-math" if layer.dtype == "f16" else "f32",
+        "data": "synthetic",
+        "config": {"workload": layer.name, "tokens": layer.tokens, "batch": layer.batch,
+                   "seq_len": layer.seq, "hidden": layer.hidden, "ffn": layer.ffn,
+                   "heads": layer.heads, "mask": "causal" if layer.causal else
+                   (f"padding U[{layer.pad_lo},{layer.seq}]" if layer.pad_lo else "none"),
+                   "dropout_p": layer.p, "storage": layer.dtype,
+                   "l2": f"inputs larger than L2: one step touches "
+                         f"{step.footprint_bytes() / 1e6:.0f} MB of distinct buffers "
+                         f"(L2 {L2_BYTES / 1e6:.0f} MB); no flush",
+                   "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
+        "pct_of_peak": round(value / world / peak * 100, 2),
+        "tokens_per_s": round(layer.tokens * world / (ms_step * 1e-3), 1),
+        "per_op": ops_report,
+        "roofline": roofline,
+        "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps},
+        "gpu_launches": int(sum(step.launches.values()) * args.steps),
+        "clocks": clocks,
+    }
+    if not args.no_cpu_baseline and world == 1:
+        line["cpu_baseline"] = cpu_baseline(layer, args.cpu_budget)
+    elif not args.no_cpu_baseline:
+        line["cpu_baseline"] = None
+    print(json.dumps(line), flush=True)
+    if args.details:
+        with open(args.details, "w") as f:
+            json.dump(line, f, indent=1)
+    if pg:
+        pg.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

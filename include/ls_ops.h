@@ -1,0 +1,171 @@
+/*
+ * ls_ops.h -- C ABI of the fused non-GEMM Transformer-layer operators for
+ * NVIDIA GB300 (sm_103a): bias+dropout+residual, bias+ReLU+dropout,
+ * LayerNorm and masked attention softmax, forward and backward.
+ *
+ * Where the operators come from (page title, section):
+ *  - "CMU 11-868 L10: accelerating the Transformer on GPUs (LightSeq)",
+ *    technique 1 "kernel fusion" (slide p.12): every non-GEMM step of the
+ *    layer is one fused kernel -- bias+dropout+residual, bias+ReLU+dropout,
+ *    and the LayerNorm and softmax reduce kernels; technique 2 "rewrite the
+ *    formula": LayerNorm statistics with one synchronisation (slide p.21), the
+ *    LayerNorm backward as two parallel sums (slide p.22), and the softmax
+ *    specialised by row length (slides p.23-26).
+ *  - "LightSeq2: Accelerated Training for Transformer-based Models on GPUs",
+ *    section 2.1.1 (fused bias+dropout+residual after self-attention) and
+ *    section 2.1.2 (the dropout mask saved in the forward pass and reused in
+ *    the backward pass).
+ *  - "CS336 Lecture 5: GPU", sections 6.1-6.2 (row softmax of the attention
+ *    scores, maximum subtracted).
+ *
+ * Conventions shared by every entry point
+ *  - Storage dtype is FP16 (LS_F16) or FP32 (LS_F32); arithmetic is FP32.
+ *    Parameters (bias, gamma, beta) and their gradients use the storage dtype;
+ *    LayerNorm statistics (mean, rstd) are FP32.
+ *  - Activations are row-major [rows, cols]; attention scores are row-major
+ *    [batch, heads, q_len, k_len].  cols (k_len) must be a multiple of 8.
+ *  - Every pointer is device memory owned by the caller and must be 16-byte
+ *    aligned.  The library allocates nothing, never synchronises, and keeps no
+ *    state except a per-thread error message.  Work is enqueued on `stream`
+ *    (a cudaStream_t; NULL is the legacy default stream) and the call returns
+ *    without waiting for it.
+ *  - An output may be the very same pointer as an input of the same shape (in
+ *    place); any other overlap between an output and another buffer is
+ *    rejected with LS_ERR_INVALID_ARGUMENT.
+ *  - Argument errors are returned before anything is enqueued.  A launch
+ *    failure returns LS_ERR_CUDA; faults during execution surface at the
+ *    caller's next synchronisation, as for any CUDA kernel.
+ *  - rows == 0 (or batch*heads*q_len == 0) is a no-op returning LS_OK.
+ *
+ * Dropout
+ *  - Drop probability p must satisfy 0 <= p < 1.  Kept values are scaled by
+ *    1/(1-p), computed in FP32.
+ *  - Element i (flat row-major index) draws the 32-bit word i & 3 of
+ *    Philox-4x32-10 (Salmon et al., SC'11) with key = (lo32(seed), hi32(seed))
+ *    and counter = (lo32(i>>2), hi32(i>>2), lo32(offset), hi32(offset)); it is
+ *    kept iff word >= floor(p * 2^32).  `offset` tells call sites apart.
+ *  - mask_bits holds ceil(rows*cols/32) uint32 words: element i is bit
+ *    (i & 31) of word (i >> 5); bits past the last element are written as 0.
+ *
+ * Column reductions (the bias, gamma and beta gradients)
+ *  - These are deterministic: per-tile FP32 partial sums go to `workspace`
+ *    and are then added in a fixed order.  Results are bitwise reproducible
+ *    for a given shape on any GPU.  The workspace is caller-owned device
+ *    memory of at least ls_colreduce_workspace_bytes(rows, cols) bytes; its
+ *    contents need no initialisation and are scratch after the call.  Two
+ *    calls that run concurrently must not share a workspace.
+ */
+#ifndef LS_OPS_H
+#define LS_OPS_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    LS_OK = 0,
+    LS_ERR_INVALID_ARGUMENT = 1,   /* NULL required pointer, bad p/eps, negative size, overlap */
+    LS_ERR_MISALIGNED = 2,         /* pointer not 16-byte aligned, or cols % 8 != 0 */
+    LS_ERR_UNSUPPORTED_SHAPE = 3,  /* LayerNorm cols > 16384, softmax k_len > 16384, too many elements */
+    LS_ERR_WORKSPACE_TOO_SMALL = 4,
+    LS_ERR_CUDA = 5                /* a CUDA call or kernel launch failed; see ls_last_error() */
+} ls_status;
+
+typedef enum { LS_F32 = 0, LS_F16 = 1 } ls_dtype;
+
+/* Static description of a status code. */
+const char* ls_status_string(ls_status status);
+/* Message of the last failing call on this host thread ("" if none). */
+const char* ls_last_error(void);
+/* Library version, major*10000 + minor*100 + patch. */
+int ls_version(void);
+
+/* Workspace bytes that the backward calls with a column reduction
+ * (ls_bias_dropout_residual_bwd, ls_bias_relu_dropout_bwd, ls_layernorm_bwd)
+ * need for an activation of shape [rows, cols]; enough for all three. */
+size_t ls_colreduce_workspace_bytes(int64_t rows, int64_t cols);
+
+/* Fused bias + dropout + residual, forward ("CMU 11-868 L10 (LightSeq)",
+ * technique 1; "LightSeq2", section 2.1.1):
+ *   out[r,c] = residual[r,c] + keep(i) * (x[r,c] + bias[c]) / (1 - p),  i = r*cols + c.
+ * x, residual, out: [rows, cols]; bias: [cols]; mask_bits (nullable): keep bits.
+ * out may be x or residual (in place). */
+ls_status ls_bias_dropout_residual_fwd(ls_dtype dtype, void* out, uint32_t* mask_bits,
+                                       const void* x, const void* bias, const void* residual,
+                                       int64_t rows, int64_t cols, float p, uint64_t seed,
+                                       uint64_t offset, void* stream);
+
+/* Backward of the above ("LightSeq2", section 2.1.2: the saved mask is reused):
+ *   dx = keep * dout / (1 - p);  dbias[c] = sum_r dx[r,c];  d residual = dout
+ * (not written: the caller uses dout itself).  mask_bits == NULL draws the
+ * keep bits again from (seed, offset); otherwise seed and offset are ignored.
+ * dbias may be NULL (then no workspace is needed).  dx may be dout. */
+ls_status ls_bias_dropout_residual_bwd(ls_dtype dtype, void* dx, void* dbias, const void* dout,
+                                       const uint32_t* mask_bits, int64_t rows, int64_t cols,
+                                       float p, uint64_t seed, uint64_t offset, void* workspace,
+                                       size_t workspace_bytes, void* stream);
+
+/* Fused bias + ReLU + dropout, forward ("CMU 11-868 L10 (LightSeq)", technique 1):
+ *   z = x + bias[c];  bit(i) = (z > 0) and keep(i);  out = bit(i) * z / (1 - p).
+ * mask_bits is required: it stores bit(i), which is all the backward needs.
+ * ReLU(0) = 0 and its slope at 0 is 0.  out may be x. */
+ls_status ls_bias_relu_dropout_fwd(ls_dtype dtype, void* out, uint32_t* mask_bits, const void* x,
+                                   const void* bias, int64_t rows, int64_t cols, float p,
+                                   uint64_t seed, uint64_t offset, void* stream);
+
+/* Backward of the above:  dx = bit * dout / (1 - p);  dbias[c] = sum_r dx[r,c].
+ * dbias may be NULL.  dx may be dout. */
+ls_status ls_bias_relu_dropout_bwd(ls_dtype dtype, void* dx, void* dbias, const void* dout,
+                                   const uint32_t* mask_bits, int64_t rows, int64_t cols, float p,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
+/* LayerNorm forward ("CMU 11-868 L10 (LightSeq)", technique 2, slide p.21): one
+ * pass computes sum(x) and sum(x^2) together (one synchronisation), then
+ *   mean = mu(x),  var = max(mu(x^2) - mu(x)^2, 0),  rstd = 1/sqrt(var + eps),
+ *   y = gamma * (x - mean) * rstd + beta.
+ * (The sums are taken about the row's first element, which leaves the
+ * identity unchanged and avoids cancellation for rows with a large mean.)
+ * x, y: [rows, cols]; gamma, beta: [cols]; mean, rstd: FP32 [rows] (both
+ * nullable).  eps >= 0.  cols <= 16384.  y may be x. */
+ls_status ls_layernorm_fwd(ls_dtype dtype, void* y, float* mean, float* rstd, const void* x,
+                           const void* gamma, const void* beta, int64_t rows, int64_t cols,
+                           float eps, void* stream);
+
+/* LayerNorm backward ("CMU 11-868 L10 (LightSeq)", technique 2, slide p.22): per
+ * row the two sums A = sum_j g_j and C = sum_j g_j * xhat_j, g = gamma * dy,
+ * xhat = (x - mean) * rstd, are computed together (one synchronisation), then
+ *   dx = rstd * (g - A/cols - xhat * C/cols),
+ *   dgamma[c] = sum_r dy * xhat,  dbeta[c] = sum_r dy.
+ * mean and rstd are the forward's saved statistics.  dgamma and dbeta are
+ * both given or both NULL (then no workspace is needed).  dx may be dy or x. */
+ls_status ls_layernorm_bwd(ls_dtype dtype, void* dx, void* dgamma, void* dbeta, const void* dy,
+                           const void* x, const void* gamma, const float* mean, const float* rstd,
+                           int64_t rows, int64_t cols, void* workspace, size_t workspace_bytes,
+                           void* stream);
+
+/* Masked attention softmax over the last axis of [batch, heads, q_len, k_len]
+ * ("CMU 11-868 L10 (LightSeq)", slides p.23-26; "CS336 Lecture 5: GPU", 6.1-6.2).
+ * Entry (b, h, q, j) is valid iff j < clamp(key_len[b], 0, k_len) (key_len is a
+ * device int32 [batch] array, or NULL for no padding mask) and, if causal,
+ * j <= q + k_len - q_len.  On valid entries y = exp(x - m) / sum(exp(x - m)),
+ * m = max of the valid x; masked entries are written as exactly 0 and are
+ * not read; a row with no valid key is all zeros.  No 1/sqrt(d) scaling is
+ * applied (the score GEMM applies it).  k_len <= 16384.  y may be x. */
+ls_status ls_softmax_fwd(ls_dtype dtype, void* y, const void* x, int64_t batch, int64_t heads,
+                         int64_t q_len, int64_t k_len, const int32_t* key_len, int causal,
+                         void* stream);
+
+/* Softmax backward:  dx = y * (dy - sum_valid(y * dy)) on valid entries, 0 on
+ * masked ones (which are not read).  Same mask arguments as the forward.
+ * dx may be dy. */
+ls_status ls_softmax_bwd(ls_dtype dtype, void* dx, const void* y, const void* dy, int64_t batch,
+                         int64_t heads, int64_t q_len, int64_t k_len, const int32_t* key_len,
+                         int causal, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* LS_OPS_H */

@@ -1,0 +1,550 @@
+// layernorm.cu -- LayerNorm forward and backward ("CMU 11-868 L10 (LightSeq)",
+// technique 2 "rewrite the formula": slide p.21 computes mu(x) and mu(x^2)
+// together so sigma = sqrt(mu(x^2) - mu(x)^2) needs one synchronisation
+// instead of two; slide p.22 rewrites the backward as two independent sums
+// plus elementwise work; FP32 arithmetic on FP16 storage).
+//
+// Row mapping.  Rows of up to 2048 elements are held in registers by a group
+// of LPR lanes (LPR = 1..32, VPT 8-element vectors per lane); a CTA of 256
+// threads holds 256/LPR rows.  Longer rows (up to 16384) use a whole CTA per
+// row.  Each lane owns the same columns in every row it visits, so the
+// backward's gamma/beta gradient partial sums never leave the SM until the
+// CTA has finished its rows.
+#include <algorithm>
+
+#include "ls_device.cuh"
+#include "ls_internal.h"
+
+namespace ls {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kCtaRowThreshold = 256;  // vectors per row held by one warp at most
+
+// ----------------------------------------------------------------------------
+// Forward, group-per-row.
+// ----------------------------------------------------------------------------
+template <typename T, int LPR, int VPT>
+__global__ void __launch_bounds__(kThreads)
+ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, const T* x,
+                    const T* __restrict__ gamma, const T* __restrict__ beta, int64_t rows,
+                    int cols, float eps) {
+    constexpr int RPC = kThreads / LPR;
+    const int gl = threadIdx.x % LPR;
+    const int64_t r = static_cast<int64_t>(blockIdx.x) * RPC + threadIdx.x / LPR;
+    const bool row_ok = r < rows;
+    const int nvec = cols / kVec;
+    const T* xr = x + (row_ok ? r : 0) * cols;
+
+    float f[VPT][kVec];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+        if (row_ok && v < nvec) {
+            load8f<T>(xr + v * kVec, f[k]);
+        } else {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) f[k][j] = 0.f;
+        }
+    }
+    // Sums about the row's first element K (held by the group's lane 0):
+    // var = mu((x-K)^2) - mu(x-K)^2 is the same identity, without cancellation
+    // when |mean| >> std.
+    const float K = __shfl_sync(0xffffffffu, f[0][0], 0, LPR);
+    float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        if (row_ok && gl + k * LPR < nvec) {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float d = f[k][j] - K;
+                s.x += d;
+                s.y = fmaf(d, d, s.y);
+            }
+        }
+    }
+    s = group_sum2<LPR>(s);  // the single synchronisation
+    const float inv_n = 1.f / static_cast<float>(cols);
+    const float m1 = s.x * inv_n;
+    const float var = fmaxf(fmaf(-m1, m1, s.y * inv_n), 0.f);
+    const float rs = rsqrtf(var + eps);
+    if (!row_ok) return;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+        if (v < nvec) {
+            float g[kVec], b[kVec], o[kVec];
+            load8f<T>(gamma + v * kVec, g);
+            load8f<T>(beta + v * kVec, b);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) o[j] = fmaf((f[k][j] - K - m1) * rs, g[j], b[j]);
+            store8f<T>(y + r * cols + v * kVec, o);
+        }
+    }
+    if (gl == 0) {
+        if (mean) mean[r] = K + m1;
+        if (rstd) rstd[r] = rs;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Forward, CTA-per-row (rows longer than a warp holds).
+// ----------------------------------------------------------------------------
+template <typename T, int WARPS, int VPT>
+__global__ void __launch_bounds__(WARPS * 32)
+ln_fwd_cta_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, const T* x,
+                  const T* __restrict__ gamma, const T* __restrict__ beta, int cols, float eps) {
+    constexpr int NT = WARPS * 32;
+    const int64_t r = blockIdx.x;
+    const int nvec = cols / kVec;
+    const T* xr = x + r * cols;
+    const float K = static_cast<float>(xr[0]);
+    float f[VPT][kVec];
+    float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = threadIdx.x + k * NT;
+        if (v < nvec) {
+            load8f<T>(xr + v * kVec, f[k]);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const float d = f[k][j] - K;
+                s.x += d;
+                s.y = fmaf(d, d, s.y);
+            }
+        }
+    }
+    s = group_sum2<32>(s);
+    __shared__ float2 part[WARPS];
+    if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+    __syncthreads();  // the single synchronisation
+    s = make_float2(0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) {
+        s.x += part[w].x;
+        s.y += part[w].y;
+    }
+    const float inv_n = 1.f / static_cast<float>(cols);
+    const float m1 = s.x * inv_n;
+    const float var = fmaxf(fmaf(-m1, m1, s.y * inv_n), 0.f);
+    const float rs = rsqrtf(var + eps);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = threadIdx.x + k * NT;
+        if (v < nvec) {
+            float g[kVec], b[kVec], o[kVec];
+            load8f<T>(gamma + v * kVec, g);
+            load8f<T>(beta + v * kVec, b);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) o[j] = fmaf((f[k][j] - K - m1) * rs, g[j], b[j]);
+            store8f<T>(y + r * cols + v * kVec, o);
+        }
+    }
+    if (threadIdx.x == 0) {
+        if (mean) mean[r] = K + m1;
+        if (rstd) rstd[r] = rs;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Backward, group-per-row.  Per row, with g = gamma*dy and xh = (x-mean)*rstd,
+// the two sums A = sum g and C = sum g*xh are reduced together; then
+//   dx = rstd * (g - A/H - xh * C/H).
+// (The pages' second sum is sum gamma*dy*x; taking it about the saved mean and
+// scaled by rstd gives C = rstd*(B - mean*A), the same algebra.)
+// dgamma/dbeta partial sums accumulate in shared memory per row slot (each
+// slot's lanes own disjoint columns), and are summed over the slots in a fixed
+// order at the end into partial[blockIdx.x, 0:H] and [blockIdx.x, H:2H].
+// ----------------------------------------------------------------------------
+template <typename T, int LPR, int VPT>
+__global__ void __launch_bounds__(kThreads)
+ln_bwd_group_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
+                    const T* __restrict__ gamma, const float* __restrict__ mean,
+                    const float* __restrict__ rstd, int64_t rows, int cols, int steps) {
+    constexpr int RPC = kThreads / LPR;  // row slots per CTA
+    extern __shared__ __align__(16) float acc[];  // [RPC][2*cols] when partial != nullptr
+    const int gl = threadIdx.x % LPR;
+    const int slot = threadIdx.x / LPR;
+    const int nvec = cols / kVec;
+    const float inv_n = 1.f / static_cast<float>(cols);
+    float* my_acc = acc + static_cast<size_t>(slot) * 2 * cols;
+
+    if (partial) {
+        for (int k = gl; k < 2 * cols; k += LPR) my_acc[k] = 0.f;
+    }
+    float gm[VPT][kVec];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+        if (v < nvec) load8f<T>(gamma + v * kVec, gm[k]);
+    }
+
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * RPC * steps;
+    for (int st = 0; st < steps; ++st) {
+        const int64_t r = base + static_cast<int64_t>(st) * RPC + slot;
+        const bool row_ok = r < rows;
+        Raw8<T> xr[VPT], dr[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = gl + k * LPR;
+            if (row_ok && v < nvec) {
+                xr[k] = load8<T>(x + r * cols + v * kVec);
+                dr[k] = load8<T>(dy + r * cols + v * kVec);
+            }
+        }
+        const float mu = row_ok ? mean[r] : 0.f;
+        const float rs = row_ok ? rstd[r] : 0.f;
+        float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            if (row_ok && gl + k * LPR < nvec) {
+                float xf[kVec], df[kVec];
+                unpack(xr[k], xf);
+                unpack(dr[k], df);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) {
+                    const float g = gm[k][j] * df[j];
+                    const float xh = (xf[j] - mu) * rs;
+                    s.x += g;
+                    s.y = fmaf(g, xh, s.y);
+                }
+            }
+        }
+        s = group_sum2<LPR>(s);  // the single synchronisation
+        const float a_n = s.x * inv_n;
+        const float c_n = s.y * inv_n;
+        if (!row_ok) continue;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = gl + k * LPR;
+            if (v < nvec) {
+                float xf[kVec], df[kVec], o[kVec];
+                unpack(xr[k], xf);
+                unpack(dr[k], df);
+                float xh[kVec];
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) {
+                    xh[j] = (xf[j] - mu) * rs;
+                    const float g = gm[k][j] * df[j];
+                    o[j] = rs * (g - a_n - xh[j] * c_n);
+                }
+                store8f<T>(dx + r * cols + v * kVec, o);
+                if (partial) {
+                    float4* pg = reinterpret_cast<float4*>(my_acc + v * kVec);
+                    float4* pb = reinterpret_cast<float4*>(my_acc + cols + v * kVec);
+                    float4 g0 = pg[0], g1 = pg[1], b0 = pb[0], b1 = pb[1];
+                    g0.x = fmaf(df[0], xh[0], g0.x); g0.y = fmaf(df[1], xh[1], g0.y);
+                    g0.z = fmaf(df[2], xh[2], g0.z); g0.w = fmaf(df[3], xh[3], g0.w);
+                    g1.x = fmaf(df[4], xh[4], g1.x); g1.y = fmaf(df[5], xh[5], g1.y);
+                    g1.z = fmaf(df[6], xh[6], g1.z); g1.w = fmaf(df[7], xh[7], g1.w);
+                    b0.x += df[0]; b0.y += df[1]; b0.z += df[2]; b0.w += df[3];
+                    b1.x += df[4]; b1.y += df[5]; b1.z += df[6]; b1.w += df[7];
+                    pg[0] = g0; pg[1] = g1; pb[0] = b0; pb[1] = b1;
+                }
+            }
+        }
+    }
+    if (partial == nullptr) return;
+    __syncthreads();
+    for (int k = threadIdx.x; k < 2 * cols; k += kThreads) {
+        float t = 0.f;
+        for (int q = 0; q < RPC; ++q) t += acc[static_cast<size_t>(q) * 2 * cols + k];
+        partial[static_cast<int64_t>(blockIdx.x) * 2 * cols + k] = t;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Backward, CTA-per-row.  Threads own disjoint columns, so the gradient
+// partial sums live in one [2*cols] shared array without conflicts.
+// ----------------------------------------------------------------------------
+template <typename T, int WARPS, int VPT>
+__global__ void __launch_bounds__(WARPS * 32)
+ln_bwd_cta_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
+                  const T* __restrict__ gamma, const float* __restrict__ mean,
+                  const float* __restrict__ rstd, int64_t rows, int cols, int steps) {
+    constexpr int NT = WARPS * 32;
+    extern __shared__ __align__(16) float acc[];  // [2*cols]
+    __shared__ float2 part[WARPS];
+    const int nvec = cols / kVec;
+    const float inv_n = 1.f / static_cast<float>(cols);
+    if (partial)
+        for (int k = threadIdx.x; k < 2 * cols; k += NT) acc[k] = 0.f;
+    float gm[VPT][kVec];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = threadIdx.x + k * NT;
+        if (v < nvec) load8f<T>(gamma + v * kVec, gm[k]);
+    }
+    for (int st = 0; st < steps; ++st) {
+        const int64_t r = static_cast<int64_t>(blockIdx.x) * steps + st;
+        if (r >= rows) break;  // uniform across the CTA
+        Raw8<T> xr[VPT], dr[VPT];
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = threadIdx.x + k * NT;
+            if (v < nvec) {
+                xr[k] = load8<T>(x + r * cols + v * kVec);
+                dr[k] = load8<T>(dy + r * cols + v * kVec);
+            }
+        }
+        const float mu = mean[r];
+        const float rs = rstd[r];
+        float2 s = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            if (threadIdx.x + k * NT < nvec) {
+                float xf[kVec], df[kVec];
+                unpack(xr[k], xf);
+                unpack(dr[k], df);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) {
+                    const float g = gm[k][j] * df[j];
+                    s.x += g;
+                    s.y = fmaf(g, (xf[j] - mu) * rs, s.y);
+                }
+            }
+        }
+        s = group_sum2<32>(s);
+        __syncthreads();  // previous row's readers of part[] are done
+        if ((threadIdx.x & 31) == 0) part[threadIdx.x >> 5] = s;
+        __syncthreads();  // the single synchronisation of this row's sums
+        s = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int w = 0; w < WARPS; ++w) {
+            s.x += part[w].x;
+            s.y += part[w].y;
+        }
+        const float a_n = s.x * inv_n;
+        const float c_n = s.y * inv_n;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = threadIdx.x + k * NT;
+            if (v < nvec) {
+                float xf[kVec], df[kVec], o[kVec];
+                unpack(xr[k], xf);
+                unpack(dr[k], df);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) {
+                    const float xh = (xf[j] - mu) * rs;
+                    o[j] = rs * (gm[k][j] * df[j] - a_n - xh * c_n);
+                    if (partial) {
+                        acc[v * kVec + j] = fmaf(df[j], xh, acc[v * kVec + j]);
+                        acc[cols + v * kVec + j] += df[j];
+                    }
+                }
+                store8f<T>(dx + r * cols + v * kVec, o);
+            }
+        }
+    }
+    if (partial == nullptr) return;
+    __syncthreads();
+    for (int k = threadIdx.x; k < 2 * cols; k += NT)
+        partial[static_cast<int64_t>(blockIdx.x) * 2 * cols + k] = acc[k];
+}
+
+// ----------------------------------------------------------------------------
+// Dispatch.
+// ----------------------------------------------------------------------------
+int pow2_at_least(int n) {
+    int p = 1;
+    while (p < n) p <<= 1;
+    return p;
+}
+
+struct LnPlan {
+    bool cta;     // CTA per row
+    int lpr;      // group path: lanes per row
+    int vpt;      // vectors per lane
+    int warps;    // CTA path: warps per row
+    int64_t grid;
+    int steps;    // backward: rows (CTA path) or row steps (group path) per CTA
+};
+
+// Target number of backward CTAs: about two per SM on a 152-SM part.  It is a
+// constant, not the device's SM count, so that the partial sums -- and with
+// them the bits of dgamma/dbeta -- do not depend on which GPU runs the call.
+constexpr int64_t kBwdTargetCtas = 304;
+
+LnPlan plan_for(int64_t rows, int64_t cols, bool bwd) {
+    const int nvec = static_cast<int>(cols / kVec);
+    LnPlan p{};
+    if (nvec <= kCtaRowThreshold) {
+        p.cta = false;
+        if (nvec <= 32) {
+            p.lpr = pow2_at_least(nvec);
+            p.vpt = 1;
+        } else {
+            p.lpr = 32;
+            p.vpt = (nvec + 31) / 32;
+        }
+        const int64_t rpc = kThreads / p.lpr;
+        if (bwd) {
+            p.steps = static_cast<int>(std::max<int64_t>(1, (rows + rpc * kBwdTargetCtas - 1) /
+                                                                (rpc * kBwdTargetCtas)));
+            p.grid = (rows + rpc * p.steps - 1) / (rpc * p.steps);
+        } else {
+            p.steps = 1;
+            p.grid = (rows + rpc - 1) / rpc;
+        }
+    } else {
+        p.cta = true;
+        p.warps = nvec <= 512 ? 4 : 8;
+        p.vpt = (nvec + p.warps * 32 - 1) / (p.warps * 32);
+        if (bwd) {
+            p.steps = static_cast<int>(
+                std::max<int64_t>(1, (rows + kBwdTargetCtas - 1) / kBwdTargetCtas));
+            p.grid = (rows + p.steps - 1) / p.steps;
+        } else {
+            p.steps = 1;
+            p.grid = rows;
+        }
+    }
+    return p;
+}
+
+template <typename K>
+cudaError_t set_smem(K kernel, size_t bytes) {
+    if (bytes <= 48 * 1024) return cudaSuccess;
+    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                static_cast<int>(bytes));
+}
+
+template <typename T, int LPR, int VPT>
+cudaError_t fwd_group(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                      const void* beta, int64_t rows, int64_t cols, float eps, const LnPlan& p,
+                      cudaStream_t s) {
+    ln_fwd_group_kernel<T, LPR, VPT><<<static_cast<unsigned>(p.grid), kThreads, 0, s>>>(
+        static_cast<T*>(y), mean, rstd, static_cast<const T*>(x), static_cast<const T*>(gamma),
+        static_cast<const T*>(beta), rows, static_cast<int>(cols), eps);
+    return cudaGetLastError();
+}
+
+template <typename T, int WARPS, int VPT>
+cudaError_t fwd_cta(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                    const void* beta, int64_t rows, int64_t cols, float eps, const LnPlan& p,
+                    cudaStream_t s) {
+    ln_fwd_cta_kernel<T, WARPS, VPT><<<static_cast<unsigned>(p.grid), WARPS * 32, 0, s>>>(
+        static_cast<T*>(y), mean, rstd, static_cast<const T*>(x), static_cast<const T*>(gamma),
+        static_cast<const T*>(beta), static_cast<int>(cols), eps);
+    return cudaGetLastError();
+}
+
+template <typename T, int LPR, int VPT>
+cudaError_t bwd_group(void* dx, float* partial, const void* dy, const void* x, const void* gamma,
+                      const float* mean, const float* rstd, int64_t rows, int64_t cols,
+                      const LnPlan& p, cudaStream_t s) {
+    const size_t smem = partial ? static_cast<size_t>(kThreads / LPR) * 2 * cols * sizeof(float)
+                                : 0;
+    auto kern = ln_bwd_group_kernel<T, LPR, VPT>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(p.grid), kThreads, smem, s>>>(
+        static_cast<T*>(dx), partial, static_cast<const T*>(dy), static_cast<const T*>(x),
+        static_cast<const T*>(gamma), mean, rstd, rows, static_cast<int>(cols), p.steps);
+    return cudaGetLastError();
+}
+
+template <typename T, int WARPS, int VPT>
+cudaError_t bwd_cta(void* dx, float* partial, const void* dy, const void* x, const void* gamma,
+                    const float* mean, const float* rstd, int64_t rows, int64_t cols,
+                    const LnPlan& p, cudaStream_t s) {
+    const size_t smem = partial ? 2 * static_cast<size_t>(cols) * sizeof(float) : 0;
+    auto kern = ln_bwd_cta_kernel<T, WARPS, VPT>;
+    cudaError_t e = set_smem(kern, smem);
+    if (e != cudaSuccess) return e;
+    kern<<<static_cast<unsigned>(p.grid), WARPS * 32, smem, s>>>(
+        static_cast<T*>(dx), partial, static_cast<const T*>(dy), static_cast<const T*>(x),
+        static_cast<const T*>(gamma), mean, rstd, rows, static_cast<int>(cols), p.steps);
+    return cudaGetLastError();
+}
+
+// Expand a runtime (lpr, vpt) or (warps, vpt) into a template instance.
+#define LS_GROUP_CASES(FN, T, ...)                                       \
+    if (p.lpr < 32) {                                                    \
+        switch (p.lpr) {                                                 \
+            case 1: return FN<T, 1, 1>(__VA_ARGS__);                     \
+            case 2: return FN<T, 2, 1>(__VA_ARGS__);                     \
+            case 4: return FN<T, 4, 1>(__VA_ARGS__);                     \
+            case 8: return FN<T, 8, 1>(__VA_ARGS__);                     \
+            case 16: return FN<T, 16, 1>(__VA_ARGS__);                   \
+        }                                                                \
+    } else {                                                             \
+        switch (p.vpt) {                                                 \
+            case 1: return FN<T, 32, 1>(__VA_ARGS__);                    \
+            case 2: return FN<T, 32, 2>(__VA_ARGS__);                    \
+            case 3: return FN<T, 32, 3>(__VA_ARGS__);                    \
+            case 4: return FN<T, 32, 4>(__VA_ARGS__);                    \
+            case 5: return FN<T, 32, 5>(__VA_ARGS__);                    \
+            case 6: return FN<T, 32, 6>(__VA_ARGS__);                    \
+            case 7: return FN<T, 32, 7>(__VA_ARGS__);                    \
+            case 8: return FN<T, 32, 8>(__VA_ARGS__);                    \
+        }                                                                \
+    }                                                                    \
+    return cudaErrorInvalidConfiguration;
+
+#define LS_CTA_CASES(FN, T, ...)                                         \
+    if (p.warps == 4) {                                                  \
+        switch (p.vpt) {                                                 \
+            case 3: return FN<T, 4, 3>(__VA_ARGS__);                     \
+            case 4: return FN<T, 4, 4>(__VA_ARGS__);                     \
+        }                                                                \
+    } else {                                                             \
+        switch (p.vpt) {                                                 \
+            case 3: return FN<T, 8, 3>(__VA_ARGS__);                     \
+            case 4: return FN<T, 8, 4>(__VA_ARGS__);                     \
+            case 5: return FN<T, 8, 5>(__VA_ARGS__);                     \
+            case 6: return FN<T, 8, 6>(__VA_ARGS__);                     \
+            case 7: return FN<T, 8, 7>(__VA_ARGS__);                     \
+            case 8: return FN<T, 8, 8>(__VA_ARGS__);                     \
+        }                                                                \
+    }                                                                    \
+    return cudaErrorInvalidConfiguration;
+
+template <typename T>
+cudaError_t fwd_dispatch(void* y, float* mean, float* rstd, const void* x, const void* gamma,
+                         const void* beta, int64_t rows, int64_t cols, float eps,
+                         cudaStream_t s) {
+    const LnPlan p = plan_for(rows, cols, false);
+    if (!p.cta) {
+        LS_GROUP_CASES(fwd_group, T, y, mean, rstd, x, gamma, beta, rows, cols, eps, p, s)
+    } else {
+        LS_CTA_CASES(fwd_cta, T, y, mean, rstd, x, gamma, beta, rows, cols, eps, p, s)
+    }
+}
+
+template <typename T>
+cudaError_t bwd_dispatch(void* dx, float* partial, const void* dy, const void* x,
+                         const void* gamma, const float* mean, const float* rstd, int64_t rows,
+                         int64_t cols, cudaStream_t s) {
+    const LnPlan p = plan_for(rows, cols, true);
+    if (!p.cta) {
+        LS_GROUP_CASES(bwd_group, T, dx, partial, dy, x, gamma, mean, rstd, rows, cols, p, s)
+    } else {
+        LS_CTA_CASES(bwd_cta, T, dx, partial, dy, x, gamma, mean, rstd, rows, cols, p, s)
+    }
+}
+
+}  // namespace
+
+ColReducePlan layernorm_bwd_plan(int64_t rows, int64_t cols) {
+    const LnPlan p = plan_for(rows, cols, true);
+    return ColReducePlan{p.grid, 2 * cols};
+}
+
+cudaError_t launch_layernorm_fwd(DType dt, void* y, float* mean, float* rstd, const void* x,
+                                 const void* gamma, const void* beta, int64_t rows, int64_t cols,
+                                 float eps, cudaStream_t s) {
+    if (dt == DType::F16)
+        return fwd_dispatch<__half>(y, mean, rstd, x, gamma, beta, rows, cols, eps, s);
+    return fwd_dispatch<float>(y, mean, rstd, x, gamma, beta, rows, cols, eps, s);
+}
+
+cudaError_t launch_layernorm_bwd(DType dt, void* dx, float* partial, const void* dy,
+                                 const void* x, const void* gamma, const float* mean,
+                                 const float* rstd, int64_t rows, int64_t cols, cudaStream_t s) {
+    if (dt == DType::F16)
+        return bwd_dispatch<__half>(dx, partial, dy, x, gamma, mean, rstd, rows, cols, s);
+    return bwd_dispatch<float>(dx, partial, dy, x, gamma, mean, rstd, rows, cols, s);
+}
+
+}  // namespace ls

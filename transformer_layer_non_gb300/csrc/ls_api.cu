@@ -1,0 +1,414 @@
+// ls_api.cu -- the C ABI declared in include/ls_ops.h.  Every entry point
+// validates its arguments on the host (returning before anything is enqueued
+// on an error), then hands the call to a launcher in ls_internal.h.  Nothing
+// here allocates, synchronises, or keeps state beyond the per-thread message
+// of the last error.
+#include <math.h>
+#include <stdarg.h>
+#include <stdio.h>
+#include <string.h>
+
+#include <algorithm>
+
+#include "../../include/ls_ops.h"
+#include "ls_internal.h"
+
+namespace {
+
+thread_local char g_last_error[512] = "";
+
+ls_status fail(ls_status st, const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+    return st;
+}
+
+ls_status ok() {
+    g_last_error[0] = '\0';
+    return LS_OK;
+}
+
+ls_status from_cuda(cudaError_t e, const char* what) {
+    if (e == cudaSuccess) return ok();
+    return fail(LS_ERR_CUDA, "%s: %s (%s)", what, cudaGetErrorName(e), cudaGetErrorString(e));
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// A byte range [p, p+n) of one argument.
+struct Span {
+    const char* name;
+    const void* p;
+    size_t n;
+};
+
+bool overlaps(const Span& a, const Span& b) {
+    if (!a.p || !b.p || a.n == 0 || b.n == 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + b.n && b0 < a0 + a.n;
+}
+
+// Outputs may coincide exactly with an input of the same size (in place);
+// every other overlap involving an output is an error.
+ls_status check_overlaps(const Span* outs, int nout, const Span* ins, int nin) {
+    for (int i = 0; i < nout; ++i) {
+        for (int j = i + 1; j < nout; ++j)
+            if (overlaps(outs[i], outs[j]))
+                return fail(LS_ERR_INVALID_ARGUMENT, "outputs %s and %s overlap", outs[i].name,
+                            outs[j].name);
+        for (int j = 0; j < nin; ++j) {
+            if (!overlaps(outs[i], ins[j])) continue;
+            if (outs[i].p == ins[j].p && outs[i].n == ins[j].n) continue;  // exact alias
+            return fail(LS_ERR_INVALID_ARGUMENT, "output %s partially overlaps input %s",
+                        outs[i].name, ins[j].name);
+        }
+    }
+    return LS_OK;
+}
+
+ls_status check_dtype(ls_dtype dt, ls::DType* out) {
+    if (dt == LS_F16) { *out = ls::DType::F16; return LS_OK; }
+    if (dt == LS_F32) { *out = ls::DType::F32; return LS_OK; }
+    return fail(LS_ERR_INVALID_ARGUMENT, "unknown dtype %d", static_cast<int>(dt));
+}
+
+size_t elem_size(ls::DType dt) { return dt == ls::DType::F16 ? 2 : 4; }
+
+// Common checks of a [rows, cols] activation.
+ls_status check_shape(int64_t rows, int64_t cols, int64_t max_cols) {
+    if (rows < 0) return fail(LS_ERR_INVALID_ARGUMENT, "rows = %lld < 0", (long long)rows);
+    if (cols <= 0) return fail(LS_ERR_INVALID_ARGUMENT, "cols = %lld <= 0", (long long)cols);
+    if (cols % 8 != 0)
+        return fail(LS_ERR_MISALIGNED, "cols = %lld is not a multiple of 8", (long long)cols);
+    if (cols > max_cols)
+        return fail(LS_ERR_UNSUPPORTED_SHAPE, "cols = %lld exceeds %lld", (long long)cols,
+                    (long long)max_cols);
+    // Keep every flat element index below 2^62 and every grid dimension legal.
+    if (rows > (int64_t{1} << 40) || rows * cols > (int64_t{1} << 46))
+        return fail(LS_ERR_UNSUPPORTED_SHAPE, "too many elements (%lld x %lld)", (long long)rows,
+                    (long long)cols);
+    return LS_OK;
+}
+
+ls_status check_ptr(const void* p, const char* name, bool required) {
+    if (!p) {
+        if (required) return fail(LS_ERR_INVALID_ARGUMENT, "%s is NULL", name);
+        return LS_OK;
+    }
+    if (!aligned16(p)) return fail(LS_ERR_MISALIGNED, "%s is not 16-byte aligned", name);
+    return LS_OK;
+}
+
+ls_status check_p(float p, ls::DropoutRng* rng, uint64_t seed, uint64_t offset) {
+    if (!(p >= 0.f && p < 1.f))
+        return fail(LS_ERR_INVALID_ARGUMENT, "dropout probability p = %g is not in [0, 1)",
+                    static_cast<double>(p));
+    double t = floor(static_cast<double>(p) * 4294967296.0);
+    if (t > 4294967295.0) t = 4294967295.0;
+    rng->thr = static_cast<uint32_t>(t);
+    rng->scale = 1.0f / (1.0f - p);
+    rng->seed = seed;
+    rng->offset = offset;
+    return LS_OK;
+}
+
+size_t mask_bytes(int64_t rows, int64_t cols) {
+    return static_cast<size_t>((rows * cols + 31) / 32) * 4;
+}
+
+// Dropout ops accept any cols % 8 == 0 whose vector count fits a grid row.
+constexpr int64_t kMaxDropoutCols = int64_t{1} << 22;
+
+#define LS_TRY(expr)                         \
+    do {                                     \
+        ls_status _st = (expr);              \
+        if (_st != LS_OK) return _st;        \
+    } while (0)
+
+}  // namespace
+
+// The library is built with hidden visibility; only the C ABI is exported.
+#pragma GCC visibility push(default)
+extern "C" {
+
+const char* ls_status_string(ls_status status) {
+    switch (status) {
+        case LS_OK: return "LS_OK";
+        case LS_ERR_INVALID_ARGUMENT: return "LS_ERR_INVALID_ARGUMENT";
+        case LS_ERR_MISALIGNED: return "LS_ERR_MISALIGNED";
+        case LS_ERR_UNSUPPORTED_SHAPE: return "LS_ERR_UNSUPPORTED_SHAPE";
+        case LS_ERR_WORKSPACE_TOO_SMALL: return "LS_ERR_WORKSPACE_TOO_SMALL";
+        case LS_ERR_CUDA: return "LS_ERR_CUDA";
+    }
+    return "unknown ls_status";
+}
+
+const char* ls_last_error(void) { return g_last_error; }
+
+int ls_version(void) { return 10000; }
+
+size_t ls_colreduce_workspace_bytes(int64_t rows, int64_t cols) {
+    if (rows <= 0 || cols <= 0 || cols % 8 != 0) return 0;
+    const size_t a = ls::dropout_bwd_plan(rows, cols).bytes();
+    const size_t b = cols <= ls::kMaxRowLen ? ls::layernorm_bwd_plan(rows, cols).bytes() : 0;
+    return std::max(a, b);
+}
+
+ls_status ls_bias_dropout_residual_fwd(ls_dtype dtype, void* out, uint32_t* mask_bits,
+                                       const void* x, const void* bias, const void* residual,
+                                       int64_t rows, int64_t cols, float p, uint64_t seed,
+                                       uint64_t offset, void* stream) {
+    ls::DType dt;
+    LS_TRY(check_dtype(dtype, &dt));
+    LS_TRY(check_shape(rows, cols, kMaxDropoutCols));
+    ls::DropoutRng rng;
+    LS_TRY(check_p(p, &rng, seed, offset));
+    if (rows == 0) return ok();
+    LS_TRY(check_ptr(out, "out", true));
+    LS_TRY(check_ptr(mask_bits, "mask_bits", false));
+    LS_TRY(check_ptr(x, "x", true));
+    LS_TRY(check_ptr(bias, "bias", true));
+    LS_TRY(check_ptr(residual, "residual", true));
+    const size_t nb = static_cast<size_t>(rows * cols) * elem_size(dt);
+    const Span outs[] = {{"out", out, nb}, {"mask_bits", mask_bits, mask_bytes(rows, cols)}};
+    const Span ins[] = {{"x", x, nb}, {"residual", residual, nb},
+                        {"bias", bias, static_cast<size_t>(cols) * elem_size(dt)}};
+    LS_TRY(check_overlaps(outs, 2, ins, 3));
+    return from_cuda(ls::launch_dropout_fwd(dt, false, out, reinterpret_cast<uint8_t*>(mask_bits),
+                                            x, bias, residual, rows, cols, rng,
+                                            static_cast<cudaStream_t>(stream)),
+                     "ls_bias_dropout_residual_fwd launch");
+}
+
+static ls_status dropout_bwd_common(const char* fn, ls_dtype dtype, void* dx, void* dbias,
+                                    const void* dout, const uint32_t* mask_bits, bool regen_ok,
+                                    int64_t rows, int64_t cols, float p, uint64_t seed,
+                                    uint64_t offset, void* workspace, size_t workspace_bytes,
+                                    void* stream) {
+    ls::DType dt;
+    LS_TRY(check_dtype(dtype, &dt));
+    LS_TRY(check_shape(rows, cols, kMaxDropoutCols));
+    ls::DropoutRng rng;
+    LS_TRY(check_p(p, &rng, seed, offset));
+    if (rows == 0) {
+        // The bias gradient of an empty batch is zero.
+        if (dbias) {
+            LS_TRY(check_ptr(dbias, "dbias", true));
+            return from_cuda(cudaMemsetAsync(dbias, 0, static_cast<size_t>(cols) * elem_size(dt),
+                                             static_cast<cudaStream_t>(stream)),
+                             fn);
+        }
+        return ok();
+    }
+    LS_TRY(check_ptr(dx, "dx", true));
+    LS_TRY(check_ptr(dbias, "dbias", false));
+    LS_TRY(check_ptr(dout, "dout", true));
+    LS_TRY(check_ptr(mask_bits, "mask_bits", !regen_ok));
+    const ls::ColReducePlan plan = ls::dropout_bwd_plan(rows, cols);
+    if (dbias) {
+        LS_TRY(check_ptr(workspace, "workspace", true));
+        if (workspace_bytes < plan.bytes())
+            return fail(LS_ERR_WORKSPACE_TOO_SMALL, "%s: workspace of %zu bytes, need %zu", fn,
+                        workspace_bytes, plan.bytes());
+    }
+    const size_t nb = static_cast<size_t>(rows * cols) * elem_size(dt);
+    const size_t bb = static_cast<size_t>(cols) * elem_size(dt);
+    const Span outs[] = {{"dx", dx, nb}, {"dbias", dbias, bb},
+                         {"workspace", dbias ? workspace : nullptr, plan.bytes()}};
+    const Span ins[] = {{"dout", dout, nb}, {"mask_bits", mask_bits, mask_bytes(rows, cols)}};
+    LS_TRY(check_overlaps(outs, 3, ins, 2));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    float* partial = dbias ? static_cast<float*>(workspace) : nullptr;
+    cudaError_t e = ls::launch_dropout_bwd(dt, dx, partial, dout,
+                                           reinterpret_cast<const uint8_t*>(mask_bits), rows,
+                                           cols, rng, s);
+    if (e == cudaSuccess && dbias)
+        e = ls::launch_colreduce(dt, dbias, nullptr, cols, partial, plan.parts, cols, s);
+    return from_cuda(e, fn);
+}
+
+ls_status ls_bias_dropout_residual_bwd(ls_dtype dtype, void* dx, void* dbias, const void* dout,
+                                       const uint32_t* mask_bits, int64_t rows, int64_t cols,
+                                       float p, uint64_t seed, uint64_t offset, void* workspace,
+                                       size_t workspace_bytes, void* stream) {
+    return dropout_bwd_common("ls_bias_dropout_residual_bwd", dtype, dx, dbias, dout, mask_bits,
+                              true, rows, cols, p, seed, offset, workspace, workspace_bytes,
+                              stream);
+}
+
+ls_status ls_bias_relu_dropout_fwd(ls_dtype dtype, void* out, uint32_t* mask_bits, const void* x,
+                                   const void* bias, int64_t rows, int64_t cols, float p,
+                                   uint64_t seed, uint64_t offset, void* stream) {
+    ls::DType dt;
+    LS_TRY(check_dtype(dtype, &dt));
+    LS_TRY(check_shape(rows, cols, kMaxDropoutCols));
+    ls::DropoutRng rng;
+    LS_TRY(check_p(p, &rng, seed, offset));
+    if (rows == 0) return ok();
+    LS_TRY(check_ptr(out, "out", true));
+    LS_TRY(check_ptr(mask_bits, "mask_bits", true));
+    LS_TRY(check_ptr(x, "x", true));
+    LS_TRY(check_ptr(bias, "bias", true));
+    const size_t nb = static_cast<size_t>(rows * cols) * elem_size(dt);
+    const Span outs[] = {{"out", out, nb}, {"mask_bits", mask_bits, mask_bytes(rows, cols)}};
+    const Span ins[] = {{"x", x, nb}, {"bias", bias, static_cast<size_t>(cols) * elem_size(dt)}};
+    LS_TRY(check_overlaps(outs, 2, ins, 2));
+    return from_cuda(ls::launch_dropout_fwd(dt, true, out, reinterpret_cast<uint8_t*>(mask_bits),
+                                            x, bias, nullptr, rows, cols, rng,
+                                            static_cast<cudaStream_t>(stream)),
+                     "ls_bias_relu_dropout_fwd launch");
+}
+
+ls_status ls_bias_relu_dropout_bwd(ls_dtype dtype, void* dx, void* dbias, const void* dout,
+                                   const uint32_t* mask_bits, int64_t rows, int64_t cols, float p,
+                                   void* workspace, size_t workspace_bytes, void* stream) {
+    return dropout_bwd_common("ls_bias_relu_dropout_bwd", dtype, dx, dbias, dout, mask_bits,
+                              false, rows, cols, p, 0, 0, workspace, workspace_bytes, stream);
+}
+
+ls_status ls_layernorm_fwd(ls_dtype dtype, void* y, float* mean, float* rstd, const void* x,
+                           const void* gamma, const void* beta, int64_t rows, int64_t cols,
+                           float eps, void* stream) {
+    ls::DType dt;
+    LS_TRY(check_dtype(dtype, &dt));
+    LS_TRY(check_shape(rows, cols, ls::kMaxRowLen));
+    if (!(eps >= 0.f) || isinf(eps))
+        return fail(LS_ERR_INVALID_ARGUMENT, "eps = %g must be finite and >= 0",
+                    static_cast<double>(eps));
+    if (rows == 0) return ok();
+    LS_TRY(check_ptr(y, "y", true));
+    LS_TRY(check_ptr(mean, "mean", false));
+    LS_TRY(check_ptr(rstd, "rstd", false));
+    LS_TRY(check_ptr(x, "x", true));
+    LS_TRY(check_ptr(gamma, "gamma", true));
+    LS_TRY(check_ptr(beta, "beta", true));
+    const size_t nb = static_cast<size_t>(rows * cols) * elem_size(dt);
+    const size_t pb = static_cast<size_t>(cols) * elem_size(dt);
+    const size_t sb = static_cast<size_t>(rows) * sizeof(float);
+    const Span outs[] = {{"y", y, nb}, {"mean", mean, sb}, {"rstd", rstd, sb}};
+    const Span ins[] = {{"x", x, nb}, {"gamma", gamma, pb}, {"beta", beta, pb}};
+    LS_TRY(check_overlaps(outs, 3, ins, 3));
+    return from_cuda(ls::launch_layernorm_fwd(dt, y, mean, rstd, x, gamma, beta, rows, cols, eps,
+                                              static_cast<cudaStream_t>(stream)),
+                     "ls_layernorm_fwd launch");
+}
+
+ls_status ls_layernorm_bwd(ls_dtype dtype, void* dx, void* dgamma, void* dbeta, const void* dy,
+                           const void* x, const void* gamma, const float* mean, const float* rstd,
+                           int64_t rows, int64_t cols, void* workspace, size_t workspace_bytes,
+                           void* stream) {
+    ls::DType dt;
+    LS_TRY(check_dtype(dtype, &dt));
+    LS_TRY(check_shape(rows, cols, ls::kMaxRowLen));
+    if ((dgamma == nullptr) != (dbeta == nullptr))
+        return fail(LS_ERR_INVALID_ARGUMENT, "dgamma and dbeta must both be given or both NULL");
+    const size_t pb = static_cast<size_t>(cols) * elem_size(dt);
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (rows == 0) {
+        if (dgamma) {
+            LS_TRY(check_ptr(dgamma, "dgamma", true));
+            LS_TRY(check_ptr(dbeta, "dbeta", true));
+            cudaError_t e = cudaMemsetAsync(dgamma, 0, pb, s);
+            if (e == cudaSuccess) e = cudaMemsetAsync(dbeta, 0, pb, s);
+            return from_cuda(e, "ls_layernorm_bwd");
+        }
+        return ok();
+    }
+    LS_TRY(check_ptr(dx, "dx", true));
+    LS_TRY(check_ptr(dgamma, "dgamma", false));
+    LS_TRY(check_ptr(dbeta, "dbeta", false));
+    LS_TRY(check_ptr(dy, "dy", true));
+    LS_TRY(check_ptr(x, "x", true));
+    LS_TRY(check_ptr(gamma, "gamma", true));
+    LS_TRY(check_ptr(mean, "mean", true));
+    LS_TRY(check_ptr(rstd, "rstd", true));
+    const ls::ColReducePlan plan = ls::layernorm_bwd_plan(rows, cols);
+    if (dgamma) {
+        LS_TRY(check_ptr(workspace, "workspace", true));
+        if (workspace_bytes < plan.bytes())
+            return fail(LS_ERR_WORKSPACE_TOO_SMALL, "ls_layernorm_bwd: workspace of %zu bytes, need %zu",
+                        workspace_bytes, plan.bytes());
+    }
+    const size_t nb = static_cast<size_t>(rows * cols) * elem_size(dt);
+    const size_t sb = static_cast<size_t>(rows) * sizeof(float);
+    const Span outs[] = {{"dx", dx, nb}, {"dgamma", dgamma, pb}, {"dbeta", dbeta, pb},
+                         {"workspace", dgamma ? workspace : nullptr, plan.bytes()}};
+    const Span ins[] = {{"dy", dy, nb},       {"x", x, nb},       {"gamma", gamma, pb},
+                        {"mean", mean, sb},   {"rstd", rstd, sb}};
+    LS_TRY(check_overlaps(outs, 4, ins, 5));
+    float* partial = dgamma ? static_cast<float*>(workspace) : nullptr;
+    cudaError_t e =
+        ls::launch_layernorm_bwd(dt, dx, partial, dy, x, gamma, mean, rstd, rows, cols, s);
+    if (e == cudaSuccess && dgamma) {
+        // Each partial row is [dgamma part | dbeta part]: one reduction of
+        // 2*cols columns, the first half to dgamma and the second to dbeta.
+        e = ls::launch_colreduce(dt, dgamma, dbeta, cols, partial, plan.parts, plan.width, s);
+    }
+    return from_cuda(e, "ls_layernorm_bwd launch");
+}
+
+static ls_status softmax_common(const char* fn, ls_dtype dtype, int64_t batch, int64_t heads,
+                                int64_t q_len, int64_t k_len, const int32_t* key_len,
+                                ls::DType* dt, int64_t* nrows) {
+    LS_TRY(check_dtype(dtype, dt));
+    if (batch < 0 || heads < 0 || q_len < 0)
+        return fail(LS_ERR_INVALID_ARGUMENT, "%s: negative batch/heads/q_len", fn);
+    if (k_len <= 0) return fail(LS_ERR_INVALID_ARGUMENT, "%s: k_len = %lld <= 0", fn, (long long)k_len);
+    if (k_len % 8 != 0)
+        return fail(LS_ERR_MISALIGNED, "%s: k_len = %lld is not a multiple of 8", fn, (long long)k_len);
+    if (k_len > ls::kMaxRowLen)
+        return fail(LS_ERR_UNSUPPORTED_SHAPE, "%s: k_len = %lld exceeds %lld", fn,
+                    (long long)k_len, (long long)ls::kMaxRowLen);
+    if (q_len > (int64_t{1} << 30) || batch > (int64_t{1} << 30) || heads > (int64_t{1} << 30))
+        return fail(LS_ERR_UNSUPPORTED_SHAPE, "%s: dimension too large", fn);
+    const double n = static_cast<double>(batch) * heads * q_len;
+    if (n * k_len > static_cast<double>(int64_t{1} << 46) || n > static_cast<double>(1u << 31) * 256)
+        return fail(LS_ERR_UNSUPPORTED_SHAPE, "%s: too many elements", fn);
+    *nrows = batch * heads * q_len;
+    if (key_len && (reinterpret_cast<uintptr_t>(key_len) & 3u))
+        return fail(LS_ERR_MISALIGNED, "%s: key_len is not 4-byte aligned", fn);
+    return LS_OK;
+}
+
+ls_status ls_softmax_fwd(ls_dtype dtype, void* y, const void* x, int64_t batch, int64_t heads,
+                         int64_t q_len, int64_t k_len, const int32_t* key_len, int causal,
+                         void* stream) {
+    ls::DType dt;
+    int64_t nrows;
+    LS_TRY(softmax_common("ls_softmax_fwd", dtype, batch, heads, q_len, k_len, key_len, &dt, &nrows));
+    if (nrows == 0) return ok();
+    LS_TRY(check_ptr(y, "y", true));
+    LS_TRY(check_ptr(x, "x", true));
+    const size_t nb = static_cast<size_t>(nrows * k_len) * elem_size(dt);
+    const Span outs[] = {{"y", y, nb}};
+    const Span ins[] = {{"x", x, nb}, {"key_len", key_len, static_cast<size_t>(batch) * 4}};
+    LS_TRY(check_overlaps(outs, 1, ins, 2));
+    const ls::SoftmaxShape sh{batch, heads, q_len, k_len, key_len, causal ? 1 : 0};
+    return from_cuda(ls::launch_softmax_fwd(dt, y, x, sh, static_cast<cudaStream_t>(stream)),
+                     "ls_softmax_fwd launch");
+}
+
+ls_status ls_softmax_bwd(ls_dtype dtype, void* dx, const void* y, const void* dy, int64_t batch,
+                         int64_t heads, int64_t q_len, int64_t k_len, const int32_t* key_len,
+                         int causal, void* stream) {
+    ls::DType dt;
+    int64_t nrows;
+    LS_TRY(softmax_common("ls_softmax_bwd", dtype, batch, heads, q_len, k_len, key_len, &dt, &nrows));
+    if (nrows == 0) return ok();
+    LS_TRY(check_ptr(dx, "dx", true));
+    LS_TRY(check_ptr(y, "y", true));
+    LS_TRY(check_ptr(dy, "dy", true));
+    const size_t nb = static_cast<size_t>(nrows * k_len) * elem_size(dt);
+    const Span outs[] = {{"dx", dx, nb}};
+    const Span ins[] = {{"y", y, nb}, {"dy", dy, nb},
+                        {"key_len", key_len, static_cast<size_t>(batch) * 4}};
+    LS_TRY(check_overlaps(outs, 1, ins, 3));
+    const ls::SoftmaxShape sh{batch, heads, q_len, k_len, key_len, causal ? 1 : 0};
+    return from_cuda(ls::launch_softmax_bwd(dt, dx, y, dy, sh, static_cast<cudaStream_t>(stream)),
+                     "ls_softmax_bwd launch");
+}
+
+}  // extern "C"
+#pragma GCC visibility pop

@@ -1,0 +1,172 @@
+// ls_device.cuh -- device building blocks shared by the operator kernels:
+// 8-element vector I/O (one 16-byte access for FP16, two for FP32), FP32
+// conversion in registers, the Philox-4x32-10 counter-based generator, and
+// shuffle reductions over a group of lanes.
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace ls {
+
+constexpr int kVec = 8;  // elements per vector access, both dtypes
+
+// ---------------------------------------------------------------------------
+// 8-element vectors.  Raw8<T> keeps the loaded bits (4 registers for FP16,
+// 8 for FP32) so that many loads can be in flight before any conversion.
+// ---------------------------------------------------------------------------
+template <typename T> struct Raw8;
+template <> struct Raw8<__half> { uint4 v; };
+template <> struct Raw8<float> { float4 a, b; };
+
+__device__ __forceinline__ uint4 ld16(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+// Streaming load for data read exactly once (evict-first in L1/L2).
+__device__ __forceinline__ uint4 ld16_stream(const void* p) {
+    uint4 r;
+    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
+    return r;
+}
+__device__ __forceinline__ void st16(void* p, uint4 v) {
+    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
+                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ uint4 f2u4(float4 f) {
+    return make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z),
+                      __float_as_uint(f.w));
+}
+__device__ __forceinline__ float4 u2f4(uint4 u) {
+    return make_float4(__uint_as_float(u.x), __uint_as_float(u.y), __uint_as_float(u.z),
+                       __uint_as_float(u.w));
+}
+
+template <typename T> __device__ __forceinline__ Raw8<T> load8(const T* p);
+template <> __device__ __forceinline__ Raw8<__half> load8<__half>(const __half* p) {
+    return Raw8<__half>{ld16(p)};
+}
+template <> __device__ __forceinline__ Raw8<float> load8<float>(const float* p) {
+    return Raw8<float>{u2f4(ld16(p)), u2f4(ld16(p + 4))};
+}
+
+template <typename T> __device__ __forceinline__ void store8(T* p, const Raw8<T>& r);
+template <> __device__ __forceinline__ void store8<__half>(__half* p, const Raw8<__half>& r) {
+    st16(p, r.v);
+}
+template <> __device__ __forceinline__ void store8<float>(float* p, const Raw8<float>& r) {
+    st16(p, f2u4(r.a));
+    st16(p + 4, f2u4(r.b));
+}
+
+__device__ __forceinline__ float2 h2f(uint32_t u) {
+    __half2 h = *reinterpret_cast<__half2*>(&u);
+    return __half22float2(h);
+}
+__device__ __forceinline__ uint32_t f2h(float a, float b) {
+    __half2 h = __floats2half2_rn(a, b);  // round to nearest even
+    return *reinterpret_cast<uint32_t*>(&h);
+}
+
+__device__ __forceinline__ void unpack(const Raw8<__half>& r, float (&f)[8]) {
+    float2 t;
+    t = h2f(r.v.x); f[0] = t.x; f[1] = t.y;
+    t = h2f(r.v.y); f[2] = t.x; f[3] = t.y;
+    t = h2f(r.v.z); f[4] = t.x; f[5] = t.y;
+    t = h2f(r.v.w); f[6] = t.x; f[7] = t.y;
+}
+__device__ __forceinline__ void unpack(const Raw8<float>& r, float (&f)[8]) {
+    f[0] = r.a.x; f[1] = r.a.y; f[2] = r.a.z; f[3] = r.a.w;
+    f[4] = r.b.x; f[5] = r.b.y; f[6] = r.b.z; f[7] = r.b.w;
+}
+template <typename T> __device__ __forceinline__ Raw8<T> pack(const float (&f)[8]);
+template <> __device__ __forceinline__ Raw8<__half> pack<__half>(const float (&f)[8]) {
+    return Raw8<__half>{make_uint4(f2h(f[0], f[1]), f2h(f[2], f[3]), f2h(f[4], f[5]),
+                                   f2h(f[6], f[7]))};
+}
+template <> __device__ __forceinline__ Raw8<float> pack<float>(const float (&f)[8]) {
+    return Raw8<float>{make_float4(f[0], f[1], f[2], f[3]), make_float4(f[4], f[5], f[6], f[7])};
+}
+
+template <typename T> __device__ __forceinline__ void load8f(const T* p, float (&f)[8]) {
+    unpack(load8<T>(p), f);
+}
+template <typename T> __device__ __forceinline__ void store8f(T* p, const float (&f)[8]) {
+    store8<T>(p, pack<T>(f));
+}
+
+// ---------------------------------------------------------------------------
+// Philox-4x32-10 (Salmon, Moraes, Dror, Shaw, SC'11).  One call maps a
+// 128-bit counter and a 64-bit key to 128 random bits.  Round: with the two
+// 32x32->64 products M0*c0 and M1*c2,
+//   c <- (hi(M1*c2) ^ c1 ^ k0, lo(M1*c2), hi(M0*c0) ^ c3 ^ k1, lo(M0*c0)),
+// and the key is bumped by the Weyl constants between rounds.
+// ---------------------------------------------------------------------------
+struct PhiloxKey {
+    uint32_t k0, k1;
+};
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+    constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
+    uint32_t k0 = key.k0, k1 = key.k1;
+#pragma unroll
+    for (int round = 0; round < 10; ++round) {
+        const uint64_t p0 = static_cast<uint64_t>(M0) * c.x;
+        const uint64_t p1 = static_cast<uint64_t>(M1) * c.z;
+        c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
+                       static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
+        k0 += W0;
+        k1 += W1;
+    }
+    return c;
+}
+
+// Dropout keep bits of the 8 consecutive elements starting at flat index i
+// (i a multiple of 4): element i+j draws word j&3 of counter block (i>>2)+(j>>2).
+// Bit j of the result is set iff element i+j is kept (word >= thr).
+__device__ __forceinline__ uint32_t keep_bits8(uint64_t i, uint32_t thr, PhiloxKey key,
+                                               uint32_t off_lo, uint32_t off_hi) {
+    const uint64_t blk = i >> 2;
+    const uint4 a = philox4x32_10(
+        make_uint4(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), off_lo, off_hi),
+        key);
+    const uint64_t blk1 = blk + 1;
+    const uint4 b = philox4x32_10(
+        make_uint4(static_cast<uint32_t>(blk1), static_cast<uint32_t>(blk1 >> 32), off_lo, off_hi),
+        key);
+    return (a.x >= thr ? 1u : 0u) | (a.y >= thr ? 2u : 0u) | (a.z >= thr ? 4u : 0u) |
+           (a.w >= thr ? 8u : 0u) | (b.x >= thr ? 16u : 0u) | (b.y >= thr ? 32u : 0u) |
+           (b.z >= thr ? 64u : 0u) | (b.w >= thr ? 128u : 0u);
+}
+
+// ---------------------------------------------------------------------------
+// Reductions over groups of W consecutive lanes (W a power of two <= 32).
+// ---------------------------------------------------------------------------
+template <int W> __device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
+}
+template <int W> __device__ __forceinline__ float group_max(float v) {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    return v;
+}
+// Both members of the pair reduced with one exchange per step: the single
+// synchronisation point of the one-pass statistics.
+template <int W> __device__ __forceinline__ float2 group_sum2(float2 v) {
+#pragma unroll
+    for (int o = W / 2; o > 0; o >>= 1) {
+        v.x += __shfl_xor_sync(0xffffffffu, v.x, o);
+        v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
+    }
+    return v;
+}
+
+}  // namespace ls

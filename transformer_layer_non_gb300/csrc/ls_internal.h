@@ -1,0 +1,65 @@
+// ls_internal.h -- launchers behind the C ABI.  Arguments reaching these
+// functions have been validated by ls_api.cu; each launcher only picks a
+// kernel instance and grid for the shape and enqueues it on the stream.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+namespace ls {
+
+enum class DType { F32 = 0, F16 = 1 };
+
+struct DropoutRng {
+    uint32_t thr;       // keep iff Philox word >= thr
+    float scale;        // 1 / (1 - p) in FP32
+    uint64_t seed;
+    uint64_t offset;
+};
+
+// Column-reduction plan shared by the launchers and the workspace query.
+// Partial sums are FP32 [parts, width]; `parts` depends only on the shape, so
+// results are bitwise reproducible on any GPU.
+struct ColReducePlan {
+    int64_t parts;
+    int64_t width;
+    size_t bytes() const { return static_cast<size_t>(parts * width) * sizeof(float); }
+};
+ColReducePlan dropout_bwd_plan(int64_t rows, int64_t cols);
+ColReducePlan layernorm_bwd_plan(int64_t rows, int64_t cols);
+
+// Sum `parts` FP32 rows of `width` columns in a fixed order; columns
+// [0, split) go to out0[0..split) and columns [split, width) to
+// out1[0..width-split) (out1 may be null when split == width).
+cudaError_t launch_colreduce(DType dt, void* out0, void* out1, int64_t split,
+                             const float* partial, int64_t parts, int64_t width, cudaStream_t s);
+
+cudaError_t launch_dropout_fwd(DType dt, bool relu, void* out, uint8_t* mask, const void* x,
+                               const void* bias, const void* residual, int64_t rows, int64_t cols,
+                               const DropoutRng& rng, cudaStream_t s);
+// mask == nullptr: redraw keep bits from rng.  partial == nullptr: no bias gradient.
+cudaError_t launch_dropout_bwd(DType dt, void* dx, float* partial, const void* dout,
+                               const uint8_t* mask, int64_t rows, int64_t cols,
+                               const DropoutRng& rng, cudaStream_t s);
+
+cudaError_t launch_layernorm_fwd(DType dt, void* y, float* mean, float* rstd, const void* x,
+                                 const void* gamma, const void* beta, int64_t rows, int64_t cols,
+                                 float eps, cudaStream_t s);
+cudaError_t launch_layernorm_bwd(DType dt, void* dx, float* partial, const void* dy,
+                                 const void* x, const void* gamma, const float* mean,
+                                 const float* rstd, int64_t rows, int64_t cols, cudaStream_t s);
+
+struct SoftmaxShape {
+    int64_t batch, heads, q_len, k_len;
+    const int32_t* key_len;
+    int causal;
+};
+cudaError_t launch_softmax_fwd(DType dt, void* y, const void* x, const SoftmaxShape& sh,
+                               cudaStream_t s);
+cudaError_t launch_softmax_bwd(DType dt, void* dx, const void* y, const void* dy,
+                               const SoftmaxShape& sh, cudaStream_t s);
+
+constexpr int64_t kMaxRowLen = 16384;
+
+}  // namespace ls

@@ -1,0 +1,440 @@
+// softmax.cu -- masked attention softmax, forward and backward, specialised by
+// row length ("CMU 11-868 L10 (LightSeq)", slides p.23-26: the two dependent
+// reductions of the softmax -- row maximum, then sum of exponentials -- are
+// kept, and instead the number of lanes per row and elements per lane are
+// fixed at compile time for each row length and the right instance is picked
+// at call time; "CS336 Lecture 5: GPU", section 6.2: subtract the row maximum
+// before exponentiating).
+//
+// Row-length classes (k_len = 8 * nvec):
+//   nvec <= 32        LPR = next power of two >= nvec lanes per row, one
+//                     16-byte vector per lane; 256/LPR rows per 256-thread CTA
+//                     (k_len 16 -> 2 lanes/row, 128 rows per CTA).
+//   32 < nvec <= 128  a warp per row, VPT = 2..4 vectors per lane.
+//   nvec > 128        a CTA per row (4 or 8 warps), partial results of the two
+//                     reductions through shared memory.
+// Masked keys are never loaded: a lane loads a vector only if it holds at
+// least one valid key; masked outputs are written as exact zeros.
+#include <math.h>
+
+#include "ls_device.cuh"
+#include "ls_internal.h"
+
+namespace ls {
+namespace {
+
+constexpr int kThreads = 256;
+constexpr float kLog2e = 1.4426950408889634f;
+
+struct RowMask {
+    const int32_t* key_len;  // [batch] or nullptr
+    int64_t heads_q;         // heads * q_len
+    int q_len;
+    int shift;               // k_len - q_len (causal diagonal offset)
+    int causal;
+};
+
+// Number of leading valid keys of a row (0..k_len).
+__device__ __forceinline__ int valid_len(int64_t row, int k_len, const RowMask& m) {
+    int v = k_len;
+    if (m.key_len) {
+        const int64_t b = row / m.heads_q;
+        const int kl = m.key_len[b];
+        v = min(v, max(kl, 0));
+    }
+    if (m.causal) {
+        const int q = static_cast<int>(row % m.q_len);
+        v = min(v, max(q + m.shift + 1, 0));
+    }
+    return v;
+}
+
+// ----------------------------------------------------------------------------
+// Group-per-row kernels.
+// ----------------------------------------------------------------------------
+template <typename T, int LPR, int VPT>
+__global__ void __launch_bounds__(kThreads)
+softmax_fwd_group_kernel(T* y, const T* x, int64_t nrows, int k_len, RowMask mk) {
+    constexpr int RPC = kThreads / LPR;
+    const int gl = threadIdx.x % LPR;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * RPC + threadIdx.x / LPR;
+    const bool row_ok = row < nrows;
+    const int vlen = row_ok ? valid_len(row, k_len, mk) : 0;
+    const int nvec = k_len / kVec;
+    const int64_t base = (row_ok ? row : 0) * k_len;
+
+    float f[VPT][kVec];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+        if (v * kVec < vlen) {
+            load8f<T>(x + base + v * kVec, f[k]);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                if (v * kVec + j < vlen) m = fmaxf(m, f[k][j]);
+        }
+    }
+    m = group_max<LPR>(m);
+    const float ml = m * kLog2e;
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const bool on = v * kVec + j < vlen;
+            const float e = on ? exp2f(fmaf(f[k][j], kLog2e, -ml)) : 0.f;
+            f[k][j] = e;
+            s += e;
+        }
+    }
+    s = group_sum<LPR>(s);
+    const float inv = s > 0.f ? 1.f / s : 0.f;
+    if (!row_ok) return;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+        if (v < nvec) {
+            float o[kVec];
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) o[j] = f[k][j] * inv;  // masked: 0 * inv = 0
+            store8f<T>(y + base + v * kVec, o);
+        }
+    }
+}
+
+template <typename T, int LPR, int VPT>
+__global__ void __launch_bounds__(kThreads)
+softmax_bwd_group_kernel(T* dx, const T* y, const T* dy, int64_t nrows, int k_len, RowMask mk) {
+    constexpr int RPC = kThreads / LPR;
+    const int gl = threadIdx.x % LPR;
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * RPC + threadIdx.x / LPR;
+    const bool row_ok = row < nrows;
+    const int vlen = row_ok ? valid_len(row, k_len, mk) : 0;
+    const int nvec = k_len / kVec;
+    const int64_t base = (row_ok ? row : 0) * k_len;
+
+    Raw8<T> yr[VPT], dr[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+        if (v * kVec < vlen) {
+            yr[k] = load8<T>(y + base + v * kVec);
+            dr[k] = load8<T>(dy + base + v * kVec);
+        }
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+        if (v * kVec < vlen) {
+            float yf[kVec], df[kVec];
+            unpack(yr[k], yf);
+            unpack(dr[k], df);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                if (v * kVec + j < vlen) dot = fmaf(yf[j], df[j], dot);
+        }
+    }
+    dot = group_sum<LPR>(dot);
+    if (!row_ok) return;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+        if (v < nvec) {
+            float o[kVec];
+            if (v * kVec < vlen) {
+                float yf[kVec], df[kVec];
+                unpack(yr[k], yf);
+                unpack(dr[k], df);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j)
+                    o[j] = (v * kVec + j < vlen) ? yf[j] * (df[j] - dot) : 0.f;
+            } else {
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) o[j] = 0.f;
+            }
+            store8f<T>(dx + base + v * kVec, o);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// CTA-per-row kernels (k_len > 1024).
+// ----------------------------------------------------------------------------
+template <int WARPS>
+__device__ __forceinline__ float cta_max(float v, float* red) {
+    v = group_max<32>(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = red[0];
+#pragma unroll
+    for (int w = 1; w < WARPS; ++w) r = fmaxf(r, red[w]);
+    return r;
+}
+template <int WARPS>
+__device__ __forceinline__ float cta_sum(float v, float* red) {
+    v = group_sum<32>(v);
+    __syncthreads();
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    float r = 0.f;
+#pragma unroll
+    for (int w = 0; w < WARPS; ++w) r += red[w];
+    return r;
+}
+
+template <typename T, int WARPS, int VPT>
+__global__ void __launch_bounds__(WARPS * 32)
+softmax_fwd_cta_kernel(T* y, const T* x, int k_len, RowMask mk) {
+    constexpr int NT = WARPS * 32;
+    __shared__ float red[WARPS];
+    const int64_t row = blockIdx.x;
+    const int vlen = valid_len(row, k_len, mk);
+    const int nvec = k_len / kVec;
+    const int64_t base = row * k_len;
+    float f[VPT][kVec];
+    float m = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = threadIdx.x + k * NT;
+        if (v * kVec < vlen) {
+            load8f<T>(x + base + v * kVec, f[k]);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                if (v * kVec + j < vlen) m = fmaxf(m, f[k][j]);
+        }
+    }
+    m = cta_max<WARPS>(m, red);
+    const float ml = m * kLog2e;
+    float s = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = threadIdx.x + k * NT;
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) {
+            const bool on = v * kVec + j < vlen;
+            const float e = on ? exp2f(fmaf(f[k][j], kLog2e, -ml)) : 0.f;
+            f[k][j] = e;
+            s += e;
+        }
+    }
+    s = cta_sum<WARPS>(s, red);
+    const float inv = s > 0.f ? 1.f / s : 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = threadIdx.x + k * NT;
+        if (v < nvec) {
+            float o[kVec];
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) o[j] = f[k][j] * inv;
+            store8f<T>(y + base + v * kVec, o);
+        }
+    }
+}
+
+template <typename T, int WARPS, int VPT>
+__global__ void __launch_bounds__(WARPS * 32)
+softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk) {
+    constexpr int NT = WARPS * 32;
+    __shared__ float red[WARPS];
+    const int64_t row = blockIdx.x;
+    const int vlen = valid_len(row, k_len, mk);
+    const int nvec = k_len / kVec;
+    const int64_t base = row * k_len;
+    Raw8<T> yr[VPT], dr[VPT];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = threadIdx.x + k * NT;
+        if (v * kVec < vlen) {
+            yr[k] = load8<T>(y + base + v * kVec);
+            dr[k] = load8<T>(dy + base + v * kVec);
+        }
+    }
+    float dot = 0.f;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = threadIdx.x + k * NT;
+        if (v * kVec < vlen) {
+            float yf[kVec], df[kVec];
+            unpack(yr[k], yf);
+            unpack(dr[k], df);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                if (v * kVec + j < vlen) dot = fmaf(yf[j], df[j], dot);
+        }
+    }
+    dot = cta_sum<WARPS>(dot, red);
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = threadIdx.x + k * NT;
+        if (v < nvec) {
+            float o[kVec];
+            if (v * kVec < vlen) {
+                float yf[kVec], df[kVec];
+                unpack(yr[k], yf);
+                unpack(dr[k], df);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j)
+                    o[j] = (v * kVec + j < vlen) ? yf[j] * (df[j] - dot) : 0.f;
+            } else {
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) o[j] = 0.f;
+            }
+            store8f<T>(dx + base + v * kVec, o);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Dispatch by row length.
+// ----------------------------------------------------------------------------
+struct SmPlan {
+    bool cta;
+    int lpr, vpt, warps;
+    int64_t grid;
+};
+
+SmPlan plan_for(int64_t nrows, int64_t k_len) {
+    const int nvec = static_cast<int>(k_len / kVec);
+    SmPlan p{};
+    if (nvec <= 128) {
+        p.cta = false;
+        if (nvec <= 32) {
+            p.lpr = 1;
+            while (p.lpr < nvec) p.lpr <<= 1;
+            p.vpt = 1;
+        } else {
+            p.lpr = 32;
+            p.vpt = (nvec + 31) / 32;
+        }
+        const int64_t rpc = kThreads / p.lpr;
+        p.grid = (nrows + rpc - 1) / rpc;
+    } else {
+        p.cta = true;
+        p.warps = nvec <= 512 ? 4 : 8;
+        p.vpt = (nvec + p.warps * 32 - 1) / (p.warps * 32);
+        p.grid = nrows;
+    }
+    return p;
+}
+
+RowMask make_mask(const SoftmaxShape& sh) {
+    RowMask m;
+    m.key_len = sh.key_len;
+    m.heads_q = sh.heads * sh.q_len;
+    m.q_len = static_cast<int>(sh.q_len);
+    m.shift = static_cast<int>(sh.k_len - sh.q_len);
+    m.causal = sh.causal;
+    return m;
+}
+
+template <typename T, int LPR, int VPT>
+cudaError_t fwd_group(void* y, const void* x, int64_t nrows, int k_len, const RowMask& m,
+                      const SmPlan& p, cudaStream_t s) {
+    softmax_fwd_group_kernel<T, LPR, VPT><<<static_cast<unsigned>(p.grid), kThreads, 0, s>>>(
+        static_cast<T*>(y), static_cast<const T*>(x), nrows, k_len, m);
+    return cudaGetLastError();
+}
+template <typename T, int LPR, int VPT>
+cudaError_t bwd_group(void* dx, const void* y, const void* dy, int64_t nrows, int k_len,
+                      const RowMask& m, const SmPlan& p, cudaStream_t s) {
+    softmax_bwd_group_kernel<T, LPR, VPT><<<static_cast<unsigned>(p.grid), kThreads, 0, s>>>(
+        static_cast<T*>(dx), static_cast<const T*>(y), static_cast<const T*>(dy), nrows, k_len, m);
+    return cudaGetLastError();
+}
+template <typename T, int WARPS, int VPT>
+cudaError_t fwd_cta(void* y, const void* x, int64_t nrows, int k_len, const RowMask& m,
+                    const SmPlan& p, cudaStream_t s) {
+    softmax_fwd_cta_kernel<T, WARPS, VPT><<<static_cast<unsigned>(p.grid), WARPS * 32, 0, s>>>(
+        static_cast<T*>(y), static_cast<const T*>(x), k_len, m);
+    return cudaGetLastError();
+}
+template <typename T, int WARPS, int VPT>
+cudaError_t bwd_cta(void* dx, const void* y, const void* dy, int64_t nrows, int k_len,
+                    const RowMask& m, const SmPlan& p, cudaStream_t s) {
+    softmax_bwd_cta_kernel<T, WARPS, VPT><<<static_cast<unsigned>(p.grid), WARPS * 32, 0, s>>>(
+        static_cast<T*>(dx), static_cast<const T*>(y), static_cast<const T*>(dy), k_len, m);
+    return cudaGetLastError();
+}
+
+#define LS_SM_GROUP_CASES(FN, T, ...)                                    \
+    switch (p.lpr) {                                                     \
+        case 1: return FN<T, 1, 1>(__VA_ARGS__);                         \
+        case 2: return FN<T, 2, 1>(__VA_ARGS__);                         \
+        case 4: return FN<T, 4, 1>(__VA_ARGS__);                         \
+        case 8: return FN<T, 8, 1>(__VA_ARGS__);                         \
+        case 16: return FN<T, 16, 1>(__VA_ARGS__);                       \
+        case 32:                                                         \
+            switch (p.vpt) {                                             \
+                case 1: return FN<T, 32, 1>(__VA_ARGS__);                \
+                case 2: return FN<T, 32, 2>(__VA_ARGS__);                \
+                case 3: return FN<T, 32, 3>(__VA_ARGS__);                \
+                case 4: return FN<T, 32, 4>(__VA_ARGS__);                \
+            }                                                            \
+    }                                                                    \
+    return cudaErrorInvalidConfiguration;
+
+#define LS_SM_CTA_CASES(FN, T, ...)                                      \
+    if (p.warps == 4) {                                                  \
+        switch (p.vpt) {                                                 \
+            case 2: return FN<T, 4, 2>(__VA_ARGS__);                     \
+            case 3: return FN<T, 4, 3>(__VA_ARGS__);                     \
+            case 4: return FN<T, 4, 4>(__VA_ARGS__);                     \
+        }                                                                \
+    } else {                                                             \
+        switch (p.vpt) {                                                 \
+            case 3: return FN<T, 8, 3>(__VA_ARGS__);                     \
+            case 4: return FN<T, 8, 4>(__VA_ARGS__);                     \
+            case 5: return FN<T, 8, 5>(__VA_ARGS__);                     \
+            case 6: return FN<T, 8, 6>(__VA_ARGS__);                     \
+            case 7: return FN<T, 8, 7>(__VA_ARGS__);                     \
+            case 8: return FN<T, 8, 8>(__VA_ARGS__);                     \
+        }                                                                \
+    }                                                                    \
+    return cudaErrorInvalidConfiguration;
+
+template <typename T>
+cudaError_t fwd_dispatch(void* y, const void* x, const SoftmaxShape& sh, cudaStream_t s) {
+    const int64_t nrows = sh.batch * sh.heads * sh.q_len;
+    const int k_len = static_cast<int>(sh.k_len);
+    const SmPlan p = plan_for(nrows, sh.k_len);
+    const RowMask m = make_mask(sh);
+    if (!p.cta) {
+        LS_SM_GROUP_CASES(fwd_group, T, y, x, nrows, k_len, m, p, s)
+    } else {
+        LS_SM_CTA_CASES(fwd_cta, T, y, x, nrows, k_len, m, p, s)
+    }
+}
+
+template <typename T>
+cudaError_t bwd_dispatch(void* dx, const void* y, const void* dy, const SoftmaxShape& sh,
+                         cudaStream_t s) {
+    const int64_t nrows = sh.batch * sh.heads * sh.q_len;
+    const int k_len = static_cast<int>(sh.k_len);
+    const SmPlan p = plan_for(nrows, sh.k_len);
+    const RowMask m = make_mask(sh);
+    if (!p.cta) {
+        LS_SM_GROUP_CASES(bwd_group, T, dx, y, dy, nrows, k_len, m, p, s)
+    } else {
+        LS_SM_CTA_CASES(bwd_cta, T, dx, y, dy, nrows, k_len, m, p, s)
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_softmax_fwd(DType dt, void* y, const void* x, const SoftmaxShape& sh,
+                               cudaStream_t s) {
+    if (dt == DType::F16) return fwd_dispatch<__half>(y, x, sh, s);
+    return fwd_dispatch<float>(y, x, sh, s);
+}
+
+cudaError_t launch_softmax_bwd(DType dt, void* dx, const void* y, const void* dy,
+                               const SoftmaxShape& sh, cudaStream_t s) {
+    if (dt == DType::F16) return bwd_dispatch<__half>(dx, y, dy, sh, s);
+    return bwd_dispatch<float>(dx, y, dy, sh, s);
+}
+
+}  // namespace ls

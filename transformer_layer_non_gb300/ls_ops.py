@@ -1,0 +1,209 @@
+"""Thin Python binding of the ``ls_ops`` C ABI (``include/ls_ops.h``).
+
+Each function has the C entry point's name and argument order, takes torch
+CUDA tensors (or raw integers for pointers), and only marshals arguments:
+every step of every operator runs in the CUDA library.  There is no fallback:
+if the library cannot be built or loaded, importing this module's functions
+raises.  Work is enqueued on ``stream`` (default: torch's current stream) and
+nothing is synchronised.
+
+Status codes other than ``LS_OK`` raise :class:`LsError` carrying the code
+and the library's message.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional
+
+from . import build as _build
+
+LS_OK = 0
+LS_ERR_INVALID_ARGUMENT = 1
+LS_ERR_MISALIGNED = 2
+LS_ERR_UNSUPPORTED_SHAPE = 3
+LS_ERR_WORKSPACE_TOO_SMALL = 4
+LS_ERR_CUDA = 5
+
+LS_F32 = 0
+LS_F16 = 1
+
+# Every entry point declared in include/ls_ops.h.
+EXPORTS = (
+    "ls_status_string", "ls_last_error", "ls_version", "ls_colreduce_workspace_bytes",
+    "ls_bias_dropout_residual_fwd", "ls_bias_dropout_residual_bwd",
+    "ls_bias_relu_dropout_fwd", "ls_bias_relu_dropout_bwd",
+    "ls_layernorm_fwd", "ls_layernorm_bwd", "ls_softmax_fwd", "ls_softmax_bwd",
+)
+
+
+class LsError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{status_string(status)}: {message}")
+        self.status = status
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I64 = ctypes.c_int64
+_U64 = ctypes.c_uint64
+_F32 = ctypes.c_float
+_INT = ctypes.c_int
+_SZ = ctypes.c_size_t
+
+_SIGNATURES = {
+    "ls_status_string": (ctypes.c_char_p, [_INT]),
+    "ls_last_error": (ctypes.c_char_p, []),
+    "ls_version": (_INT, []),
+    "ls_colreduce_workspace_bytes": (_SZ, [_I64, _I64]),
+    "ls_bias_dropout_residual_fwd": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _F32, _U64, _U64, _P]),
+    "ls_bias_dropout_residual_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _F32, _U64, _U64, _P, _SZ, _P]),
+    "ls_bias_relu_dropout_fwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _F32, _U64, _U64, _P]),
+    "ls_bias_relu_dropout_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _F32, _P, _SZ, _P]),
+    "ls_layernorm_fwd": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _F32, _P]),
+    "ls_layernorm_bwd": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P]),
+    "ls_softmax_fwd": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
+    "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
+}
+
+
+def library_path() -> str:
+    return _build.LIB
+
+
+def load(build_if_needed: bool = True):
+    """Load libls_ops.so (building it first if it is missing or stale)."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    path = _build.build() if build_if_needed else _build.LIB
+    if not os.path.exists(path):
+        raise RuntimeError(f"libls_ops.so not found at {path}; build it with "
+                           "`python -m transformer_layer_non_gb300.build`")
+    lib = ctypes.CDLL(path)
+    for name, (res, args) in _SIGNATURES.items():
+        fn = getattr(lib, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = lib
+    return lib
+
+
+def status_string(status: int) -> str:
+    return load().ls_status_string(status).decode()
+
+
+def last_error() -> str:
+    return load().ls_last_error().decode()
+
+
+def version() -> int:
+    return load().ls_version()
+
+
+def colreduce_workspace_bytes(rows: int, cols: int) -> int:
+    return int(load().ls_colreduce_workspace_bytes(rows, cols))
+
+
+def _check(status: int):
+    if status != LS_OK:
+        raise LsError(status, last_error())
+
+
+# --- argument marshalling -------------------------------------------------
+def _ptr(t) -> Optional[int]:
+    """Device address of a tensor (or an int address, or None -> NULL)."""
+    if t is None:
+        return None
+    if isinstance(t, int):
+        return t
+    return t.data_ptr()
+
+
+def _dtype_code(t) -> int:
+    import torch
+
+    if t.dtype == torch.float16:
+        return LS_F16
+    if t.dtype == torch.float32:
+        return LS_F32
+    raise TypeError(f"unsupported storage dtype {t.dtype}; use float16 or float32")
+
+
+def _stream(stream) -> Optional[int]:
+    if stream is None:
+        import torch
+
+        return torch.cuda.current_stream().cuda_stream
+    if isinstance(stream, int):
+        return stream
+    return stream.cuda_stream
+
+
+def _rows_cols(t):
+    cols = t.shape[-1]
+    return t.numel() // cols if cols else 0, cols
+
+
+def _nbytes(ws) -> int:
+    return 0 if ws is None else ws.numel() * ws.element_size()
+
+
+# --- operators --------------------------------------------------------------
+def ls_bias_dropout_residual_fwd(out, mask_bits, x, bias, residual, p: float, seed: int,
+                                 offset: int, stream=None):
+    rows, cols = _rows_cols(x)
+    _check(load().ls_bias_dropout_residual_fwd(
+        _dtype_code(x), _ptr(out), _ptr(mask_bits), _ptr(x), _ptr(bias), _ptr(residual),
+        rows, cols, p, seed, offset, _stream(stream)))
+
+
+def ls_bias_dropout_residual_bwd(dx, dbias, dout, mask_bits, p: float, seed: int = 0,
+                                 offset: int = 0, workspace=None, stream=None):
+    rows, cols = _rows_cols(dout)
+    _check(load().ls_bias_dropout_residual_bwd(
+        _dtype_code(dout), _ptr(dx), _ptr(dbias), _ptr(dout), _ptr(mask_bits), rows, cols, p,
+        seed, offset, _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def ls_bias_relu_dropout_fwd(out, mask_bits, x, bias, p: float, seed: int, offset: int,
+                             stream=None):
+    rows, cols = _rows_cols(x)
+    _check(load().ls_bias_relu_dropout_fwd(
+        _dtype_code(x), _ptr(out), _ptr(mask_bits), _ptr(x), _ptr(bias), rows, cols, p, seed,
+        offset, _stream(stream)))
+
+
+def ls_bias_relu_dropout_bwd(dx, dbias, dout, mask_bits, p: float, workspace=None, stream=None):
+    rows, cols = _rows_cols(dout)
+    _check(load().ls_bias_relu_dropout_bwd(
+        _dtype_code(dout), _ptr(dx), _ptr(dbias), _ptr(dout), _ptr(mask_bits), rows, cols, p,
+        _ptr(workspace), _nbytes(workspace), _stream(stream)))
+
+
+def ls_layernorm_fwd(y, mean, rstd, x, gamma, beta, eps: float = 1e-5, stream=None):
+    rows, cols = _rows_cols(x)
+    _check(load().ls_layernorm_fwd(
+        _dtype_code(x), _ptr(y), _ptr(mean), _ptr(rstd), _ptr(x), _ptr(gamma), _ptr(beta),
+        rows, cols, eps, _stream(stream)))
+
+
+def ls_layernorm_bwd(dx, dgamma, dbeta, dy, x, gamma, mean, rstd, workspace=None, stream=None):
+    rows, cols = _rows_cols(x)
+    _check(load().ls_layernorm_bwd(
+        _dtype_code(x), _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(dy), _ptr(x), _ptr(gamma),
+        _ptr(mean), _ptr(rstd), rows, cols, _ptr(workspace), _nbytes(workspace),
+        _stream(stream)))
+
+
+def ls_softmax_fwd(y, x, key_len=None, causal: bool = False, stream=None):
+    """x, y: [batch, heads, q_len, k_len]; key_len: int32 [batch] on the device or None."""
+    b, h, lq, lk = x.shape
+    _check(load().ls_softmax_fwd(_dtype_code(x), _ptr(y), _ptr(x), b, h, lq, lk, _ptr(key_len),
+                                 int(bool(causal)), _stream(stream)))
+
+
+def ls_softmax_bwd(dx, y, dy, key_len=None, causal: bool = False, stream=None):
+    b, h, lq, lk = y.shape
+    _check(load().ls_softmax_bwd(_dtype_code(y), _ptr(dx), _ptr(y), _ptr(dy), b, h, lq, lk,
+                                 _ptr(key_len), int(bool(causal)), _stream(stream)))

@@ -146,6 +146,37 @@ ls_status ls_layernorm_bwd(ls_dtype dtype, void* dx, void* dgamma, void* dbeta, 
                            int64_t rows, int64_t cols, void* workspace, size_t workspace_bytes,
                            void* stream);
 
+/* LayerNorm backward that needs no caller workspace.  The paper has no
+ * counterpart of this entry point.  It computes what ls_layernorm_bwd computes
+ * (same kernels, same fixed-order reductions, hence the same bits) for callers
+ * that cannot allocate device memory and so cannot hand ls_layernorm_bwd the
+ * workspace for the gamma/beta partial sums: for example a plugin running
+ * inside a host application that owns every device allocation, or a code path
+ * where calling cudaMalloc is not allowed (it synchronises the device, and it
+ * fails while a CUDA graph is being captured).
+ *  - The scratch is an array of LS_NOALLOC_SCRATCH_BYTES (8 MiB) inside the
+ *    library's device image; every GPU that loads the library holds it until
+ *    the process exits.  The call itself allocates nothing (no cudaMalloc,
+ *    cudaFree or allocating library routine).
+ *  - Every shape with cols <= 3448 fits; wider rows fit only for fewer rows.
+ *    A shape whose partial sums need more scratch is rejected with
+ *    LS_ERR_UNSUPPORTED_SHAPE before anything is enqueued.
+ *  - The first call on a device looks up the array's device address
+ *    (cudaGetSymbolAddress) with that device current.  Make that first call
+ *    outside any stream capture.
+ *  - All calls share the one array, which keeps the last call's contents.  A
+ *    call overwrites every scratch byte it reads, so nothing has to start at
+ *    zero.  Calls that can overlap on the GPU (on different streams, or graphs
+ *    replayed concurrently) race on the array and produce wrong dgamma/dbeta:
+ *    order them on one stream.
+ * Arguments, layouts, aliasing and errors are otherwise those of
+ * ls_layernorm_bwd; with dgamma = dbeta = NULL no scratch is used. */
+#define LS_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)
+ls_status ls_layernorm_bwd_noalloc(ls_dtype dtype, void* dx, void* dgamma, void* dbeta,
+                                   const void* dy, const void* x, const void* gamma,
+                                   const float* mean, const float* rstd, int64_t rows,
+                                   int64_t cols, void* stream);
+
 /* Masked attention softmax over the last axis of [batch, heads, q_len, k_len]
  * ("CMU 11-868 L10 (LightSeq)", slides p.23-26; "CS336 Lecture 5: GPU", 6.1-6.2).
  * Entry (b, h, q, j) is valid iff j < clamp(key_len[b], 0, k_len) (key_len is a

@@ -129,6 +129,13 @@ constexpr int64_t kMaxDropoutCols = int64_t{1} << 22;
 
 }  // namespace
 
+void ls::set_last_error_message(const char* fmt, ...) {
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(g_last_error, sizeof(g_last_error), fmt, ap);
+    va_end(ap);
+}
+
 // The library is built with hidden visibility; only the C ABI is exported.
 #pragma GCC visibility push(default)
 extern "C" {

@@ -62,4 +62,7 @@ cudaError_t launch_softmax_bwd(DType dt, void* dx, const void* y, const void* dy
 
 constexpr int64_t kMaxRowLen = 16384;
 
+// Set this host thread's ls_last_error() message (printf-style).
+void set_last_error_message(const char* fmt, ...);
+
 }  // namespace ls

@@ -34,6 +34,7 @@ EXPORTS = (
     "ls_bias_dropout_residual_fwd", "ls_bias_dropout_residual_bwd",
     "ls_bias_relu_dropout_fwd", "ls_bias_relu_dropout_bwd",
     "ls_layernorm_fwd", "ls_layernorm_bwd", "ls_softmax_fwd", "ls_softmax_bwd",
+    "ls_layernorm_bwd_noalloc",
 )
 
 
@@ -62,6 +63,7 @@ _SIGNATURES = {
     "ls_bias_relu_dropout_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _F32, _P, _SZ, _P]),
     "ls_layernorm_fwd": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _I64, _I64, _F32, _P]),
     "ls_layernorm_bwd": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P, _SZ, _P]),
+    "ls_layernorm_bwd_noalloc": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
     "ls_softmax_fwd": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
 }
@@ -194,6 +196,16 @@ def ls_layernorm_bwd(dx, dgamma, dbeta, dy, x, gamma, mean, rstd, workspace=None
         _dtype_code(x), _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(dy), _ptr(x), _ptr(gamma),
         _ptr(mean), _ptr(rstd), rows, cols, _ptr(workspace), _nbytes(workspace),
         _stream(stream)))
+
+
+def ls_layernorm_bwd_noalloc(dx, dgamma, dbeta, dy, x, gamma, mean, rstd, stream=None):
+    """ls_layernorm_bwd without a workspace argument: the gamma/beta partial
+    sums go to the library's built-in device scratch (for callers that cannot
+    allocate device memory).  Calls that overlap on the GPU must not be issued."""
+    rows, cols = _rows_cols(x)
+    _check(load().ls_layernorm_bwd_noalloc(
+        _dtype_code(x), _ptr(dx), _ptr(dgamma), _ptr(dbeta), _ptr(dy), _ptr(x), _ptr(gamma),
+        _ptr(mean), _ptr(rstd), rows, cols, _stream(stream)))
 
 
 def ls_softmax_fwd(y, x, key_len=None, causal: bool = False, stream=None):

@@ -52,6 +52,10 @@ def parse_args():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--details", default=None, help="also write a per-op JSON report here")
+    ap.add_argument("--profile-op", default=None,
+                    help="run the layer once, then only this operator inside the NVTX range "
+                         "'profile' (for ncu --nvtx --nvtx-include profile/); no timing")
+    ap.add_argument("--profile-launches", type=int, default=2)
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -140,7 +144,27 @@ class ClockSampler:
 # The layer step on the GPU.
 # ---------------------------------------------------------------------------
 class LayerStep:
-    """Device buffers of one layer and the ordered list of operator calls."""
+    """Device buffers of one layer and its operator calls.  All tensors live in
+    one dict `t` (inputs and outputs have distinct keys); each operator is a
+    function of such a dict, so the same call can run on cloned buffer sets."""
+
+    # operator -> the tensors it touches
+    TENSORS = {
+        "softmax_fwd": ("scores", "key_len", "probs"),
+        "attn_bdr_fwd": ("attn_x", "attn_bias", "attn_res", "attn_out", "attn_mask"),
+        "ln1_fwd": ("ln1_x", "ln1_gamma", "ln1_beta", "ln1_y", "ln1_mean", "ln1_rstd"),
+        "ffn1_brd_fwd": ("ffn1_x", "ffn1_bias", "ffn1_out", "ffn1_mask"),
+        "ffn2_bdr_fwd": ("ffn2_x", "ffn2_bias", "ffn2_res", "ffn2_out", "ffn2_mask"),
+        "ln2_fwd": ("ln2_x", "ln2_gamma", "ln2_beta", "ln2_y", "ln2_mean", "ln2_rstd"),
+        "ln2_bwd": ("ln2_dy", "ln2_x", "ln2_gamma", "ln2_mean", "ln2_rstd", "ln2_dx",
+                    "ln2_dgamma", "ln2_dbeta"),
+        "ffn2_bdr_bwd": ("ffn2_dout", "ffn2_mask", "ffn2_dx", "ffn2_dbias"),
+        "ffn1_brd_bwd": ("ffn1_dout", "ffn1_mask", "ffn1_dx", "ffn1_dbias"),
+        "ln1_bwd": ("ln1_dy", "ln1_x", "ln1_gamma", "ln1_mean", "ln1_rstd", "ln1_dx",
+                    "ln1_dgamma", "ln1_dbeta"),
+        "attn_bdr_bwd": ("attn_dout", "attn_mask", "attn_dx", "attn_dbias"),
+        "softmax_bwd": ("probs", "scores_dy", "key_len", "scores_dx"),
+    }
 
     def __init__(self, layer, seed, device):
         import numpy as np
@@ -158,10 +182,10 @@ class LayerStep:
         host = synth.layer_inputs(L, seed)
         self.key_len_np = host.get("key_len")
         dev = lambda a: torch.from_numpy(np.ascontiguousarray(a)).to(device)  # noqa: E731
-        self.inp = {k: dev(v) for k, v in host.items()}
+        self.inputs = sorted(host)
         e = lambda *s, d=dt: torch.empty(s, dtype=d, device=device)  # noqa: E731
         nw = lambda n: (n + 31) // 32  # noqa: E731
-        self.out = {
+        out = {
             "attn_out": e(T, H), "attn_mask": e(nw(T * H), d=torch.int32),
             "ln1_y": e(T, H), "ln1_mean": e(T, d=torch.float32), "ln1_rstd": e(T, d=torch.float32),
             "ffn1_out": e(T, F), "ffn1_mask": e(nw(T * F), d=torch.int32),
@@ -175,6 +199,9 @@ class LayerStep:
             "attn_dx": e(T, H), "attn_dbias": e(H),
             "scores_dx": e(L.batch, L.heads, L.seq, L.seq),
         }
+        self.outputs = sorted(out)
+        self.t = {k: dev(v) for k, v in host.items()}
+        self.t.update(out)
         ws = max(ls_ops.colreduce_workspace_bytes(T, F), ls_ops.colreduce_workspace_bytes(T, H))
         self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
         self.bytes = accounting.layer_step_bytes(T, H, F, L.batch, L.heads, L.seq, self.esize,
@@ -183,71 +210,105 @@ class LayerStep:
         for k in ("ln2_bwd", "ffn2_bdr_bwd", "ffn1_brd_bwd", "ln1_bwd", "attn_bdr_bwd"):
             self.launches[k] = 2  # main kernel + deterministic column reduction
 
-    def ops(self):
+    def ops(self, t=None):
         """(name, thunk) in layer order: forward, then backward in reverse."""
-        ls, i, o, L, ws = self.ls, self.inp, self.out, self.layer, self.workspace
-        kl = i.get("key_len")
+        t = self.t if t is None else t
+        ls, L, ws = self.ls, self.layer, self.workspace
+        kl = t.get("key_len")
         p = L.p
         return [
-            ("softmax_fwd", lambda: ls.ls_softmax_fwd(o["probs"], i["scores"], kl, L.causal)),
+            ("softmax_fwd", lambda: ls.ls_softmax_fwd(t["probs"], t["scores"], kl, L.causal)),
             ("attn_bdr_fwd", lambda: ls.ls_bias_dropout_residual_fwd(
-                o["attn_out"], o["attn_mask"], i["attn_x"], i["attn_bias"], i["attn_res"], p, 0, 1)),
-            ("ln1_fwd", lambda: ls.ls_layernorm_fwd(o["ln1_y"], o["ln1_mean"], o["ln1_rstd"],
-                                                    i["ln1_x"], i["ln1_gamma"], i["ln1_beta"], 1e-5)),
+                t["attn_out"], t["attn_mask"], t["attn_x"], t["attn_bias"], t["attn_res"], p, 0, 1)),
+            ("ln1_fwd", lambda: ls.ls_layernorm_fwd(t["ln1_y"], t["ln1_mean"], t["ln1_rstd"],
+                                                    t["ln1_x"], t["ln1_gamma"], t["ln1_beta"], 1e-5)),
             ("ffn1_brd_fwd", lambda: ls.ls_bias_relu_dropout_fwd(
-                o["ffn1_out"], o["ffn1_mask"], i["ffn1_x"], i["ffn1_bias"], p, 0, 2)),
+                t["ffn1_out"], t["ffn1_mask"], t["ffn1_x"], t["ffn1_bias"], p, 0, 2)),
             ("ffn2_bdr_fwd", lambda: ls.ls_bias_dropout_residual_fwd(
-                o["ffn2_out"], o["ffn2_mask"], i["ffn2_x"], i["ffn2_bias"], i["ffn2_res"], p, 0, 3)),
-            ("ln2_fwd", lambda: ls.ls_layernorm_fwd(o["ln2_y"], o["ln2_mean"], o["ln2_rstd"],
-                                                    i["ln2_x"], i["ln2_gamma"], i["ln2_beta"], 1e-5)),
+                t["ffn2_out"], t["ffn2_mask"], t["ffn2_x"], t["ffn2_bias"], t["ffn2_res"], p, 0, 3)),
+            ("ln2_fwd", lambda: ls.ls_layernorm_fwd(t["ln2_y"], t["ln2_mean"], t["ln2_rstd"],
+                                                    t["ln2_x"], t["ln2_gamma"], t["ln2_beta"], 1e-5)),
             ("ln2_bwd", lambda: ls.ls_layernorm_bwd(
-                o["ln2_dx"], o["ln2_dgamma"], o["ln2_dbeta"], i["ln2_dy"], i["ln2_x"],
-                i["ln2_gamma"], o["ln2_mean"], o["ln2_rstd"], workspace=ws)),
+                t["ln2_dx"], t["ln2_dgamma"], t["ln2_dbeta"], t["ln2_dy"], t["ln2_x"],
+                t["ln2_gamma"], t["ln2_mean"], t["ln2_rstd"], workspace=ws)),
             ("ffn2_bdr_bwd", lambda: ls.ls_bias_dropout_residual_bwd(
-                o["ffn2_dx"], o["ffn2_dbias"], i["ffn2_dout"], o["ffn2_mask"], p, workspace=ws)),
+                t["ffn2_dx"], t["ffn2_dbias"], t["ffn2_dout"], t["ffn2_mask"], p, workspace=ws)),
             ("ffn1_brd_bwd", lambda: ls.ls_bias_relu_dropout_bwd(
-                o["ffn1_dx"], o["ffn1_dbias"], i["ffn1_dout"], o["ffn1_mask"], p, workspace=ws)),
+                t["ffn1_dx"], t["ffn1_dbias"], t["ffn1_dout"], t["ffn1_mask"], p, workspace=ws)),
             ("ln1_bwd", lambda: ls.ls_layernorm_bwd(
-                o["ln1_dx"], o["ln1_dgamma"], o["ln1_dbeta"], i["ln1_dy"], i["ln1_x"],
-                i["ln1_gamma"], o["ln1_mean"], o["ln1_rstd"], workspace=ws)),
+                t["ln1_dx"], t["ln1_dgamma"], t["ln1_dbeta"], t["ln1_dy"], t["ln1_x"],
+                t["ln1_gamma"], t["ln1_mean"], t["ln1_rstd"], workspace=ws)),
             ("attn_bdr_bwd", lambda: ls.ls_bias_dropout_residual_bwd(
-                o["attn_dx"], o["attn_dbias"], i["attn_dout"], o["attn_mask"], p, workspace=ws)),
-            ("softmax_bwd", lambda: ls.ls_softmax_bwd(o["scores_dx"], o["probs"], i["scores_dy"],
+                t["attn_dx"], t["attn_dbias"], t["attn_dout"], t["attn_mask"], p, workspace=ws)),
+            ("softmax_bwd", lambda: ls.ls_softmax_bwd(t["scores_dx"], t["probs"], t["scores_dy"],
                                                       kl, L.causal)),
         ]
 
+    def nbytes(self, keys):
+        return sum(self.t[k].numel() * self.t[k].element_size() for k in keys if k in self.t)
+
     def footprint_bytes(self):
-        t = self.torch
-        tot = sum(v.numel() * v.element_size() for v in self.inp.values())
-        tot += sum(v.numel() * v.element_size() for v in self.out.values())
-        return tot
+        return self.nbytes(self.t.keys())
 
 
-def capture(step, with_events):
-    """Capture one step in a CUDA graph; optionally with an external timing
-    event before the first and after every operator."""
-    torch = step.torch
+def capture(thunks):
+    """Capture the thunks, in order, in one CUDA graph (after one eager pass)."""
+    import torch
+
     s = torch.cuda.Stream()
     s.wait_stream(torch.cuda.current_stream())
-    events = []
     with torch.cuda.stream(s):
-        for _, fn in step.ops():  # eager warm-up outside capture (loads modules)
+        for fn in thunks:
             fn()
     torch.cuda.current_stream().wait_stream(s)
     torch.cuda.synchronize()
     g = torch.cuda.CUDAGraph()
-    if with_events:
-        events = [torch.cuda.Event(enable_timing=True, external=True)
-                  for _ in range(len(step.ops()) + 1)]
     with torch.cuda.graph(g):
-        if with_events:
-            events[0].record()
-        for k, (_, fn) in enumerate(step.ops()):
+        for fn in thunks:
             fn()
-            if with_events:
-                events[k + 1].record()
     torch.cuda.synchronize()
-    return g, events
+    return g
+
+
+def time_graph(g, reps):
+    import torch
+
+    g.replay()
+    torch.cuda.synchronize()
+    a = torch.cuda.Event(enable_timing=True)
+    b = torch.cuda.Event(enable_timing=True)
+    a.record()
+    for _ in range(reps):
+        g.replay()
+    b.record()
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def per_op_isolated(step, reps=10):
+    """Device time per launch of each operator, measured alone: one graph
+    replays the operator back to back over enough cloned buffer sets that
+    every launch finds its inputs outside L2 (sets x footprint >= 3 x L2)."""
+    import math
+
+    names = [n for n, _ in step.ops()]
+    res = {}
+    for n in names:
+        keys = [k for k in LayerStep.TENSORS[n] if k in step.t]
+        fp = step.nbytes(keys)
+        nsets = max(2, min(48, math.ceil(3 * L2_BYTES / max(fp, 1))))
+        sets = []
+        for _ in range(nsets):
+            t = dict(step.t)
+            for k in keys:
+                t[k] = step.t[k].clone()
+            sets.append(t)
+        thunks = [dict(step.ops(t))[n] for t in sets]
+        g = capture(thunks)
+        ms = time_graph(g, reps) / nsets
+        res[n] = {"ms": ms, "sets": nsets, "footprint": fp}
+        del g, sets, thunks
+    return res
 
 
 def kernels_sha():
@@ -404,11 +465,7 @@ def run_ours(args):
     step = LayerStep(layer, args.seed, device)
     step_bytes = sum(step.bytes.values())
     names = [n for n, _ in step.ops()]
-    graph, _ = capture(step, with_events=False)
-    try:
-        igraph, events = capture(step, with_events=True)
-    except TypeError:
-        igraph, events = None, None
+    graph = capture([fn for _, fn in step.ops()])
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -435,43 +492,36 @@ def run_ours(args):
         pg.all_reduce(t, op=pg.ReduceOp.MAX)
         ms = float(t.item())
     ms_step = ms / args.steps
-
-    # Per-operator device time: external event nodes inside the step graph,
-    # one replay at a time (the events of a replay bracket each operator).
-    per_op = {n: 0.0 for n in names}
-    n_inst = min(args.steps, 500)
-    if igraph is not None:
-        for _ in range(n_inst):
-            igraph.replay()
-            torch.cuda.synchronize()
-            for k, n in enumerate(names):
-                per_op[n] += events[k].elapsed_time(events[k + 1])
-        per_op = {n: v / n_inst for n, v in per_op.items()}
     t_busy1 = time.time()
+
+    # Per-operator device time, each operator alone and L2-cold.
+    iso = per_op_isolated(step)
+    per_op = {n: iso[n]["ms"] for n in names}
 
     # End to end through the public API with host buffers: per step, copy every
     # input from pinned host memory, run the step, copy every output back.
     e2e_steps = min(args.steps, 50)
-    host_in = {k: v.cpu().pin_memory() for k, v in step.inp.items()}
-    host_out = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in step.out.items()}
+    host_in = {k: step.t[k].cpu().pin_memory() for k in step.inputs}
+    host_out = {k: torch.empty(step.t[k].shape, dtype=step.t[k].dtype).pin_memory()
+                for k in step.outputs}
     h2d = sum(v.numel() * v.element_size() for v in host_in.values())
     d2h = sum(v.numel() * v.element_size() for v in host_out.values())
     for _ in range(3):
         for k, v in host_in.items():
-            step.inp[k].copy_(v, non_blocking=True)
+            step.t[k].copy_(v, non_blocking=True)
         graph.replay()
         for k, v in host_out.items():
-            v.copy_(step.out[k], non_blocking=True)
+            v.copy_(step.t[k], non_blocking=True)
     torch.cuda.synchronize()
     f0 = torch.cuda.Event(enable_timing=True)
     f1 = torch.cuda.Event(enable_timing=True)
     f0.record()
     for _ in range(e2e_steps):
         for k, v in host_in.items():
-            step.inp[k].copy_(v, non_blocking=True)
+            step.t[k].copy_(v, non_blocking=True)
         graph.replay()
         for k, v in host_out.items():
-            v.copy_(step.out[k], non_blocking=True)
+            v.copy_(step.t[k], non_blocking=True)
     f1.record()
     torch.cuda.synchronize()
     e2e_ms = f0.elapsed_time(f1) / e2e_steps
@@ -485,13 +535,11 @@ def run_ours(args):
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
     ops_report = {}
     for n in names:
-        t_us = per_op[n] * 1e3 if igraph is not None else None
-        gbs = step.bytes[n] / (per_op[n] * 1e-3) / 1e9 if igraph is not None and per_op[n] > 0 else None
-        ops_report[n] = {"us": None if t_us is None else round(t_us, 2),
-                         "bytes": int(step.bytes[n]),
-                         "GB/s": None if gbs is None else round(gbs, 1),
-                         "frac": None if gbs is None else round(gbs / peak, 4)}
-    dominant = max(names, key=lambda n: per_op[n]) if igraph is not None else "softmax_bwd"
+        gbs = step.bytes[n] / (per_op[n] * 1e-3) / 1e9
+        ops_report[n] = {"us": round(per_op[n] * 1e3, 2), "bytes": int(step.bytes[n]),
+                         "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                         "buffer_sets": iso[n]["sets"]}
+    dominant = max(names, key=lambda n: per_op[n])
     dom = ops_report[dominant]
     roofline = {"bound": "hbm", "kernel": dominant,
                 "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
@@ -515,6 +563,8 @@ def run_ours(args):
         "pct_of_peak": round(value / world / peak * 100, 2),
         "tokens_per_s": round(layer.tokens * world / (ms_step * 1e-3), 1),
         "per_op": ops_report,
+        "per_op_note": "each operator alone, back to back over rotating L2-cold buffer sets",
+        "sum_per_op_us": round(sum(per_op.values()) * 1e3, 2),
         "roofline": roofline,
         "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -535,10 +585,39 @@ def run_ours(args):
     return 0
 
 
+def run_profile_op(args):
+    """One eager pass of the whole layer (so backward inputs exist), then
+    --profile-launches calls of one operator inside the NVTX range 'profile'."""
+    import torch
+
+    from transformer_layer_non_gb300 import ls_ops, synth
+
+    ls_ops.load()
+    step = LayerStep(synth.LAYERS[args.workload], args.seed, torch.device("cuda", 0))
+    ops = dict(step.ops())
+    if args.profile_op not in ops:
+        print(json.dumps({"error": f"unknown op {args.profile_op}", "ops": list(ops)}))
+        return 2
+    for _, fn in step.ops():
+        fn()
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("profile")
+    for _ in range(args.profile_launches):
+        ops[args.profile_op]()
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_op": args.profile_op, "workload": args.workload,
+                      "launches": args.profile_launches,
+                      "algorithmic_bytes": int(step.bytes[args.profile_op])}))
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
+    if args.profile_op:
+        return run_profile_op(args)
     return run_ours(args)
 
 

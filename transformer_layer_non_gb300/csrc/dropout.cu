@@ -3,16 +3,23 @@
 // elementwise steps between two GEMMs is one kernel; "LightSeq2", sections
 // 2.1.1-2.1.2: the dropout mask is saved in the forward and reused backward).
 //
-// Layout.  A CTA of 256 threads works on a tile of (256/LANES)*U rows by
-// LANES*8 columns.  Lane `l` of a row group owns one 8-element column vector
-// (16 bytes in FP16) and keeps it for every row of the tile, so bias values
-// are loaded once per thread and bias-gradient partial sums accumulate in
-// registers.  All U row loads of a thread are issued before any arithmetic so
-// that U (or 2U) independent 16-byte loads per thread are in flight.
+// Forward layout.  The activation is a flat array of 8-element vectors (16
+// bytes in FP16); with cols % 8 == 0 a vector never straddles a row and its 8
+// keep bits are one mask byte.  A persistent grid (a multiple of the SM count)
+// walks the vectors in rounds: in round k, warp w of CTA b takes the 32
+// consecutive vectors starting at (k * W + b + w * gridDim) * 32, W = all warps.
+// The last, partial round is thus spread over every CTA instead of piling onto
+// a few SMs.  Each thread keeps two register buffers of U rounds: the loads of
+// one buffer are in flight while the other is computed (two Philox calls per
+// vector, FP32 arithmetic) and stored.
 //
-// Mask.  With cols % 8 == 0 the 8 elements of a vector are one mask byte
-// (byte i/8 of the little-endian uint32 word array), so every thread writes or
-// reads exactly one byte per vector.
+// Backward layout.  The bias gradient needs column sums, so the backward works
+// on 2-D tiles of 128 rows x 64 columns: lane l of an 8-lane row group owns one
+// column vector for all rows of the tile and accumulates its partial sums in
+// registers; the 32 row slots are summed in shared memory in a fixed order into
+// one FP32 partial row per tile.  A persistent grid walks the tiles.  A second
+// kernel adds the partial rows of each column in a fixed order, so the result
+// does not depend on the grid or the GPU.
 #include "ls_device.cuh"
 #include "ls_internal.h"
 
@@ -21,52 +28,67 @@ namespace {
 
 constexpr int kThreads = 256;
 
-// Forward.  RELU=false: out = residual + keep*(x+bias)*scale, bit = keep.
-//           RELU=true:  z = x+bias; bit = (z>0)&keep; out = bit*z*scale.
-template <typename T, bool RELU, int LANES, int U>
-__global__ void __launch_bounds__(kThreads)
-dropout_fwd_kernel(T* out, uint8_t* __restrict__ mask, const T* x, const T* __restrict__ bias,
-                   const T* residual, int64_t rows, int cols, uint32_t thr, float scale,
-                   PhiloxKey key, uint32_t off_lo, uint32_t off_hi, int mask_tail_bytes) {
-    constexpr int RPS = kThreads / LANES;  // rows per step
-    const int lane = threadIdx.x % LANES;
-    const int slot = threadIdx.x / LANES;
-    const int nvec = cols / kVec;
-    const int cv = blockIdx.y * LANES + lane;
-    const bool col_ok = cv < nvec;
-    const int c0 = cv * kVec;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * (RPS * U) + slot;
+// ---------------------------------------------------------------------------
+// Forward.
+// ---------------------------------------------------------------------------
+struct FwdArgs {
+    uint64_t nv;        // vectors in the tensor (rows * cols / 8)
+    uint32_t nvr;       // vectors per row
+    uint32_t step_col;  // (vectors per round) mod nvr
+    uint32_t thr;
+    float scale;
+    PhiloxKey key;
+    uint32_t off_lo, off_hi;
+    int mask_tail_bytes;
+};
 
-    Raw8<T> xr[U];
-    Raw8<T> rr[U];
+template <typename T, bool RELU, int U>
+__device__ __forceinline__ void fwd_load(Raw8<T> (&xr)[U], Raw8<T> (&rr)[U], const T* x,
+                                         const T* residual, uint64_t v, uint64_t S, uint64_t nv) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int64_t r = r0 + static_cast<int64_t>(u) * RPS;
-        if (col_ok && r < rows) {
-            const int64_t off = r * cols + c0;
-            xr[u] = load8<T>(x + off);
-            if (!RELU) rr[u] = load8<T>(residual + off);
+        const uint64_t vu = v + u * S;
+        if (vu < nv) {
+            xr[u] = load8<T>(x + vu * kVec);
+            if (!RELU) rr[u] = load8<T>(residual + vu * kVec);
         }
     }
-    float b[kVec];
-    if (col_ok) load8f<T>(bias + c0, b);
+}
 
+// Keep bits of the U vectors of a chunk; called right after the chunk's loads
+// are issued, so the Philox arithmetic overlaps their latency.
+template <int U>
+__device__ __forceinline__ void fwd_keep(uint32_t (&keep)[U], uint64_t v, uint64_t S,
+                                         const FwdArgs& a, const PhiloxSchedule& ks) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int64_t r = r0 + static_cast<int64_t>(u) * RPS;
-        if (!(col_ok && r < rows)) continue;
-        const int64_t i = r * cols + c0;
-        const uint32_t keep = keep_bits8(static_cast<uint64_t>(i), thr, key, off_lo, off_hi);
-        float xf[kVec], o[kVec];
+        const uint64_t vu = v + u * S;
+        keep[u] = vu < a.nv ? keep_bits8(vu * kVec, a.thr, ks, a.off_lo, a.off_hi) : 0u;
+    }
+}
+
+template <typename T, bool RELU, int U>
+__device__ __forceinline__ void fwd_compute(const Raw8<T> (&xr)[U], const Raw8<T> (&rr)[U],
+                                            const uint32_t (&kp)[U], T* out, uint8_t* mask,
+                                            const T* __restrict__ bias, uint64_t v, uint32_t cv,
+                                            uint64_t S, const FwdArgs& a) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const uint64_t vu = v + u * S;
+        if (vu >= a.nv) break;
+        float b[kVec], xf[kVec], o[kVec];
+        load8f<T>(bias + static_cast<size_t>(cv) * kVec, b);
         unpack(xr[u], xf);
-        uint32_t bits = 0;
+        const uint32_t keep = kp[u];
+        uint32_t bits;
         if (RELU) {
+            bits = 0;
 #pragma unroll
             for (int j = 0; j < kVec; ++j) {
                 const float z = xf[j] + b[j];
                 const bool on = (z > 0.f) && ((keep >> j) & 1u);
                 bits |= on ? (1u << j) : 0u;
-                o[j] = on ? z * scale : 0.f;
+                o[j] = on ? z * a.scale : 0.f;
             }
         } else {
             float rf[kVec];
@@ -74,96 +96,192 @@ dropout_fwd_kernel(T* out, uint8_t* __restrict__ mask, const T* x, const T* __re
 #pragma unroll
             for (int j = 0; j < kVec; ++j) {
                 const float z = xf[j] + b[j];
-                o[j] = ((keep >> j) & 1u) ? rf[j] + z * scale : rf[j];
+                o[j] = ((keep >> j) & 1u) ? rf[j] + z * a.scale : rf[j];
             }
             bits = keep;
         }
-        store8f<T>(out + i, o);
-        if (mask) mask[i >> 3] = static_cast<uint8_t>(bits);
-    }
-    // Bytes of the last mask word past the last element are defined as 0.
-    if (mask && mask_tail_bytes > 0 && blockIdx.x == 0 && blockIdx.y == 0 && threadIdx.x == 0) {
-        const int64_t nbytes = rows * cols / 8;
-        for (int k = 0; k < mask_tail_bytes; ++k) mask[nbytes + k] = 0;
+        store8f<T>(out + vu * kVec, o);
+        if (mask) mask[vu] = static_cast<uint8_t>(bits);
+        cv += a.step_col;
+        if (cv >= a.nvr) cv -= a.nvr;
     }
 }
 
-// Backward: dx = bit * dout * scale; the bit comes from the mask, or (REGEN)
-// is drawn again from Philox.  With partial != nullptr the column sums of dx
-// over the CTA's rows go to partial[blockIdx.x, :].
-template <typename T, bool REGEN, int LANES, int U>
-__global__ void __launch_bounds__(kThreads)
-dropout_bwd_kernel(T* dx, float* __restrict__ partial, const T* dout,
-                   const uint8_t* __restrict__ mask, int64_t rows, int cols, uint32_t thr,
-                   float scale, PhiloxKey key, uint32_t off_lo, uint32_t off_hi) {
-    constexpr int RPS = kThreads / LANES;
-    const int lane = threadIdx.x % LANES;
-    const int slot = threadIdx.x / LANES;
-    const int nvec = cols / kVec;
-    const int cv = blockIdx.y * LANES + lane;
-    const bool col_ok = cv < nvec;
-    const int c0 = cv * kVec;
-    const int64_t r0 = static_cast<int64_t>(blockIdx.x) * (RPS * U) + slot;
-
-    Raw8<T> dr[U];
-    uint32_t mb[U];
+template <typename T, bool RELU, int U>
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 4 : 2)
+dropout_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias,
+                   const T* residual, FwdArgs a) {
+    const PhiloxSchedule ks = philox_schedule(a.key);
+    pdl_enter();
+    const uint64_t S = static_cast<uint64_t>(gridDim.x) * kThreads;  // vectors per round
+    const uint64_t gw = blockIdx.x + static_cast<uint64_t>(threadIdx.x >> 5) * gridDim.x;
+    uint64_t v = gw * 32 + (threadIdx.x & 31);
+    uint32_t cv = static_cast<uint32_t>(v % a.nvr);
+    // (U rounds) mod nvr, from the per-round step.
+    uint32_t stepU = 0;
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int64_t r = r0 + static_cast<int64_t>(u) * RPS;
+        stepU += a.step_col;
+        if (stepU >= a.nvr) stepU -= a.nvr;
+    }
+    Raw8<T> xa[U], ra[U], xb[U], rb[U];
+    uint32_t ka[U], kb[U];
+    fwd_load<T, RELU, U>(xa, ra, x, residual, v, S, a.nv);
+    fwd_keep<U>(ka, v, S, a, ks);
+    while (v < a.nv) {
+        const uint64_t v1 = v + U * S;
+        uint32_t cv1 = cv + stepU;
+        if (cv1 >= a.nvr) cv1 -= a.nvr;
+        fwd_load<T, RELU, U>(xb, rb, x, residual, v1, S, a.nv);
+        fwd_keep<U>(kb, v1, S, a, ks);
+        fwd_compute<T, RELU, U>(xa, ra, ka, out, mask, bias, v, cv, S, a);
+        if (v1 >= a.nv) break;
+        v = v1 + U * S;
+        cv = cv1 + stepU;
+        if (cv >= a.nvr) cv -= a.nvr;
+        fwd_load<T, RELU, U>(xa, ra, x, residual, v, S, a.nv);
+        fwd_keep<U>(ka, v, S, a, ks);
+        fwd_compute<T, RELU, U>(xb, rb, kb, out, mask, bias, v1, cv1, S, a);
+    }
+    // Bytes of the last mask word past the last element are defined as 0.
+    if (mask && a.mask_tail_bytes > 0 && blockIdx.x == 0 && threadIdx.x == 0)
+        for (int k = 0; k < a.mask_tail_bytes; ++k) mask[a.nv + k] = 0;
+}
+
+// ---------------------------------------------------------------------------
+// Backward.
+// ---------------------------------------------------------------------------
+constexpr int kBwdLanes = 8;                         // lanes per row segment (64 columns)
+constexpr int kBwdRps = kThreads / kBwdLanes;        // row slots per CTA
+constexpr int kBwdU = 4;                             // rows per slot per tile
+constexpr int kBwdRowsPerTile = kBwdRps * kBwdU;     // 128
+constexpr int kBwdColsPerTile = kBwdLanes * kVec;    // 64
+
+struct BwdArgs {
+    int64_t rows;
+    int cols;
+    int nbands;
+    int64_t ntiles;
+    uint32_t thr;
+    float scale;
+    PhiloxKey key;
+    uint32_t off_lo, off_hi;
+};
+
+// Loads of one tile; with REGEN the keep bits are drawn here, after the loads
+// are issued, so the Philox arithmetic overlaps their latency.
+template <typename T, bool REGEN>
+__device__ __forceinline__ void bwd_load(Raw8<T> (&dr)[kBwdU], uint32_t (&mb)[kBwdU],
+                                         const T* dout, const uint8_t* mask, int64_t tile,
+                                         const BwdArgs& a, const PhiloxSchedule& ks) {
+    const int64_t chunk = tile / a.nbands;
+    const int band = static_cast<int>(tile - chunk * a.nbands);
+    const int lane = threadIdx.x % kBwdLanes;
+    const int c0 = (band * kBwdLanes + lane) * kVec;
+    const int64_t r0 = chunk * kBwdRowsPerTile + threadIdx.x / kBwdLanes;
+#pragma unroll
+    for (int u = 0; u < kBwdU; ++u) {
+        const int64_t r = r0 + static_cast<int64_t>(u) * kBwdRps;
         mb[u] = 0;
-        if (col_ok && r < rows) {
-            const int64_t off = r * cols + c0;
+        if (tile < a.ntiles && c0 < a.cols && r < a.rows) {
+            const int64_t off = r * a.cols + c0;
             dr[u] = load8<T>(dout + off);
             if (!REGEN) mb[u] = mask[off >> 3];
         }
     }
+    if (REGEN) {
+#pragma unroll
+        for (int u = 0; u < kBwdU; ++u) {
+            const int64_t r = r0 + static_cast<int64_t>(u) * kBwdRps;
+            if (tile < a.ntiles && c0 < a.cols && r < a.rows)
+                mb[u] = keep_bits8(static_cast<uint64_t>(r * a.cols + c0), a.thr, ks, a.off_lo,
+                                   a.off_hi);
+        }
+    }
+}
+
+template <typename T, bool REGEN>
+__device__ __forceinline__ void bwd_compute(const Raw8<T> (&dr)[kBwdU],
+                                            const uint32_t (&mb)[kBwdU], T* dx, float* partial,
+                                            float (*red)[kBwdColsPerTile], int64_t tile,
+                                            const BwdArgs& a) {
+    const int64_t chunk = tile / a.nbands;
+    const int band = static_cast<int>(tile - chunk * a.nbands);
+    const int lane = threadIdx.x % kBwdLanes;
+    const int slot = threadIdx.x / kBwdLanes;
+    const int c0 = (band * kBwdLanes + lane) * kVec;
+    const int64_t r0 = chunk * kBwdRowsPerTile + slot;
     float acc[kVec];
 #pragma unroll
     for (int j = 0; j < kVec; ++j) acc[j] = 0.f;
-
 #pragma unroll
-    for (int u = 0; u < U; ++u) {
-        const int64_t r = r0 + static_cast<int64_t>(u) * RPS;
-        if (!(col_ok && r < rows)) continue;
-        const int64_t i = r * cols + c0;
-        const uint32_t bits =
-            REGEN ? keep_bits8(static_cast<uint64_t>(i), thr, key, off_lo, off_hi) : mb[u];
+    for (int u = 0; u < kBwdU; ++u) {
+        const int64_t r = r0 + static_cast<int64_t>(u) * kBwdRps;
+        if (!(c0 < a.cols && r < a.rows)) continue;
+        const int64_t i = r * a.cols + c0;
+        const uint32_t bits = mb[u];
         float g[kVec];
         unpack(dr[u], g);
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
-            g[j] = ((bits >> j) & 1u) ? g[j] * scale : 0.f;
+            g[j] = ((bits >> j) & 1u) ? g[j] * a.scale : 0.f;
             acc[j] += g[j];
         }
         store8f<T>(dx + i, g);
     }
     if (partial == nullptr) return;
-
-    // Sum the RPS row slots of each column in a fixed order.
-    __shared__ __align__(16) float red[RPS][LANES * kVec];
+    // Sum the row slots of each column in a fixed order.
+    __syncthreads();  // the previous tile's readers of red[] are done
     float4* dst = reinterpret_cast<float4*>(&red[slot][lane * kVec]);
     dst[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
     dst[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
     __syncthreads();
-    for (int k = threadIdx.x; k < LANES * kVec; k += kThreads) {
-        const int col = blockIdx.y * LANES * kVec + k;
-        if (col >= cols) continue;
-        float s = 0.f;
+    if (threadIdx.x < kBwdColsPerTile) {
+        const int col = band * kBwdColsPerTile + threadIdx.x;
+        if (col < a.cols) {
+            float s = 0.f;
 #pragma unroll 8
-        for (int q = 0; q < RPS; ++q) s += red[q][k];
-        partial[static_cast<int64_t>(blockIdx.x) * cols + col] = s;
+            for (int q = 0; q < kBwdRps; ++q) s += red[q][threadIdx.x];
+            partial[chunk * a.cols + col] = s;
+        }
     }
 }
 
-// partial [parts, width] FP32 -> out [width] in T, summing rows in a fixed
-// order: thread group g takes rows g, g+G, ...; then the G group sums are added
-// in group order.
+template <typename T, bool REGEN>
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 3 : 2)
+dropout_bwd_kernel(T* dx, float* __restrict__ partial, const T* dout,
+                   const uint8_t* __restrict__ mask, BwdArgs a) {
+    __shared__ __align__(16) float red[kBwdRps][kBwdColsPerTile];
+    const PhiloxSchedule ks = philox_schedule(a.key);
+    pdl_enter();
+    int64_t t = blockIdx.x;
+    Raw8<T> da[kBwdU], db[kBwdU];
+    uint32_t ma[kBwdU], mbb[kBwdU];
+    bwd_load<T, REGEN>(da, ma, dout, mask, t, a, ks);
+    while (t < a.ntiles) {
+        const int64_t t1 = t + gridDim.x;
+        bwd_load<T, REGEN>(db, mbb, dout, mask, t1, a, ks);
+        bwd_compute<T, REGEN>(da, ma, dx, partial, red, t, a);
+        if (t1 >= a.ntiles) break;
+        t = t1 + gridDim.x;
+        bwd_load<T, REGEN>(da, ma, dout, mask, t, a, ks);
+        bwd_compute<T, REGEN>(db, mbb, dx, partial, red, t1, a);
+    }
+}
+
+// ---------------------------------------------------------------------------
+// Fixed-order column reduction: partial [parts, width] FP32 -> out0/out1.
+// Group g of a CTA adds rows g, g + G, ...; the G group sums are then added in
+// group order.
+// ---------------------------------------------------------------------------
 constexpr int kRedCols = 32;
-constexpr int kRedGroups = 16;
+constexpr int kRedGroups = 32;
 template <typename T>
 __global__ void __launch_bounds__(kRedCols* kRedGroups)
 colreduce_kernel(T* __restrict__ out0, T* __restrict__ out1, int64_t split,
                  const float* __restrict__ partial, int64_t parts, int64_t width) {
+    __shared__ float sm[kRedGroups][kRedCols + 1];
+    pdl_enter();
     const int cx = threadIdx.x % kRedCols;
     const int gy = threadIdx.x / kRedCols;
     const int64_t col = static_cast<int64_t>(blockIdx.x) * kRedCols + cx;
@@ -172,7 +290,6 @@ colreduce_kernel(T* __restrict__ out0, T* __restrict__ out1, int64_t split,
 #pragma unroll 4
         for (int64_t p = gy; p < parts; p += kRedGroups) s += partial[p * width + col];
     }
-    __shared__ float sm[kRedGroups][kRedCols + 1];
     sm[gy][cx] = s;
     __syncthreads();
     if (gy == 0 && col < width) {
@@ -186,54 +303,70 @@ colreduce_kernel(T* __restrict__ out0, T* __restrict__ out1, int64_t split,
     }
 }
 
-// Tile shapes.  Forward: 32 lanes x 8 elements = 256 columns per tile, so a
-// warp writes one full 32-byte mask sector per row.  Backward: 8 lanes
-// (64 columns) per row and 128 rows per tile, so the bias-gradient partial
-// sums are few (one row of `cols` floats per 128 input rows).
-constexpr int kFwdLanes = 32, kFwdU = 4;
-constexpr int kBwdLanes = 8, kBwdU = 4;
-constexpr int kBwdRowsPerTile = (kThreads / kBwdLanes) * kBwdU;
-
 PhiloxKey make_key(uint64_t seed) {
     return PhiloxKey{static_cast<uint32_t>(seed), static_cast<uint32_t>(seed >> 32)};
 }
+
+template <typename K>
+int occupancy(K kernel, int threads, size_t smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
+        n < 1)
+        n = 1;
+    return n;
+}
+
+constexpr int kFwdU = 2;
 
 template <typename T, bool RELU>
 cudaError_t fwd_impl(void* out, uint8_t* mask, const void* x, const void* bias,
                      const void* residual, int64_t rows, int64_t cols, const DropoutRng& rng,
                      cudaStream_t s) {
-    constexpr int RPT = (kThreads / kFwdLanes) * kFwdU;
-    const int64_t nvec = cols / kVec;
-    dim3 grid(static_cast<unsigned>((rows + RPT - 1) / RPT),
-              static_cast<unsigned>((nvec + kFwdLanes - 1) / kFwdLanes));
-    const int64_t n = rows * cols;
-    const int tail = static_cast<int>(((n + 31) / 32) * 4 - n / 8);
-    dropout_fwd_kernel<T, RELU, kFwdLanes, kFwdU><<<grid, kThreads, 0, s>>>(
-        static_cast<T*>(out), mask, static_cast<const T*>(x), static_cast<const T*>(bias),
-        static_cast<const T*>(residual), rows, static_cast<int>(cols), rng.thr, rng.scale,
-        make_key(rng.seed), static_cast<uint32_t>(rng.offset),
-        static_cast<uint32_t>(rng.offset >> 32), tail);
-    return cudaGetLastError();
+    auto kern = dropout_fwd_kernel<T, RELU, kFwdU>;
+    static const int occ = occupancy(kern, kThreads, 0);
+    FwdArgs a;
+    a.nv = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols) / kVec;
+    a.nvr = static_cast<uint32_t>(cols / kVec);
+    const int64_t want = static_cast<int64_t>((a.nv + kThreads * kFwdU - 1) / (kThreads * kFwdU));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, int64_t{sm_count()} * occ));
+    a.step_col = static_cast<uint32_t>((static_cast<uint64_t>(grid) * kThreads) % a.nvr);
+    a.thr = rng.thr;
+    a.scale = rng.scale;
+    a.key = make_key(rng.seed);
+    a.off_lo = static_cast<uint32_t>(rng.offset);
+    a.off_hi = static_cast<uint32_t>(rng.offset >> 32);
+    a.mask_tail_bytes = static_cast<int>(((a.nv + 3) / 4) * 4 - a.nv);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
+                      static_cast<T*>(out), mask, static_cast<const T*>(x),
+                      static_cast<const T*>(bias), static_cast<const T*>(residual), a);
 }
 
 template <typename T>
 cudaError_t bwd_impl(void* dx, float* partial, const void* dout, const uint8_t* mask,
                      int64_t rows, int64_t cols, const DropoutRng& rng, cudaStream_t s) {
-    const int64_t nvec = cols / kVec;
-    dim3 grid(static_cast<unsigned>((rows + kBwdRowsPerTile - 1) / kBwdRowsPerTile),
-              static_cast<unsigned>((nvec + kBwdLanes - 1) / kBwdLanes));
-    const PhiloxKey key = make_key(rng.seed);
-    const uint32_t olo = static_cast<uint32_t>(rng.offset);
-    const uint32_t ohi = static_cast<uint32_t>(rng.offset >> 32);
-    if (mask)
-        dropout_bwd_kernel<T, false, kBwdLanes, kBwdU><<<grid, kThreads, 0, s>>>(
-            static_cast<T*>(dx), partial, static_cast<const T*>(dout), mask, rows,
-            static_cast<int>(cols), rng.thr, rng.scale, key, olo, ohi);
-    else
-        dropout_bwd_kernel<T, true, kBwdLanes, kBwdU><<<grid, kThreads, 0, s>>>(
-            static_cast<T*>(dx), partial, static_cast<const T*>(dout), nullptr, rows,
-            static_cast<int>(cols), rng.thr, rng.scale, key, olo, ohi);
-    return cudaGetLastError();
+    BwdArgs a;
+    a.rows = rows;
+    a.cols = static_cast<int>(cols);
+    a.nbands = static_cast<int>((cols + kBwdColsPerTile - 1) / kBwdColsPerTile);
+    a.ntiles = ((rows + kBwdRowsPerTile - 1) / kBwdRowsPerTile) * a.nbands;
+    a.thr = rng.thr;
+    a.scale = rng.scale;
+    a.key = make_key(rng.seed);
+    a.off_lo = static_cast<uint32_t>(rng.offset);
+    a.off_hi = static_cast<uint32_t>(rng.offset >> 32);
+    if (mask) {
+        auto kern = dropout_bwd_kernel<T, false>;
+        static const int occ = occupancy(kern, kThreads, 0);
+        const int64_t grid = std::min<int64_t>(a.ntiles, int64_t{sm_count()} * occ);
+        return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
+                          static_cast<T*>(dx), partial, static_cast<const T*>(dout), mask, a);
+    }
+    auto kern = dropout_bwd_kernel<T, true>;
+    static const int occ = occupancy(kern, kThreads, 0);
+    const int64_t grid = std::min<int64_t>(a.ntiles, int64_t{sm_count()} * occ);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
+                      static_cast<T*>(dx), partial, static_cast<const T*>(dout),
+                      static_cast<const uint8_t*>(nullptr), a);
 }
 
 }  // namespace
@@ -244,14 +377,13 @@ ColReducePlan dropout_bwd_plan(int64_t rows, int64_t cols) {
 
 cudaError_t launch_colreduce(DType dt, void* out0, void* out1, int64_t split,
                              const float* partial, int64_t parts, int64_t width, cudaStream_t s) {
-    const unsigned grid = static_cast<unsigned>((width + kRedCols - 1) / kRedCols);
+    const dim3 grid(static_cast<unsigned>((width + kRedCols - 1) / kRedCols));
+    const dim3 block(kRedCols * kRedGroups);
     if (dt == DType::F16)
-        colreduce_kernel<__half><<<grid, kRedCols * kRedGroups, 0, s>>>(
-            static_cast<__half*>(out0), static_cast<__half*>(out1), split, partial, parts, width);
-    else
-        colreduce_kernel<float><<<grid, kRedCols * kRedGroups, 0, s>>>(
-            static_cast<float*>(out0), static_cast<float*>(out1), split, partial, parts, width);
-    return cudaGetLastError();
+        return launch_pdl(colreduce_kernel<__half>, grid, block, 0, s, static_cast<__half*>(out0),
+                          static_cast<__half*>(out1), split, partial, parts, width);
+    return launch_pdl(colreduce_kernel<float>, grid, block, 0, s, static_cast<float*>(out0),
+                      static_cast<float*>(out1), split, partial, parts, width);
 }
 
 cudaError_t launch_dropout_fwd(DType dt, bool relu, void* out, uint8_t* mask, const void* x,

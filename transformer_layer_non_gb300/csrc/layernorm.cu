@@ -22,26 +22,38 @@ constexpr int kThreads = 256;
 constexpr int kCtaRowThreshold = 256;  // vectors per row held by one warp at most
 
 // ----------------------------------------------------------------------------
-// Forward, group-per-row.
+// Forward, group-per-row, persistent.  Row round k gives group slot q of CTA b
+// the row k*stride + q*gridDim + b (stride = all groups), so a partial last
+// round is spread over every CTA.  For rows of up to 2 vectors per lane each
+// group keeps two register buffers: the next row's loads are in flight while
+// the current row is reduced and stored (wider rows keep one buffer).
+// Loop conditions are warp-uniform (__any_sync) because the groups of one warp
+// reduce with full-warp shuffles.
 // ----------------------------------------------------------------------------
 template <typename T, int LPR, int VPT>
-__global__ void __launch_bounds__(kThreads)
-ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, const T* x,
-                    const T* __restrict__ gamma, const T* __restrict__ beta, int64_t rows,
-                    int cols, float eps) {
-    constexpr int RPC = kThreads / LPR;
-    const int gl = threadIdx.x % LPR;
-    const int64_t r = static_cast<int64_t>(blockIdx.x) * RPC + threadIdx.x / LPR;
-    const bool row_ok = r < rows;
+__device__ __forceinline__ void ln_fwd_load(Raw8<T> (&xr)[VPT], const T* x, int64_t r,
+                                            int64_t rows, int cols, int gl) {
+    if (r >= rows) return;
     const int nvec = cols / kVec;
-    const T* xr = x + (row_ok ? r : 0) * cols;
-
-    float f[VPT][kVec];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = gl + k * LPR;
-        if (row_ok && v < nvec) {
-            load8f<T>(xr + v * kVec, f[k]);
+        if (v < nvec) xr[k] = load8<T>(x + r * cols + v * kVec);
+    }
+}
+
+template <typename T, int LPR, int VPT>
+__device__ __forceinline__ void ln_fwd_row(const Raw8<T> (&xr)[VPT], T* y, float* mean,
+                                           float* rstd, const T* __restrict__ gamma,
+                                           const T* __restrict__ beta, int64_t r, int64_t rows,
+                                           int cols, float eps, int gl) {
+    const bool row_ok = r < rows;
+    const int nvec = cols / kVec;
+    float f[VPT][kVec];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        if (row_ok && gl + k * LPR < nvec) {
+            unpack(xr[k], f[k]);
         } else {
 #pragma unroll
             for (int j = 0; j < kVec; ++j) f[k][j] = 0.f;
@@ -87,6 +99,38 @@ ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, co
     }
 }
 
+template <typename T, int LPR, int VPT>
+__global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : (VPT <= 4 ? 3 : 2))
+ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, const T* x,
+                    const T* __restrict__ gamma, const T* __restrict__ beta, int64_t rows,
+                    int cols, float eps) {
+    constexpr int RPC = kThreads / LPR;
+    pdl_enter();
+    const int gl = threadIdx.x % LPR;
+    const int slot = threadIdx.x / LPR;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * RPC;
+    int64_t r = static_cast<int64_t>(slot) * gridDim.x + blockIdx.x;
+    Raw8<T> xa[VPT], xb[VPT];
+    if (VPT > 2) {
+        // Wide rows: one buffer (a second would cost occupancy).
+        for (; __any_sync(0xffffffffu, r < rows); r += stride) {
+            ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
+            ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gamma, beta, r, rows, cols, eps, gl);
+        }
+        return;
+    }
+    ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
+    while (__any_sync(0xffffffffu, r < rows)) {
+        const int64_t r1 = r + stride;
+        ln_fwd_load<T, LPR, VPT>(xb, x, r1, rows, cols, gl);
+        ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gamma, beta, r, rows, cols, eps, gl);
+        if (!__any_sync(0xffffffffu, r1 < rows)) break;
+        r = r1 + stride;
+        ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
+        ln_fwd_row<T, LPR, VPT>(xb, y, mean, rstd, gamma, beta, r1, rows, cols, eps, gl);
+    }
+}
+
 // ----------------------------------------------------------------------------
 // Forward, CTA-per-row (rows longer than a warp holds).
 // ----------------------------------------------------------------------------
@@ -95,6 +139,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 ln_fwd_cta_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, const T* x,
                   const T* __restrict__ gamma, const T* __restrict__ beta, int cols, float eps) {
     constexpr int NT = WARPS * 32;
+    pdl_enter();
     const int64_t r = blockIdx.x;
     const int nvec = cols / kVec;
     const T* xr = x + r * cols;
@@ -157,12 +202,13 @@ ln_fwd_cta_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, cons
 // order at the end into partial[blockIdx.x, 0:H] and [blockIdx.x, H:2H].
 // ----------------------------------------------------------------------------
 template <typename T, int LPR, int VPT>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kThreads, VPT <= 2 ? 3 : (VPT <= 5 ? 2 : 1))
 ln_bwd_group_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
                     const T* __restrict__ gamma, const float* __restrict__ mean,
-                    const float* __restrict__ rstd, int64_t rows, int cols, int steps) {
+                    const float* __restrict__ rstd, int64_t rows, int cols, int rows_per_cta) {
     constexpr int RPC = kThreads / LPR;  // row slots per CTA
     extern __shared__ __align__(16) float acc[];  // [RPC][2*cols] when partial != nullptr
+    pdl_enter();
     const int gl = threadIdx.x % LPR;
     const int slot = threadIdx.x / LPR;
     const int nvec = cols / kVec;
@@ -179,10 +225,12 @@ ln_bwd_group_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
         if (v < nvec) load8f<T>(gamma + v * kVec, gm[k]);
     }
 
-    const int64_t base = static_cast<int64_t>(blockIdx.x) * RPC * steps;
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * rows_per_cta;
+    const int64_t end = std::min<int64_t>(rows, base + rows_per_cta);
+    const int steps = (rows_per_cta + RPC - 1) / RPC;
     for (int st = 0; st < steps; ++st) {
         const int64_t r = base + static_cast<int64_t>(st) * RPC + slot;
-        const bool row_ok = r < rows;
+        const bool row_ok = r < end;
         Raw8<T> xr[VPT], dr[VPT];
 #pragma unroll
         for (int k = 0; k < VPT; ++k) {
@@ -265,6 +313,7 @@ ln_bwd_cta_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
     constexpr int NT = WARPS * 32;
     extern __shared__ __align__(16) float acc[];  // [2*cols]
     __shared__ float2 part[WARPS];
+    pdl_enter();
     const int nvec = cols / kVec;
     const float inv_n = 1.f / static_cast<float>(cols);
     if (partial)
@@ -357,7 +406,7 @@ struct LnPlan {
     int vpt;      // vectors per lane
     int warps;    // CTA path: warps per row
     int64_t grid;
-    int steps;    // backward: rows (CTA path) or row steps (group path) per CTA
+    int steps;    // backward: rows per CTA (both paths)
 };
 
 // Target number of backward CTAs: about two per SM on a 152-SM part.  It is a
@@ -379,12 +428,12 @@ LnPlan plan_for(int64_t rows, int64_t cols, bool bwd) {
         }
         const int64_t rpc = kThreads / p.lpr;
         if (bwd) {
-            p.steps = static_cast<int>(std::max<int64_t>(1, (rows + rpc * kBwdTargetCtas - 1) /
-                                                                (rpc * kBwdTargetCtas)));
-            p.grid = (rows + rpc * p.steps - 1) / (rpc * p.steps);
+            p.steps = static_cast<int>(
+                std::max<int64_t>(1, (rows + kBwdTargetCtas - 1) / kBwdTargetCtas));
+            p.grid = (rows + p.steps - 1) / p.steps;
         } else {
             p.steps = 1;
-            p.grid = (rows + rpc - 1) / rpc;
+            p.grid = (rows + rpc - 1) / rpc;  // upper bound; the launcher caps it
         }
     } else {
         p.cta = true;
@@ -409,24 +458,36 @@ cudaError_t set_smem(K kernel, size_t bytes) {
                                 static_cast<int>(bytes));
 }
 
+template <typename K>
+int occupancy(K kernel, int threads, size_t smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
+        n < 1)
+        n = 1;
+    return n;
+}
+
 template <typename T, int LPR, int VPT>
 cudaError_t fwd_group(void* y, float* mean, float* rstd, const void* x, const void* gamma,
                       const void* beta, int64_t rows, int64_t cols, float eps, const LnPlan& p,
                       cudaStream_t s) {
-    ln_fwd_group_kernel<T, LPR, VPT><<<static_cast<unsigned>(p.grid), kThreads, 0, s>>>(
-        static_cast<T*>(y), mean, rstd, static_cast<const T*>(x), static_cast<const T*>(gamma),
-        static_cast<const T*>(beta), rows, static_cast<int>(cols), eps);
-    return cudaGetLastError();
+    auto kern = ln_fwd_group_kernel<T, LPR, VPT>;
+    static const int occ = occupancy(kern, kThreads, 0);
+    const int64_t grid = std::min<int64_t>(p.grid, int64_t{sm_count()} * occ);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
+                      static_cast<T*>(y), mean, rstd, static_cast<const T*>(x),
+                      static_cast<const T*>(gamma), static_cast<const T*>(beta), rows,
+                      static_cast<int>(cols), eps);
 }
 
 template <typename T, int WARPS, int VPT>
 cudaError_t fwd_cta(void* y, float* mean, float* rstd, const void* x, const void* gamma,
                     const void* beta, int64_t rows, int64_t cols, float eps, const LnPlan& p,
                     cudaStream_t s) {
-    ln_fwd_cta_kernel<T, WARPS, VPT><<<static_cast<unsigned>(p.grid), WARPS * 32, 0, s>>>(
-        static_cast<T*>(y), mean, rstd, static_cast<const T*>(x), static_cast<const T*>(gamma),
-        static_cast<const T*>(beta), static_cast<int>(cols), eps);
-    return cudaGetLastError();
+    return launch_pdl(ln_fwd_cta_kernel<T, WARPS, VPT>, dim3(static_cast<unsigned>(p.grid)),
+                      dim3(WARPS * 32), 0, s, static_cast<T*>(y), mean, rstd,
+                      static_cast<const T*>(x), static_cast<const T*>(gamma),
+                      static_cast<const T*>(beta), static_cast<int>(cols), eps);
 }
 
 template <typename T, int LPR, int VPT>
@@ -438,10 +499,10 @@ cudaError_t bwd_group(void* dx, float* partial, const void* dy, const void* x, c
     auto kern = ln_bwd_group_kernel<T, LPR, VPT>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(p.grid), kThreads, smem, s>>>(
-        static_cast<T*>(dx), partial, static_cast<const T*>(dy), static_cast<const T*>(x),
-        static_cast<const T*>(gamma), mean, rstd, rows, static_cast<int>(cols), p.steps);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(p.grid)), dim3(kThreads), smem, s,
+                      static_cast<T*>(dx), partial, static_cast<const T*>(dy),
+                      static_cast<const T*>(x), static_cast<const T*>(gamma), mean, rstd, rows,
+                      static_cast<int>(cols), p.steps);
 }
 
 template <typename T, int WARPS, int VPT>
@@ -452,10 +513,10 @@ cudaError_t bwd_cta(void* dx, float* partial, const void* dy, const void* x, con
     auto kern = ln_bwd_cta_kernel<T, WARPS, VPT>;
     cudaError_t e = set_smem(kern, smem);
     if (e != cudaSuccess) return e;
-    kern<<<static_cast<unsigned>(p.grid), WARPS * 32, smem, s>>>(
-        static_cast<T*>(dx), partial, static_cast<const T*>(dy), static_cast<const T*>(x),
-        static_cast<const T*>(gamma), mean, rstd, rows, static_cast<int>(cols), p.steps);
-    return cudaGetLastError();
+    return launch_pdl(kern, dim3(static_cast<unsigned>(p.grid)), dim3(WARPS * 32), smem, s,
+                      static_cast<T*>(dx), partial, static_cast<const T*>(dy),
+                      static_cast<const T*>(x), static_cast<const T*>(gamma), mean, rstd, rows,
+                      static_cast<int>(cols), p.steps);
 }
 
 // Expand a runtime (lpr, vpt) or (warps, vpt) into a template instance.

@@ -9,6 +9,7 @@
 #include <string.h>
 
 #include <algorithm>
+#include <atomic>
 
 #include "../../include/ls_ops.h"
 #include "ls_internal.h"
@@ -128,6 +129,23 @@ constexpr int64_t kMaxDropoutCols = int64_t{1} << 22;
     } while (0)
 
 }  // namespace
+
+int ls::sm_count() {
+    static std::atomic<int> cache[64];
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 1;
+    if (dev >= 64) {
+        int n = 0;
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+        return n > 0 ? n : 1;
+    }
+    int n = cache[dev].load(std::memory_order_relaxed);
+    if (n > 0) return n;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+        n = 1;
+    cache[dev].store(n, std::memory_order_relaxed);
+    return n;
+}
 
 void ls::set_last_error_message(const char* fmt, ...) {
     va_list ap;

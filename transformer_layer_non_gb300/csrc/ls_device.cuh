@@ -111,18 +111,34 @@ struct PhiloxKey {
     uint32_t k0, k1;
 };
 
-__device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
-    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
+// The ten round keys of one 64-bit key (key + r * Weyl constant).  Computed
+// once per thread from kernel arguments, so they are the same in every thread
+// and every call.
+struct PhiloxSchedule {
+    uint32_t k0[10], k1[10];
+};
+
+__device__ __forceinline__ PhiloxSchedule philox_schedule(PhiloxKey key) {
     constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
-    uint32_t k0 = key.k0, k1 = key.k1;
+    PhiloxSchedule s;
+#pragma unroll
+    for (int r = 0; r < 10; ++r) {
+        s.k0[r] = key.k0 + static_cast<uint32_t>(r) * W0;
+        s.k1[r] = key.k1 + static_cast<uint32_t>(r) * W1;
+    }
+    return s;
+}
+
+__device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxSchedule& ks) {
+    constexpr uint32_t M0 = 0xD2511F53u, M1 = 0xCD9E8D57u;
 #pragma unroll
     for (int round = 0; round < 10; ++round) {
         const uint64_t p0 = static_cast<uint64_t>(M0) * c.x;
         const uint64_t p1 = static_cast<uint64_t>(M1) * c.z;
-        c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ k0, static_cast<uint32_t>(p1),
-                       static_cast<uint32_t>(p0 >> 32) ^ c.w ^ k1, static_cast<uint32_t>(p0));
-        k0 += W0;
-        k1 += W1;
+        c = make_uint4(static_cast<uint32_t>(p1 >> 32) ^ c.y ^ ks.k0[round],
+                       static_cast<uint32_t>(p1),
+                       static_cast<uint32_t>(p0 >> 32) ^ c.w ^ ks.k1[round],
+                       static_cast<uint32_t>(p0));
     }
     return c;
 }
@@ -130,16 +146,16 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, PhiloxKey key) {
 // Dropout keep bits of the 8 consecutive elements starting at flat index i
 // (i a multiple of 4): element i+j draws word j&3 of counter block (i>>2)+(j>>2).
 // Bit j of the result is set iff element i+j is kept (word >= thr).
-__device__ __forceinline__ uint32_t keep_bits8(uint64_t i, uint32_t thr, PhiloxKey key,
+__device__ __forceinline__ uint32_t keep_bits8(uint64_t i, uint32_t thr, const PhiloxSchedule& ks,
                                                uint32_t off_lo, uint32_t off_hi) {
     const uint64_t blk = i >> 2;
     const uint4 a = philox4x32_10(
         make_uint4(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), off_lo, off_hi),
-        key);
+        ks);
     const uint64_t blk1 = blk + 1;
     const uint4 b = philox4x32_10(
         make_uint4(static_cast<uint32_t>(blk1), static_cast<uint32_t>(blk1 >> 32), off_lo, off_hi),
-        key);
+        ks);
     return (a.x >= thr ? 1u : 0u) | (a.y >= thr ? 2u : 0u) | (a.z >= thr ? 4u : 0u) |
            (a.w >= thr ? 8u : 0u) | (b.x >= thr ? 16u : 0u) | (b.y >= thr ? 32u : 0u) |
            (b.z >= thr ? 64u : 0u) | (b.w >= thr ? 128u : 0u);
@@ -167,6 +183,42 @@ template <int W> __device__ __forceinline__ float2 group_sum2(float2 v) {
         v.y += __shfl_xor_sync(0xffffffffu, v.y, o);
     }
     return v;
+}
+
+}  // namespace ls
+
+namespace ls {
+
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel is launched with programmatic
+// stream serialisation, so the next kernel on the stream may be scheduled
+// while this one drains.  A kernel therefore waits for its predecessor's
+// completion (and memory flush) before its first global access, then lets its
+// own successor launch.  Launched without the attribute, both are no-ops.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+__device__ __forceinline__ void pdl_enter() {
+    pdl_wait();
+    pdl_trigger();
+}
+
+template <typename... KArgs, typename... Args>
+inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                              cudaStream_t stream, Args... args) {
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
 }
 
 }  // namespace ls

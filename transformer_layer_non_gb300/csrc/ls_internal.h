@@ -62,6 +62,9 @@ cudaError_t launch_softmax_bwd(DType dt, void* dx, const void* y, const void* dy
 
 constexpr int64_t kMaxRowLen = 16384;
 
+// Streaming multiprocessors of the current device (queried once per device).
+int sm_count();
+
 // Set this host thread's ls_last_error() message (printf-style).
 void set_last_error_message(const char* fmt, ...);
 

@@ -17,6 +17,8 @@
 // least one valid key; masked outputs are written as exact zeros.
 #include <math.h>
 
+#include <algorithm>
+
 #include "ls_device.cuh"
 #include "ls_internal.h"
 
@@ -50,26 +52,49 @@ __device__ __forceinline__ int valid_len(int64_t row, int k_len, const RowMask& 
 }
 
 // ----------------------------------------------------------------------------
-// Group-per-row kernels.
+// Group-per-row kernels, persistent.  Row round k gives group slot q of CTA b
+// the row k*stride + q*gridDim + b, so the partial last round is spread over
+// every CTA.  For rows of up to 2 vectors per lane, two register buffers per
+// group: the next row's loads are in flight while the current row is reduced
+// and stored (wider rows keep one buffer and rely on occupancy).  Loop
+// conditions are warp-uniform because the groups of a warp reduce with
+// full-warp shuffles.
 // ----------------------------------------------------------------------------
 template <typename T, int LPR, int VPT>
-__global__ void __launch_bounds__(kThreads)
-softmax_fwd_group_kernel(T* y, const T* x, int64_t nrows, int k_len, RowMask mk) {
-    constexpr int RPC = kThreads / LPR;
-    const int gl = threadIdx.x % LPR;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * RPC + threadIdx.x / LPR;
-    const bool row_ok = row < nrows;
-    const int vlen = row_ok ? valid_len(row, k_len, mk) : 0;
-    const int nvec = k_len / kVec;
-    const int64_t base = (row_ok ? row : 0) * k_len;
+struct RowBuf {
+    Raw8<T> a[VPT];  // x (forward) or y (backward)
+    Raw8<T> b[VPT];  // dy (backward only)
+    int vlen;
+};
 
+template <typename T, int LPR, int VPT, bool BWD>
+__device__ __forceinline__ void sm_load(RowBuf<T, LPR, VPT>& buf, const T* p, const T* q,
+                                        int64_t row, int64_t nrows, int k_len,
+                                        const RowMask& mk, int gl) {
+    buf.vlen = row < nrows ? valid_len(row, k_len, mk) : 0;
+    const int64_t base = row * k_len;
+#pragma unroll
+    for (int k = 0; k < VPT; ++k) {
+        const int v = gl + k * LPR;
+        if (v * kVec < buf.vlen) {
+            buf.a[k] = load8<T>(p + base + v * kVec);
+            if (BWD) buf.b[k] = load8<T>(q + base + v * kVec);
+        }
+    }
+}
+
+template <typename T, int LPR, int VPT>
+__device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y, int64_t row,
+                                           int64_t nrows, int k_len, int gl) {
+    const int nvec = k_len / kVec;
+    const int vlen = buf.vlen;
     float f[VPT][kVec];
     float m = -INFINITY;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = gl + k * LPR;
         if (v * kVec < vlen) {
-            load8f<T>(x + base + v * kVec, f[k]);
+            unpack(buf.a[k], f[k]);
 #pragma unroll
             for (int j = 0; j < kVec; ++j)
                 if (v * kVec + j < vlen) m = fmaxf(m, f[k][j]);
@@ -90,8 +115,9 @@ softmax_fwd_group_kernel(T* y, const T* x, int64_t nrows, int k_len, RowMask mk)
         }
     }
     s = group_sum<LPR>(s);
+    if (row >= nrows) return;
     const float inv = s > 0.f ? 1.f / s : 0.f;
-    if (!row_ok) return;
+    const int64_t base = row * k_len;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = gl + k * LPR;
@@ -105,40 +131,26 @@ softmax_fwd_group_kernel(T* y, const T* x, int64_t nrows, int k_len, RowMask mk)
 }
 
 template <typename T, int LPR, int VPT>
-__global__ void __launch_bounds__(kThreads)
-softmax_bwd_group_kernel(T* dx, const T* y, const T* dy, int64_t nrows, int k_len, RowMask mk) {
-    constexpr int RPC = kThreads / LPR;
-    const int gl = threadIdx.x % LPR;
-    const int64_t row = static_cast<int64_t>(blockIdx.x) * RPC + threadIdx.x / LPR;
-    const bool row_ok = row < nrows;
-    const int vlen = row_ok ? valid_len(row, k_len, mk) : 0;
+__device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx, int64_t row,
+                                           int64_t nrows, int k_len, int gl) {
     const int nvec = k_len / kVec;
-    const int64_t base = (row_ok ? row : 0) * k_len;
-
-    Raw8<T> yr[VPT], dr[VPT];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int v = gl + k * LPR;
-        if (v * kVec < vlen) {
-            yr[k] = load8<T>(y + base + v * kVec);
-            dr[k] = load8<T>(dy + base + v * kVec);
-        }
-    }
+    const int vlen = buf.vlen;
     float dot = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = gl + k * LPR;
         if (v * kVec < vlen) {
             float yf[kVec], df[kVec];
-            unpack(yr[k], yf);
-            unpack(dr[k], df);
+            unpack(buf.a[k], yf);
+            unpack(buf.b[k], df);
 #pragma unroll
             for (int j = 0; j < kVec; ++j)
                 if (v * kVec + j < vlen) dot = fmaf(yf[j], df[j], dot);
         }
     }
     dot = group_sum<LPR>(dot);
-    if (!row_ok) return;
+    if (row >= nrows) return;
+    const int64_t base = row * k_len;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = gl + k * LPR;
@@ -146,8 +158,8 @@ softmax_bwd_group_kernel(T* dx, const T* y, const T* dy, int64_t nrows, int k_le
             float o[kVec];
             if (v * kVec < vlen) {
                 float yf[kVec], df[kVec];
-                unpack(yr[k], yf);
-                unpack(dr[k], df);
+                unpack(buf.a[k], yf);
+                unpack(buf.b[k], df);
 #pragma unroll
                 for (int j = 0; j < kVec; ++j)
                     o[j] = (v * kVec + j < vlen) ? yf[j] * (df[j] - dot) : 0.f;
@@ -157,6 +169,46 @@ softmax_bwd_group_kernel(T* dx, const T* y, const T* dy, int64_t nrows, int k_le
             }
             store8f<T>(dx + base + v * kVec, o);
         }
+    }
+}
+
+// BWD = false: out = y, p = x.   BWD = true: out = dx, p = y, q = dy.
+template <typename T, int LPR, int VPT, bool BWD>
+__global__ void __launch_bounds__(kThreads, (sizeof(T) == 2 && (VPT == 1 || (BWD && VPT == 2))) ? 4 : 3)
+softmax_group_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, RowMask mk) {
+    constexpr int RPC = kThreads / LPR;
+    pdl_enter();
+    const int gl = threadIdx.x % LPR;
+    const int slot = threadIdx.x / LPR;
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * RPC;
+    int64_t r = static_cast<int64_t>(slot) * gridDim.x + blockIdx.x;
+    RowBuf<T, LPR, VPT> ba, bb;
+    if (VPT > 2) {
+        // Wide rows: one buffer (a second would cost occupancy).
+        for (; __any_sync(0xffffffffu, r < nrows); r += stride) {
+            sm_load<T, LPR, VPT, BWD>(ba, p, q, r, nrows, k_len, mk, gl);
+            if (BWD)
+                sm_bwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
+            else
+                sm_fwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
+        }
+        return;
+    }
+    sm_load<T, LPR, VPT, BWD>(ba, p, q, r, nrows, k_len, mk, gl);
+    while (__any_sync(0xffffffffu, r < nrows)) {
+        const int64_t r1 = r + stride;
+        sm_load<T, LPR, VPT, BWD>(bb, p, q, r1, nrows, k_len, mk, gl);
+        if (BWD)
+            sm_bwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
+        else
+            sm_fwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
+        if (!__any_sync(0xffffffffu, r1 < nrows)) break;
+        r = r1 + stride;
+        sm_load<T, LPR, VPT, BWD>(ba, p, q, r, nrows, k_len, mk, gl);
+        if (BWD)
+            sm_bwd_row<T, LPR, VPT>(bb, out, r1, nrows, k_len, gl);
+        else
+            sm_fwd_row<T, LPR, VPT>(bb, out, r1, nrows, k_len, gl);
     }
 }
 
@@ -191,6 +243,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 softmax_fwd_cta_kernel(T* y, const T* x, int k_len, RowMask mk) {
     constexpr int NT = WARPS * 32;
     __shared__ float red[WARPS];
+    pdl_enter();
     const int64_t row = blockIdx.x;
     const int vlen = valid_len(row, k_len, mk);
     const int nvec = k_len / kVec;
@@ -240,6 +293,7 @@ __global__ void __launch_bounds__(WARPS * 32)
 softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk) {
     constexpr int NT = WARPS * 32;
     __shared__ float red[WARPS];
+    pdl_enter();
     const int64_t row = blockIdx.x;
     const int vlen = valid_len(row, k_len, mk);
     const int nvec = k_len / kVec;
@@ -331,33 +385,49 @@ RowMask make_mask(const SoftmaxShape& sh) {
     return m;
 }
 
+template <typename K>
+int occupancy(K kernel, int threads, size_t smem) {
+    int n = 0;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem) != cudaSuccess ||
+        n < 1)
+        n = 1;
+    return n;
+}
+
+template <typename T, int LPR, int VPT, bool BWD>
+cudaError_t group_launch(T* out, const T* p, const T* q, int64_t nrows, int k_len,
+                         const RowMask& m, const SmPlan& pl, cudaStream_t s) {
+    auto kern = softmax_group_kernel<T, LPR, VPT, BWD>;
+    static const int occ = occupancy(kern, kThreads, 0);
+    const int64_t grid = std::min<int64_t>(pl.grid, int64_t{sm_count()} * occ);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, out, p, q,
+                      nrows, k_len, m);
+}
 template <typename T, int LPR, int VPT>
 cudaError_t fwd_group(void* y, const void* x, int64_t nrows, int k_len, const RowMask& m,
                       const SmPlan& p, cudaStream_t s) {
-    softmax_fwd_group_kernel<T, LPR, VPT><<<static_cast<unsigned>(p.grid), kThreads, 0, s>>>(
-        static_cast<T*>(y), static_cast<const T*>(x), nrows, k_len, m);
-    return cudaGetLastError();
+    return group_launch<T, LPR, VPT, false>(static_cast<T*>(y), static_cast<const T*>(x),
+                                            static_cast<const T*>(nullptr), nrows, k_len, m, p, s);
 }
 template <typename T, int LPR, int VPT>
 cudaError_t bwd_group(void* dx, const void* y, const void* dy, int64_t nrows, int k_len,
                       const RowMask& m, const SmPlan& p, cudaStream_t s) {
-    softmax_bwd_group_kernel<T, LPR, VPT><<<static_cast<unsigned>(p.grid), kThreads, 0, s>>>(
-        static_cast<T*>(dx), static_cast<const T*>(y), static_cast<const T*>(dy), nrows, k_len, m);
-    return cudaGetLastError();
+    return group_launch<T, LPR, VPT, true>(static_cast<T*>(dx), static_cast<const T*>(y),
+                                           static_cast<const T*>(dy), nrows, k_len, m, p, s);
 }
 template <typename T, int WARPS, int VPT>
 cudaError_t fwd_cta(void* y, const void* x, int64_t nrows, int k_len, const RowMask& m,
                     const SmPlan& p, cudaStream_t s) {
-    softmax_fwd_cta_kernel<T, WARPS, VPT><<<static_cast<unsigned>(p.grid), WARPS * 32, 0, s>>>(
-        static_cast<T*>(y), static_cast<const T*>(x), k_len, m);
-    return cudaGetLastError();
+    return launch_pdl(softmax_fwd_cta_kernel<T, WARPS, VPT>, dim3(static_cast<unsigned>(p.grid)),
+                      dim3(WARPS * 32), 0, s, static_cast<T*>(y), static_cast<const T*>(x), k_len,
+                      m);
 }
 template <typename T, int WARPS, int VPT>
 cudaError_t bwd_cta(void* dx, const void* y, const void* dy, int64_t nrows, int k_len,
                     const RowMask& m, const SmPlan& p, cudaStream_t s) {
-    softmax_bwd_cta_kernel<T, WARPS, VPT><<<static_cast<unsigned>(p.grid), WARPS * 32, 0, s>>>(
-        static_cast<T*>(dx), static_cast<const T*>(y), static_cast<const T*>(dy), k_len, m);
-    return cudaGetLastError();
+    return launch_pdl(softmax_bwd_cta_kernel<T, WARPS, VPT>, dim3(static_cast<unsigned>(p.grid)),
+                      dim3(WARPS * 32), 0, s, static_cast<T*>(dx), static_cast<const T*>(y),
+                      static_cast<const T*>(dy), k_len, m);
 }
 
 #define LS_SM_GROUP_CASES(FN, T, ...)                                    \

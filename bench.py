@@ -202,8 +202,7 @@ class LayerStep:
         self.outputs = sorted(out)
         self.t = {k: dev(v) for k, v in host.items()}
         self.t.update(out)
-        ws = max(ls_ops.colreduce_workspace_bytes(T, F), ls_ops.colreduce_workspace_bytes(T, H))
-        self.workspace = torch.empty(ws, dtype=torch.uint8, device=device)
+        self.workspace = ls_ops.new_workspace([(T, F), (T, H)], device=device)
         self.bytes = accounting.layer_step_bytes(T, H, F, L.batch, L.heads, L.seq, self.esize,
                                                  self.key_len_np, L.causal)
         self.launches = {k: 1 for k in self.bytes}

@@ -83,6 +83,17 @@ const char* ls_last_error(void);
 /* Library version, major*10000 + minor*100 + patch. */
 int ls_version(void);
 
+/* Device-side failure flags raised since the previous call, cleared by this
+ * call.  Kernels that stream rows through shared memory with bulk copies wait
+ * for each copy with a bounded number of polls; if a wait runs out (a healthy
+ * GPU never gets there), the kernel sets LS_DEVERR_WAIT_TIMEOUT, lets its
+ * copies in flight land, and stops early: the outputs of that call are
+ * incomplete.  Unlike every other entry point this one synchronises: it waits
+ * for all work on the current device before reading the flags.  *flags gets
+ * the OR of the flags (0 = none). */
+#define LS_DEVERR_WAIT_TIMEOUT 1u
+ls_status ls_check_device_errors(uint32_t* flags);
+
 /* Workspace bytes that the backward calls with a column reduction
  * (ls_bias_dropout_residual_bwd, ls_bias_relu_dropout_bwd, ls_layernorm_bwd)
  * need for an activation of shape [rows, cols]; enough for all three. */

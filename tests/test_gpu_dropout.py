@@ -176,3 +176,4 @@ def test_bias_grad_is_deterministic():
     b = run_dropout_bwd(True, dout, m, 0.1)
     np.testing.assert_array_equal(a[1], b[1])
     np.testing.assert_array_equal(a[0], b[0])
+

@@ -41,7 +41,7 @@ def run_bwd(dy, x, g, mean32, rstd32):
     dg = Guarded((cols,), tdtype(x.dtype))
     db = Guarded((cols,), tdtype(x.dtype))
     ws = torch.empty(max(ls_ops.colreduce_workspace_bytes(rows, cols), 16), dtype=torch.uint8,
-                     device="cuda").fill_(0xFF)
+                     device="cuda").fill_(0xFF)  # garbage: the workspace needs no init
     ls_ops.ls_layernorm_bwd(dx.t, dg.t, db.t, dev(dy), dev(x), dev(g), dev(mean32), dev(rstd32),
                             workspace=ws)
     torch.cuda.synchronize()

@@ -147,3 +147,13 @@ def test_no_mask_and_in_place():
     ls_ops.ls_softmax_bwd(dyt, dev(y16), dyt)  # dx over dy
     torch.cuda.synchronize()
     assert_close(f64(dyt), oracle.softmax_bwd(y16, dy), "in-place dx")
+
+
+def test_no_device_side_failures_after_streamed_rows():
+    # The warp-per-row softmax streams rows through shared memory with bulk
+    # copies and bounded waits; none of the calls above may have timed out.
+    require_gpu()
+    x, dy, kl = synth.sweep_inputs(512)
+    y = run_fwd(x, kl, False)
+    run_bwd(y, dy, kl, False)
+    assert ls_ops.check_device_errors() == 0

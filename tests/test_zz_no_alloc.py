@@ -30,8 +30,7 @@ def _case(seed, rows, cols):
 def _with_workspace(x, dy, g, mean, rstd):
     rows, cols = x.shape
     dx, dg, db = torch.empty_like(x), torch.empty_like(g), torch.empty_like(g)
-    ws = torch.empty(ls_ops.colreduce_workspace_bytes(rows, cols), dtype=torch.uint8,
-                     device="cuda")
+    ws = ls_ops.new_workspace([(rows, cols)])
     ls_ops.ls_layernorm_bwd(dx, dg, db, dy, x, g, mean, rstd, workspace=ws)
     return dx, dg, db
 

@@ -354,22 +354,20 @@ cudaError_t bwd_impl(void* dx, float* partial, const void* dout, const uint8_t* 
     a.key = make_key(rng.seed);
     a.off_lo = static_cast<uint32_t>(rng.offset);
     a.off_hi = static_cast<uint32_t>(rng.offset >> 32);
-    if (mask) {
-        auto kern = dropout_bwd_kernel<T, false>;
-        static const int occ = occupancy(kern, kThreads, 0);
-        const int64_t grid = std::min<int64_t>(a.ntiles, int64_t{sm_count()} * occ);
-        return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
-                          static_cast<T*>(dx), partial, static_cast<const T*>(dout), mask, a);
-    }
-    auto kern = dropout_bwd_kernel<T, true>;
-    static const int occ = occupancy(kern, kThreads, 0);
+    auto kern = mask ? dropout_bwd_kernel<T, false> : dropout_bwd_kernel<T, true>;
+    static const int occ_mask = occupancy(dropout_bwd_kernel<T, false>, kThreads, 0);
+    static const int occ_regen = occupancy(dropout_bwd_kernel<T, true>, kThreads, 0);
+    const int occ = mask ? occ_mask : occ_regen;
     const int64_t grid = std::min<int64_t>(a.ntiles, int64_t{sm_count()} * occ);
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
-                      static_cast<T*>(dx), partial, static_cast<const T*>(dout),
-                      static_cast<const uint8_t*>(nullptr), a);
+                      static_cast<T*>(dx), partial, static_cast<const T*>(dout), mask, a);
 }
 
 }  // namespace
+
+cudaError_t dropout_take_device_error(unsigned int* flags) {
+    return take_device_error_word(flags);
+}
 
 ColReducePlan dropout_bwd_plan(int64_t rows, int64_t cols) {
     return ColReducePlan{(rows + kBwdRowsPerTile - 1) / kBwdRowsPerTile, cols};

@@ -100,7 +100,7 @@ __device__ __forceinline__ void ln_fwd_row(const Raw8<T> (&xr)[VPT], T* y, float
 }
 
 template <typename T, int LPR, int VPT>
-__global__ void __launch_bounds__(kThreads, VPT <= 3 ? 4 : (VPT <= 4 ? 3 : 2))
+__global__ void __launch_bounds__(kThreads, min_ctas<T>(VPT <= 3 ? 4 : (VPT <= 4 ? 3 : 2)))
 ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, const T* x,
                     const T* __restrict__ gamma, const T* __restrict__ beta, int64_t rows,
                     int cols, float eps) {
@@ -202,7 +202,7 @@ ln_fwd_cta_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, cons
 // order at the end into partial[blockIdx.x, 0:H] and [blockIdx.x, H:2H].
 // ----------------------------------------------------------------------------
 template <typename T, int LPR, int VPT>
-__global__ void __launch_bounds__(kThreads, VPT <= 2 ? 3 : (VPT <= 5 ? 2 : 1))
+__global__ void __launch_bounds__(kThreads, min_ctas<T>(VPT <= 2 ? 3 : (VPT <= 5 ? 2 : 1)))
 ln_bwd_group_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
                     const T* __restrict__ gamma, const float* __restrict__ mean,
                     const float* __restrict__ rstd, int64_t rows, int cols, int rows_per_cta) {
@@ -298,6 +298,152 @@ ln_bwd_group_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
         float t = 0.f;
         for (int q = 0; q < RPC; ++q) t += acc[static_cast<size_t>(q) * 2 * cols + k];
         partial[static_cast<int64_t>(blockIdx.x) * 2 * cols + k] = t;
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Backward, warp per row, rows fed by bulk copies (256 <= H <= 1280).  CTA b
+// owns rows [b*R, (b+1)*R) (R from the shape-only plan); warp w takes rows
+// b*R + w + 8k.  Each warp's x and dy rows arrive in a two-stage ring of shared
+// memory (cp.async.bulk, bounded mbarrier waits), so both of a warp's rows are
+// in flight at once without holding them in registers.  dgamma/dbeta partial
+// sums stay in registers (each lane owns the same columns in every row); when
+// all rows are done the warps' sums are added in warp order through the
+// (now free) stage memory into partial[b, 0:2H].
+// ----------------------------------------------------------------------------
+constexpr int kLnTmaWarps = 8;
+constexpr int kLnTmaStages = 2;
+constexpr uint32_t kLnTmaBarBytes = 128;  // 8 warps x 2 stages x 8 bytes
+// Shared-memory layout: barriers | gamma (cols, rounded to 128 B) | stages.
+__host__ __device__ inline size_t ln_tma_gamma_bytes(int cols, size_t esize) {
+    return ((static_cast<size_t>(cols) * esize + 127) / 128) * 128;
+}
+
+template <typename T, int VPT>
+__global__ void __launch_bounds__(kLnTmaWarps * 32, 2)
+ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
+                  const T* __restrict__ gamma, const float* __restrict__ mean,
+                  const float* __restrict__ rstd, int64_t rows, int cols, int rows_per_cta) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int S = kLnTmaStages;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t row_bytes = static_cast<uint32_t>(cols) * sizeof(T);
+    const uint32_t stage_bytes = 2 * row_bytes;
+    T* gsm = reinterpret_cast<T*>(smem + kLnTmaBarBytes);
+    unsigned char* data = smem + kLnTmaBarBytes + ln_tma_gamma_bytes(cols, sizeof(T));
+    WarpRing<S> ring;
+    ring.init(reinterpret_cast<uint64_t*>(smem) + warp * S,
+              data + static_cast<size_t>(warp) * S * stage_bytes, stage_bytes);
+    pdl_enter();
+    const int nvec = cols / kVec;
+    for (int v = threadIdx.x; v < nvec; v += kLnTmaWarps * 32)
+        store8<T>(gsm + v * kVec, load8<T>(gamma + v * kVec));
+    const float inv_n = 1.f / static_cast<float>(cols);
+    const int64_t base = static_cast<int64_t>(blockIdx.x) * rows_per_cta;
+    const int64_t end = std::min<int64_t>(rows, base + rows_per_cta);
+    float ag[VPT][kVec], ab[VPT][kVec];
+#pragma unroll
+    for (int k = 0; k < VPT; ++k)
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) ag[k][j] = ab[k][j] = 0.f;
+    uint32_t parity[S] = {0, 0};
+    float mu_of[S], rs_of[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        const int64_t r = base + warp + s * kLnTmaWarps;
+        if (r < end) {
+            ring.issue(s, x + r * cols, row_bytes, dy + r * cols, row_bytes, row_bytes);
+            mu_of[s] = mean[r];
+            rs_of[s] = rstd[r];
+        }
+    }
+    bool failed = false;
+    __syncthreads();  // gamma staged
+    for (int k = 0;; ++k) {
+        const int64_t r = base + warp + static_cast<int64_t>(k) * kLnTmaWarps;
+        if (r >= end) break;
+        const int s = k % S;
+        const bool ok = ring.wait(s, parity[s]);
+        if (!__all_sync(0xffffffffu, ok)) {
+            ring.drain(parity);
+            failed = true;
+            break;
+        }
+        parity[s] ^= 1u;
+        const float mu = mu_of[s], rs = rs_of[s];
+        const T* xs = reinterpret_cast<const T*>(ring.stage(s));
+        const T* ds = reinterpret_cast<const T*>(ring.stage(s) + row_bytes);
+        float2 sum = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int k2 = 0; k2 < VPT; ++k2) {
+            const int v = lane + k2 * 32;
+            if (v < nvec) {
+                float xf[kVec], df[kVec], gf[kVec];
+                unpack(load8_smem<T>(xs + v * kVec), xf);
+                unpack(load8_smem<T>(ds + v * kVec), df);
+                unpack(load8_smem<T>(gsm + v * kVec), gf);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) {
+                    const float g = gf[j] * df[j];
+                    sum.x += g;
+                    sum.y = fmaf(g, (xf[j] - mu) * rs, sum.y);
+                }
+            }
+        }
+        sum = group_sum2<32>(sum);  // the single synchronisation
+        const float a_n = sum.x * inv_n, c_n = sum.y * inv_n;
+#pragma unroll
+        for (int k2 = 0; k2 < VPT; ++k2) {
+            const int v = lane + k2 * 32;
+            if (v < nvec) {
+                float xf[kVec], df[kVec], gf[kVec], o[kVec];
+                unpack(load8_smem<T>(xs + v * kVec), xf);
+                unpack(load8_smem<T>(ds + v * kVec), df);
+                unpack(load8_smem<T>(gsm + v * kVec), gf);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) {
+                    const float xh = (xf[j] - mu) * rs;
+                    o[j] = rs * (gf[j] * df[j] - a_n - xh * c_n);
+                    ag[k2][j] = fmaf(df[j], xh, ag[k2][j]);
+                    ab[k2][j] += df[j];
+                }
+                store8f<T>(dx + r * cols + v * kVec, o);
+            }
+        }
+        __syncwarp();  // every lane has used its reads of stage s
+        const int64_t rn = r + S * kLnTmaWarps;
+        if (rn < end) {
+            ring.issue(s, x + rn * cols, row_bytes, dy + rn * cols, row_bytes, row_bytes);
+            mu_of[s] = mean[rn];
+            rs_of[s] = rstd[rn];
+        }
+    }
+    if (partial == nullptr) return;
+    // Cross-warp sum of the parameter-gradient partials, in warp order, through
+    // the stage memory (every copy has landed and been read).
+    __syncthreads();
+    float* red = reinterpret_cast<float*>(data);  // [8 warps][2*cols]
+    float* mine = red + static_cast<size_t>(warp) * 2 * cols;
+#pragma unroll
+    for (int k2 = 0; k2 < VPT; ++k2) {
+        const int v = lane + k2 * 32;
+        if (v < nvec) {
+            float4* pg = reinterpret_cast<float4*>(mine + v * kVec);
+            float4* pb = reinterpret_cast<float4*>(mine + cols + v * kVec);
+            pg[0] = make_float4(ag[k2][0], ag[k2][1], ag[k2][2], ag[k2][3]);
+            pg[1] = make_float4(ag[k2][4], ag[k2][5], ag[k2][6], ag[k2][7]);
+            pb[0] = make_float4(ab[k2][0], ab[k2][1], ab[k2][2], ab[k2][3]);
+            pb[1] = make_float4(ab[k2][4], ab[k2][5], ab[k2][6], ab[k2][7]);
+        }
+    }
+    __syncthreads();
+    (void)failed;
+    for (int c = threadIdx.x; c < 2 * cols; c += kLnTmaWarps * 32) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kLnTmaWarps; ++w) t += red[static_cast<size_t>(w) * 2 * cols + c];
+        partial[static_cast<int64_t>(blockIdx.x) * 2 * cols + c] = t;
     }
 }
 
@@ -494,6 +640,20 @@ template <typename T, int LPR, int VPT>
 cudaError_t bwd_group(void* dx, float* partial, const void* dy, const void* x, const void* gamma,
                       const float* mean, const float* rstd, int64_t rows, int64_t cols,
                       const LnPlan& p, cudaStream_t s) {
+    if constexpr (LPR == 32 && VPT >= 1 && VPT <= 5) {
+        const size_t smem = kLnTmaBarBytes + ln_tma_gamma_bytes(static_cast<int>(cols), sizeof(T)) +
+                            static_cast<size_t>(kLnTmaWarps) * kLnTmaStages * 2 *
+                                static_cast<size_t>(cols) * sizeof(T);
+        if (smem <= 110 * 1024) {
+            auto kern = ln_bwd_tma_kernel<T, VPT>;
+            cudaError_t e = set_smem(kern, smem);
+            if (e != cudaSuccess) return e;
+            return launch_pdl(kern, dim3(static_cast<unsigned>(p.grid)), dim3(kLnTmaWarps * 32),
+                              smem, s, static_cast<T*>(dx), partial, static_cast<const T*>(dy),
+                              static_cast<const T*>(x), static_cast<const T*>(gamma), mean, rstd,
+                              rows, static_cast<int>(cols), p.steps);
+        }
+    }
     const size_t smem = partial ? static_cast<size_t>(kThreads / LPR) * 2 * cols * sizeof(float)
                                 : 0;
     auto kern = ln_bwd_group_kernel<T, LPR, VPT>;
@@ -590,6 +750,10 @@ cudaError_t bwd_dispatch(void* dx, float* partial, const void* dy, const void* x
 ColReducePlan layernorm_bwd_plan(int64_t rows, int64_t cols) {
     const LnPlan p = plan_for(rows, cols, true);
     return ColReducePlan{p.grid, 2 * cols};
+}
+
+cudaError_t layernorm_take_device_error(unsigned int* flags) {
+    return take_device_error_word(flags);
 }
 
 cudaError_t launch_layernorm_fwd(DType dt, void* y, float* mean, float* rstd, const void* x,

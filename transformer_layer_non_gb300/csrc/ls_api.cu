@@ -174,6 +174,20 @@ const char* ls_last_error(void) { return g_last_error; }
 
 int ls_version(void) { return 10000; }
 
+ls_status ls_check_device_errors(uint32_t* flags) {
+    if (!flags) return fail(LS_ERR_INVALID_ARGUMENT, "flags is NULL");
+    *flags = 0;
+    cudaError_t e = cudaDeviceSynchronize();
+    if (e != cudaSuccess) return from_cuda(e, "ls_check_device_errors: synchronise");
+    unsigned int a = 0, b = 0, c = 0;
+    e = ls::softmax_take_device_error(&a);
+    if (e == cudaSuccess) e = ls::layernorm_take_device_error(&b);
+    if (e == cudaSuccess) e = ls::dropout_take_device_error(&c);
+    if (e != cudaSuccess) return from_cuda(e, "ls_check_device_errors: read flags");
+    *flags = a | b | c;
+    return ok();
+}
+
 size_t ls_colreduce_workspace_bytes(int64_t rows, int64_t cols) {
     if (rows <= 0 || cols <= 0 || cols % 8 != 0) return 0;
     const size_t a = ls::dropout_bwd_plan(rows, cols).bytes();
@@ -389,7 +403,7 @@ static ls_status softmax_common(const char* fn, ls_dtype dtype, int64_t batch, i
     if (q_len > (int64_t{1} << 30) || batch > (int64_t{1} << 30) || heads > (int64_t{1} << 30))
         return fail(LS_ERR_UNSUPPORTED_SHAPE, "%s: dimension too large", fn);
     const double n = static_cast<double>(batch) * heads * q_len;
-    if (n * k_len > static_cast<double>(int64_t{1} << 46) || n > static_cast<double>(1u << 31) * 256)
+    if (n * k_len > static_cast<double>(int64_t{1} << 46) || n >= static_cast<double>(1u << 31))
         return fail(LS_ERR_UNSUPPORTED_SHAPE, "%s: too many elements", fn);
     *nrows = batch * heads * q_len;
     if (key_len && (reinterpret_cast<uintptr_t>(key_len) & 3u))

@@ -12,6 +12,12 @@ namespace ls {
 
 constexpr int kVec = 8;  // elements per vector access, both dtypes
 
+// Minimum resident CTAs per SM asked of the compiler: the FP16 figure, one
+// fewer for FP32 storage (whose vectors take twice the registers).
+template <typename T> __host__ __device__ constexpr int min_ctas(int for_fp16) {
+    return sizeof(T) == 2 ? for_fp16 : (for_fp16 > 1 ? for_fp16 - 1 : 1);
+}
+
 // ---------------------------------------------------------------------------
 // 8-element vectors.  Raw8<T> keeps the loaded bits (4 registers for FP16,
 // 8 for FP32) so that many loads can be in flight before any conversion.
@@ -20,23 +26,10 @@ template <typename T> struct Raw8;
 template <> struct Raw8<__half> { uint4 v; };
 template <> struct Raw8<float> { float4 a, b; };
 
-__device__ __forceinline__ uint4 ld16(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
-// Streaming load for data read exactly once (evict-first in L1/L2).
-__device__ __forceinline__ uint4 ld16_stream(const void* p) {
-    uint4 r;
-    asm volatile("ld.global.cs.v4.u32 {%0,%1,%2,%3}, [%4];"
-                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w) : "l"(p));
-    return r;
-}
-__device__ __forceinline__ void st16(void* p, uint4 v) {
-    asm volatile("st.global.v4.u32 [%0], {%1,%2,%3,%4};"
-                 :: "l"(p), "r"(v.x), "r"(v.y), "r"(v.z), "r"(v.w) : "memory");
-}
+// Plain C++ accesses: the compiler schedules them freely but never moves them
+// across the barrier/wait instructions, whose asm carries a memory clobber.
+__device__ __forceinline__ uint4 ld16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+__device__ __forceinline__ void st16(void* p, uint4 v) { *reinterpret_cast<uint4*>(p) = v; }
 
 __device__ __forceinline__ uint4 f2u4(float4 f) {
     return make_uint4(__float_as_uint(f.x), __float_as_uint(f.y), __float_as_uint(f.z),
@@ -91,6 +84,14 @@ template <> __device__ __forceinline__ Raw8<__half> pack<__half>(const float (&f
 }
 template <> __device__ __forceinline__ Raw8<float> pack<float>(const float (&f)[8]) {
     return Raw8<float>{make_float4(f[0], f[1], f[2], f[3]), make_float4(f[4], f[5], f[6], f[7])};
+}
+
+template <typename T> __device__ __forceinline__ Raw8<T> zero8();
+template <> __device__ __forceinline__ Raw8<__half> zero8<__half>() {
+    return Raw8<__half>{make_uint4(0, 0, 0, 0)};
+}
+template <> __device__ __forceinline__ Raw8<float> zero8<float>() {
+    return Raw8<float>{make_float4(0.f, 0.f, 0.f, 0.f), make_float4(0.f, 0.f, 0.f, 0.f)};
 }
 
 template <typename T> __device__ __forceinline__ void load8f(const T* p, float (&f)[8]) {
@@ -161,6 +162,14 @@ __device__ __forceinline__ uint32_t keep_bits8(uint64_t i, uint32_t thr, const P
            (b.z >= thr ? 64u : 0u) | (b.w >= thr ? 128u : 0u);
 }
 
+// e^x as 2^(x * log2 e), with 2^y from the PTX ex2.approx instruction (relative
+// error about 2^-22; results below 2^-126 flush to zero).
+__device__ __forceinline__ float exp2_approx(float y) {
+    float r;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(y));
+    return r;
+}
+
 // ---------------------------------------------------------------------------
 // Reductions over groups of W consecutive lanes (W a power of two <= 32).
 // ---------------------------------------------------------------------------
@@ -222,3 +231,156 @@ inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, s
 }
 
 }  // namespace ls
+
+namespace ls {
+
+// ---------------------------------------------------------------------------
+// Bulk copies (TMA, non-tensor form) into shared memory, completed on an
+// mbarrier.  Both addresses must be 16-byte aligned and the size a multiple
+// of 16 bytes; every caller copies whole 16-byte vectors of 16-byte-aligned
+// rows.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_init_fence() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+// One arrival that also expects `bytes` of transactions (0 completes the phase).
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return done != 0;
+}
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::
+            "r"(smem_u32(dst)),
+        "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Orders this thread's earlier generic-proxy accesses to shared memory before
+// later async-proxy (bulk copy) accesses to it.
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint4 lds16(const void* p) { return *reinterpret_cast<const uint4*>(p); }
+template <typename T> __device__ __forceinline__ Raw8<T> load8_smem(const T* p);
+template <> __device__ __forceinline__ Raw8<__half> load8_smem<__half>(const __half* p) {
+    return Raw8<__half>{lds16(p)};
+}
+template <> __device__ __forceinline__ Raw8<float> load8_smem<float>(const float* p) {
+    return Raw8<float>{u2f4(lds16(p)), u2f4(lds16(p + 4))};
+}
+
+// Device-side failure flags of the kernels in one translation unit (each
+// unit that includes this header has its own word; ls_check_device_errors
+// collects them).  Bit 0: a bulk-copy wait ran out of time.
+constexpr unsigned int kDevErrWaitTimeout = 1u;
+namespace {
+__device__ unsigned int g_device_error = 0;
+}
+__device__ __forceinline__ void flag_device_error(unsigned int bits) {
+    atomicOr(&g_device_error, bits);
+}
+// Host: read and clear this unit's flags (synchronous copy).
+static inline cudaError_t take_device_error_word(unsigned int* out) {
+    unsigned int v = 0;
+    cudaError_t e = cudaMemcpyFromSymbol(&v, g_device_error, sizeof(v));
+    if (e == cudaSuccess && v != 0) {
+        const unsigned int zero = 0;
+        e = cudaMemcpyToSymbol(g_device_error, &zero, sizeof(zero));
+    }
+    *out = v;
+    return e;
+}
+
+// Polls of an mbarrier before a wait is declared failed.  Each poll may
+// suspend the thread for a hardware-defined interval, so this bounds a wait to
+// well under a second on a healthy GPU while never firing on a slow copy.
+constexpr uint32_t kWaitPolls = 1u << 22;
+
+// An S-stage ring of shared-memory buffers owned by one warp.  Lane 0 arms a
+// stage and issues its bulk copies; all lanes wait on the stage's barrier; the
+// k-th use of stage k % S completes phase (k / S) & 1.
+template <int S>
+struct WarpRing {
+    uint64_t* bar;
+    unsigned char* buf;
+    uint32_t stage_bytes;
+    uint32_t pending;  // bit s: a copy into stage s was issued and not yet waited for
+
+    __device__ __forceinline__ void init(uint64_t* bars, unsigned char* data, uint32_t sb) {
+        bar = bars;
+        buf = data;
+        stage_bytes = sb;
+        pending = 0;
+        if ((threadIdx.x & 31) == 0) {
+#pragma unroll
+            for (int s = 0; s < S; ++s) mbar_init(bar + s, 1);
+            mbar_init_fence();
+        }
+        __syncwarp();
+    }
+    __device__ __forceinline__ unsigned char* stage(int s) const { return buf + s * stage_bytes; }
+
+    // Arm stage s for n0 + n1 bytes: n0 from src0 to the stage start, n1 from
+    // src1 to the stage at byte offset off1.  n0 = n1 = 0 completes the phase
+    // at once (the row has nothing to read).  Called by every lane.
+    // The caller's earlier reads of stage s must have completed (their values
+    // used) and the warp synchronised before it re-arms the stage.
+    __device__ __forceinline__ void issue(int s, const void* src0, uint32_t n0, const void* src1,
+                                          uint32_t n1, uint32_t off1) {
+        if ((threadIdx.x & 31) == 0) {
+            mbar_arrive_expect_tx(bar + s, n0 + n1);
+            if (n0) bulk_g2s(stage(s), src0, n0, bar + s);
+            if (n1) bulk_g2s(stage(s) + off1, src1, n1, bar + s);
+        }
+        pending |= 1u << s;
+    }
+
+    // Bounded wait for stage s; false (and the failure flagged) on timeout.
+    __device__ __forceinline__ bool wait(int s, uint32_t parity) {
+        for (uint32_t i = 0; i < kWaitPolls; ++i) {
+            if (mbar_try_wait(bar + s, parity)) {
+                pending &= ~(1u << s);
+                return true;
+            }
+        }
+        flag_device_error(kDevErrWaitTimeout);
+        return false;
+    }
+
+    // After a failed wait: wait (bounded again) for every copy still in flight
+    // into this warp's stages, so none lands after the CTA has exited.
+    __device__ __forceinline__ void drain(const uint32_t (&parity_of)[S]) {
+#pragma unroll
+        for (int s = 0; s < S; ++s) {
+            if (pending & (1u << s)) {
+                for (uint32_t i = 0; i < kWaitPolls; ++i)
+                    if (mbar_try_wait(bar + s, parity_of[s])) break;
+            }
+        }
+        pending = 0;
+    }
+};
+
+}  // namespace ls
+

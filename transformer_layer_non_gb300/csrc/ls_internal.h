@@ -62,6 +62,12 @@ cudaError_t launch_softmax_bwd(DType dt, void* dx, const void* y, const void* dy
 
 constexpr int64_t kMaxRowLen = 16384;
 
+// Read and clear the device-side failure flags of one translation unit's
+// kernels (synchronous).
+cudaError_t softmax_take_device_error(unsigned int* flags);
+cudaError_t dropout_take_device_error(unsigned int* flags);
+cudaError_t layernorm_take_device_error(unsigned int* flags);
+
 // Streaming multiprocessors of the current device (queried once per device).
 int sm_count();
 

@@ -37,15 +37,17 @@ struct RowMask {
 };
 
 // Number of leading valid keys of a row (0..k_len).
+// Rows number fewer than 2^31 (checked on the host), so 32-bit division.
 __device__ __forceinline__ int valid_len(int64_t row, int k_len, const RowMask& m) {
     int v = k_len;
+    const uint32_t r32 = static_cast<uint32_t>(row);
     if (m.key_len) {
-        const int64_t b = row / m.heads_q;
+        const uint32_t b = r32 / static_cast<uint32_t>(m.heads_q);
         const int kl = m.key_len[b];
         v = min(v, max(kl, 0));
     }
     if (m.causal) {
-        const int q = static_cast<int>(row % m.q_len);
+        const int q = static_cast<int>(r32 % static_cast<uint32_t>(m.q_len));
         v = min(v, max(q + m.shift + 1, 0));
     }
     return v;
@@ -174,7 +176,7 @@ __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx
 
 // BWD = false: out = y, p = x.   BWD = true: out = dx, p = y, q = dy.
 template <typename T, int LPR, int VPT, bool BWD>
-__global__ void __launch_bounds__(kThreads, (sizeof(T) == 2 && (VPT == 1 || (BWD && VPT == 2))) ? 4 : 3)
+__global__ void __launch_bounds__(kThreads, min_ctas<T>((VPT == 1 || (BWD && VPT == 2)) ? 4 : 3))
 softmax_group_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, RowMask mk) {
     constexpr int RPC = kThreads / LPR;
     pdl_enter();
@@ -209,6 +211,178 @@ softmax_group_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, R
             sm_bwd_row<T, LPR, VPT>(bb, out, r1, nrows, k_len, gl);
         else
             sm_fwd_row<T, LPR, VPT>(bb, out, r1, nrows, k_len, gl);
+    }
+}
+
+// ----------------------------------------------------------------------------
+// Warp-per-row kernels fed by bulk copies (k_len 256..1024).  Each warp owns an
+// S-stage ring of row buffers in shared memory; lane 0 copies the valid prefix
+// of the warp's next rows (x, or y and dy) with cp.async.bulk while the warp
+// computes the current row from shared memory, so S rows per warp are in
+// flight independently of registers.  Measured on GB300: two stages of four
+// warps per CTA serve the forward best (more stages cost warps per SM, and the
+// per-row work then limits); the backward, which reads twice the bytes per
+// row, is faster from registers (softmax_group_kernel), so only the forward
+// dispatches here.  Rows are interleaved over warps of all
+// CTAs (row = warp_slot + k * all_warps).  A wait that runs out of time flags
+// the failure, lets the warp's copies land and ends the warp.
+// ----------------------------------------------------------------------------
+constexpr int kTmaWarps = 4;
+constexpr int kTmaStages = 2;
+
+__host__ __device__ constexpr uint32_t tma_bar_bytes() {
+    return ((kTmaWarps * kTmaStages * 8 + 127) / 128) * 128;
+}
+
+template <typename T, int VPT, bool BWD>
+__global__ void __launch_bounds__(kTmaWarps * 32)
+softmax_tma_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, RowMask mk) {
+    extern __shared__ __align__(128) unsigned char smem[];
+    constexpr int S = kTmaStages;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const uint32_t row_bytes = static_cast<uint32_t>(k_len) * sizeof(T);
+    const uint32_t stage_bytes = BWD ? 2 * row_bytes : row_bytes;
+    WarpRing<S> ring;
+    ring.init(reinterpret_cast<uint64_t*>(smem) + warp * S,
+              smem + tma_bar_bytes() + static_cast<size_t>(warp) * S * stage_bytes, stage_bytes);
+    pdl_enter();
+    const int nvec = k_len / kVec;
+    const int64_t W = static_cast<int64_t>(gridDim.x) * kTmaWarps;
+    const int64_t first = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(warp) * gridDim.x;
+    uint32_t parity[S];
+    int vlen_of[S];
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        parity[s] = 0;
+        vlen_of[s] = 0;
+        const int64_t r = first + s * W;
+        if (r < nrows) {
+            const int vl = valid_len(r, k_len, mk);
+            vlen_of[s] = vl;
+            const uint32_t n = static_cast<uint32_t>((vl + kVec - 1) / kVec) * kVec * sizeof(T);
+            ring.issue(s, p + r * k_len, n, BWD ? q + r * k_len : nullptr, BWD ? n : 0, row_bytes);
+        }
+    }
+    for (int64_t k = 0;; ++k) {
+        const int64_t r = first + k * W;
+        if (r >= nrows) break;
+        const int s = static_cast<int>(k % S);
+        const bool ok = ring.wait(s, parity[s]);
+        if (!__all_sync(0xffffffffu, ok)) {  // the warp leaves together
+            ring.drain(parity);
+            return;
+        }
+        parity[s] ^= 1u;
+        const int vlen = vlen_of[s];
+        const int nfull = vlen / kVec;   // vectors whose 8 keys are all valid
+        const int tail = vlen % kVec;    // valid keys of vector nfull (0: none)
+        const T* xs = reinterpret_cast<const T*>(ring.stage(s));
+        const T* ds = reinterpret_cast<const T*>(ring.stage(s) + row_bytes);
+        const int64_t base = r * k_len;
+        float f[VPT][kVec];
+        if (BWD) {
+            float dot = 0.f;
+#pragma unroll
+            for (int k2 = 0; k2 < VPT; ++k2) {
+                const int v = lane + k2 * 32;
+                if (v < nfull || (v == nfull && tail)) {
+                    float df[kVec];
+                    unpack(load8_smem<T>(xs + v * kVec), f[k2]);
+                    unpack(load8_smem<T>(ds + v * kVec), df);
+                    if (v < nfull) {
+#pragma unroll
+                        for (int j = 0; j < kVec; ++j) dot = fmaf(f[k2][j], df[j], dot);
+                    } else {
+#pragma unroll
+                        for (int j = 0; j < kVec; ++j)
+                            if (j < tail) dot = fmaf(f[k2][j], df[j], dot);
+                    }
+                }
+            }
+            dot = group_sum<32>(dot);
+#pragma unroll
+            for (int k2 = 0; k2 < VPT; ++k2) {
+                const int v = lane + k2 * 32;
+                if (v >= nvec) continue;
+                T* dst = out + base + v * kVec;
+                if (v < nfull || (v == nfull && tail)) {
+                    float df[kVec], o[kVec];
+                    unpack(load8_smem<T>(ds + v * kVec), df);
+#pragma unroll
+                    for (int j = 0; j < kVec; ++j) o[j] = f[k2][j] * (df[j] - dot);
+                    if (v == nfull) {
+#pragma unroll
+                        for (int j = 0; j < kVec; ++j)
+                            if (j >= tail) o[j] = 0.f;
+                    }
+                    store8f<T>(dst, o);
+                } else {
+                    store8<T>(dst, zero8<T>());
+                }
+            }
+        } else {
+            float m = -INFINITY;
+#pragma unroll
+            for (int k2 = 0; k2 < VPT; ++k2) {
+                const int v = lane + k2 * 32;
+                if (v < nfull) {
+                    unpack(load8_smem<T>(xs + v * kVec), f[k2]);
+#pragma unroll
+                    for (int j = 0; j < kVec; ++j) m = fmaxf(m, f[k2][j]);
+                } else if (v == nfull && tail) {
+                    unpack(load8_smem<T>(xs + v * kVec), f[k2]);
+#pragma unroll
+                    for (int j = 0; j < kVec; ++j)
+                        if (j < tail) m = fmaxf(m, f[k2][j]);
+                }
+            }
+            m = group_max<32>(m);
+            const float ml = m * kLog2e;
+            float sum = 0.f;
+#pragma unroll
+            for (int k2 = 0; k2 < VPT; ++k2) {
+                const int v = lane + k2 * 32;
+                if (v < nfull) {
+#pragma unroll
+                    for (int j = 0; j < kVec; ++j) {
+                        f[k2][j] = exp2_approx(fmaf(f[k2][j], kLog2e, -ml));
+                        sum += f[k2][j];
+                    }
+                } else if (v == nfull && tail) {
+#pragma unroll
+                    for (int j = 0; j < kVec; ++j) {
+                        f[k2][j] = j < tail ? exp2_approx(fmaf(f[k2][j], kLog2e, -ml)) : 0.f;
+                        sum += f[k2][j];
+                    }
+                }
+            }
+            sum = group_sum<32>(sum);
+            const float inv = sum > 0.f ? 1.f / sum : 0.f;
+#pragma unroll
+            for (int k2 = 0; k2 < VPT; ++k2) {
+                const int v = lane + k2 * 32;
+                if (v >= nvec) continue;
+                T* dst = out + base + v * kVec;
+                if (v < nfull || (v == nfull && tail)) {
+                    float o[kVec];
+#pragma unroll
+                    for (int j = 0; j < kVec; ++j) o[j] = f[k2][j] * inv;
+                    store8f<T>(dst, o);
+                } else {
+                    store8<T>(dst, zero8<T>());
+                }
+            }
+        }
+        __syncwarp();  // every lane has used its reads of stage s
+        const int64_t rn = r + S * W;
+        if (rn < nrows) {
+            const int vl = valid_len(rn, k_len, mk);
+            vlen_of[s] = vl;
+            const uint32_t n = static_cast<uint32_t>((vl + kVec - 1) / kVec) * kVec * sizeof(T);
+            ring.issue(s, p + rn * k_len, n, BWD ? q + rn * k_len : nullptr, BWD ? n : 0,
+                       row_bytes);
+        }
     }
 }
 
@@ -403,9 +577,31 @@ cudaError_t group_launch(T* out, const T* p, const T* q, int64_t nrows, int k_le
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, out, p, q,
                       nrows, k_len, m);
 }
+template <typename T, int VPT, bool BWD>
+cudaError_t tma_launch(T* out, const T* p, const T* q, int64_t nrows, int k_len,
+                       const RowMask& m, cudaStream_t s) {
+    auto kern = softmax_tma_kernel<T, VPT, BWD>;
+    const size_t stage = static_cast<size_t>(k_len) * sizeof(T) * (BWD ? 2 : 1);
+    const size_t smem = tma_bar_bytes() + static_cast<size_t>(kTmaWarps) * kTmaStages * stage;
+    if (smem > 48 * 1024) {
+        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+    }
+    const int occ = occupancy(kern, kTmaWarps * 32, smem);
+    const int64_t need = (nrows + kTmaWarps - 1) / kTmaWarps;
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(need, int64_t{sm_count()} * occ));
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kTmaWarps * 32), smem, s, out,
+                      p, q, nrows, k_len, m);
+}
+
 template <typename T, int LPR, int VPT>
 cudaError_t fwd_group(void* y, const void* x, int64_t nrows, int k_len, const RowMask& m,
                       const SmPlan& p, cudaStream_t s) {
+    if constexpr (LPR == 32)
+        return tma_launch<T, VPT, false>(static_cast<T*>(y), static_cast<const T*>(x),
+                                         static_cast<const T*>(nullptr), nrows, k_len, m, s);
+    else
     return group_launch<T, LPR, VPT, false>(static_cast<T*>(y), static_cast<const T*>(x),
                                             static_cast<const T*>(nullptr), nrows, k_len, m, p, s);
 }
@@ -494,6 +690,10 @@ cudaError_t bwd_dispatch(void* dx, const void* y, const void* dy, const SoftmaxS
 }
 
 }  // namespace
+
+cudaError_t softmax_take_device_error(unsigned int* flags) {
+    return take_device_error_word(flags);
+}
 
 cudaError_t launch_softmax_fwd(DType dt, void* y, const void* x, const SoftmaxShape& sh,
                                cudaStream_t s) {

@@ -34,7 +34,7 @@ EXPORTS = (
     "ls_bias_dropout_residual_fwd", "ls_bias_dropout_residual_bwd",
     "ls_bias_relu_dropout_fwd", "ls_bias_relu_dropout_bwd",
     "ls_layernorm_fwd", "ls_layernorm_bwd", "ls_softmax_fwd", "ls_softmax_bwd",
-    "ls_layernorm_bwd_noalloc",
+    "ls_layernorm_bwd_noalloc", "ls_check_device_errors",
 )
 
 
@@ -57,6 +57,7 @@ _SIGNATURES = {
     "ls_last_error": (ctypes.c_char_p, []),
     "ls_version": (_INT, []),
     "ls_colreduce_workspace_bytes": (_SZ, [_I64, _I64]),
+    "ls_check_device_errors": (_INT, [ctypes.POINTER(ctypes.c_uint32)]),
     "ls_bias_dropout_residual_fwd": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _F32, _U64, _U64, _P]),
     "ls_bias_dropout_residual_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _F32, _U64, _U64, _P, _SZ, _P]),
     "ls_bias_relu_dropout_fwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _F32, _U64, _U64, _P]),
@@ -105,6 +106,26 @@ def version() -> int:
 
 def colreduce_workspace_bytes(rows: int, cols: int) -> int:
     return int(load().ls_colreduce_workspace_bytes(rows, cols))
+
+
+def new_workspace(shapes, device="cuda"):
+    """A workspace large enough for the backward calls with a column
+    reduction on every [rows, cols] in `shapes`."""
+    import torch
+
+    n = max([colreduce_workspace_bytes(r, c) for r, c in shapes] + [256])
+    return torch.zeros(n, dtype=torch.uint8, device=device)
+
+
+LS_DEVERR_WAIT_TIMEOUT = 1
+
+
+def check_device_errors() -> int:
+    """Synchronise the current device and return (and clear) the library's
+    device-side failure flags (0 = none)."""
+    v = ctypes.c_uint32(0)
+    _check(load().ls_check_device_errors(ctypes.byref(v)))
+    return int(v.value)
 
 
 def _check(status: int):

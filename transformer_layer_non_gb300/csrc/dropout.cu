@@ -31,13 +31,15 @@ constexpr int kThreads = 256;
 // ---------------------------------------------------------------------------
 // Forward.
 // ---------------------------------------------------------------------------
+// Kernel arguments live in the constant bank, so the Philox round keys,
+// computed once on the host, are instruction operands rather than registers.
 struct FwdArgs {
     uint64_t nv;        // vectors in the tensor (rows * cols / 8)
     uint32_t nvr;       // vectors per row
     uint32_t step_col;  // (vectors per round) mod nvr
     uint32_t thr;
     float scale;
-    PhiloxKey key;
+    PhiloxSchedule ks;
     uint32_t off_lo, off_hi;
     int mask_tail_bytes;
 };
@@ -110,8 +112,8 @@ __device__ __forceinline__ void fwd_compute(const Raw8<T> (&xr)[U], const Raw8<T
 template <typename T, bool RELU, int U>
 __global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 4 : 2)
 dropout_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias,
-                   const T* residual, FwdArgs a) {
-    const PhiloxSchedule ks = philox_schedule(a.key);
+                   const T* residual, const __grid_constant__ FwdArgs a) {
+    const PhiloxSchedule& ks = a.ks;
     pdl_enter();
     const uint64_t S = static_cast<uint64_t>(gridDim.x) * kThreads;  // vectors per round
     const uint64_t gw = blockIdx.x + static_cast<uint64_t>(threadIdx.x >> 5) * gridDim.x;
@@ -164,7 +166,7 @@ struct BwdArgs {
     int64_t ntiles;
     uint32_t thr;
     float scale;
-    PhiloxKey key;
+    PhiloxSchedule ks;
     uint32_t off_lo, off_hi;
 };
 
@@ -250,9 +252,9 @@ __device__ __forceinline__ void bwd_compute(const Raw8<T> (&dr)[kBwdU],
 template <typename T, bool REGEN>
 __global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 3 : 2)
 dropout_bwd_kernel(T* dx, float* __restrict__ partial, const T* dout,
-                   const uint8_t* __restrict__ mask, BwdArgs a) {
+                   const uint8_t* __restrict__ mask, const __grid_constant__ BwdArgs a) {
     __shared__ __align__(16) float red[kBwdRps][kBwdColsPerTile];
-    const PhiloxSchedule ks = philox_schedule(a.key);
+    const PhiloxSchedule& ks = a.ks;
     pdl_enter();
     int64_t t = blockIdx.x;
     Raw8<T> da[kBwdU], db[kBwdU];
@@ -332,7 +334,7 @@ cudaError_t fwd_impl(void* out, uint8_t* mask, const void* x, const void* bias,
     a.step_col = static_cast<uint32_t>((static_cast<uint64_t>(grid) * kThreads) % a.nvr);
     a.thr = rng.thr;
     a.scale = rng.scale;
-    a.key = make_key(rng.seed);
+    a.ks = philox_schedule(make_key(rng.seed));
     a.off_lo = static_cast<uint32_t>(rng.offset);
     a.off_hi = static_cast<uint32_t>(rng.offset >> 32);
     a.mask_tail_bytes = static_cast<int>(((a.nv + 3) / 4) * 4 - a.nv);
@@ -351,7 +353,7 @@ cudaError_t bwd_impl(void* dx, float* partial, const void* dout, const uint8_t* 
     a.ntiles = ((rows + kBwdRowsPerTile - 1) / kBwdRowsPerTile) * a.nbands;
     a.thr = rng.thr;
     a.scale = rng.scale;
-    a.key = make_key(rng.seed);
+    a.ks = philox_schedule(make_key(rng.seed));
     a.off_lo = static_cast<uint32_t>(rng.offset);
     a.off_hi = static_cast<uint32_t>(rng.offset >> 32);
     auto kern = mask ? dropout_bwd_kernel<T, false> : dropout_bwd_kernel<T, true>;

@@ -358,16 +358,21 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
             rs_of[s] = rstd[r];
         }
     }
-    bool failed = false;
+    bool done = false;  // set when the warp's rows are done (or a wait failed)
     __syncthreads();  // gamma staged
-    for (int k = 0;; ++k) {
-        const int64_t r = base + warp + static_cast<int64_t>(k) * kLnTmaWarps;
-        if (r >= end) break;
-        const int s = k % S;
+    // Unrolled by the stage count so that the stage index is a constant.
+    for (int k0 = 0; !done; k0 += S) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        const int64_t r = base + warp + static_cast<int64_t>(k0 + s) * kLnTmaWarps;
+        if (r >= end) {
+            done = true;
+            break;
+        }
         const bool ok = ring.wait(s, parity[s]);
         if (!__all_sync(0xffffffffu, ok)) {
             ring.drain(parity);
-            failed = true;
+            done = true;
             break;
         }
         parity[s] ^= 1u;
@@ -419,6 +424,7 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
             rs_of[s] = rstd[rn];
         }
     }
+    }
     if (partial == nullptr) return;
     // Cross-warp sum of the parameter-gradient partials, in warp order, through
     // the stage memory (every copy has landed and been read).
@@ -438,7 +444,6 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
         }
     }
     __syncthreads();
-    (void)failed;
     for (int c = threadIdx.x; c < 2 * cols; c += kLnTmaWarps * 32) {
         float t = 0.f;
 #pragma unroll

@@ -19,6 +19,33 @@ template <typename T> __host__ __device__ constexpr int min_ctas(int for_fp16) {
 }
 
 // ---------------------------------------------------------------------------
+// Division of a 31-bit numerator by a fixed divisor d >= 1 as a multiply and
+// a shift (Granlund & Montgomery, "Division by invariant integers using
+// multiplication", PLDI 1994): with l = ceil(log2 d) and m = floor(2^(31+l)/d)
+// + 1 (at most 2^32), floor(n/d) = floor(n*m / 2^(31+l)) for 0 <= n < 2^31.
+// ---------------------------------------------------------------------------
+struct FastDiv {
+    uint64_t m;
+    uint32_t shift;  // 31 + l
+    uint32_t d;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t l = 0;
+    while ((uint64_t{1} << l) < d) ++l;
+    FastDiv f;
+    f.shift = 31 + l;
+    f.m = ((uint64_t{1} << f.shift) / d) + 1;
+    f.d = d;
+    return f;
+}
+__host__ __device__ __forceinline__ uint32_t fdiv(uint32_t n, const FastDiv& f) {
+    return static_cast<uint32_t>((static_cast<uint64_t>(n) * f.m) >> f.shift);
+}
+__host__ __device__ __forceinline__ uint32_t fmod_(uint32_t n, const FastDiv& f) {
+    return n - fdiv(n, f) * f.d;
+}
+
+// ---------------------------------------------------------------------------
 // 8-element vectors.  Raw8<T> keeps the loaded bits (4 registers for FP16,
 // 8 for FP32) so that many loads can be in flight before any conversion.
 // ---------------------------------------------------------------------------
@@ -86,6 +113,21 @@ template <> __device__ __forceinline__ Raw8<float> pack<float>(const float (&f)[
     return Raw8<float>{make_float4(f[0], f[1], f[2], f[3]), make_float4(f[4], f[5], f[6], f[7])};
 }
 
+// Maximum of the 8 elements of a vector (exact: max never rounds).  FP16 takes
+// the packed half2 maximum.
+__device__ __forceinline__ float vmax8(const Raw8<__half>& r) {
+    const __half2 a = __hmax2(*reinterpret_cast<const __half2*>(&r.v.x),
+                              *reinterpret_cast<const __half2*>(&r.v.y));
+    const __half2 b = __hmax2(*reinterpret_cast<const __half2*>(&r.v.z),
+                              *reinterpret_cast<const __half2*>(&r.v.w));
+    const __half2 c = __hmax2(a, b);
+    return fmaxf(__low2float(c), __high2float(c));
+}
+__device__ __forceinline__ float vmax8(const Raw8<float>& r) {
+    return fmaxf(fmaxf(fmaxf(r.a.x, r.a.y), fmaxf(r.a.z, r.a.w)),
+                 fmaxf(fmaxf(r.b.x, r.b.y), fmaxf(r.b.z, r.b.w)));
+}
+
 template <typename T> __device__ __forceinline__ Raw8<T> zero8();
 template <> __device__ __forceinline__ Raw8<__half> zero8<__half>() {
     return Raw8<__half>{make_uint4(0, 0, 0, 0)};
@@ -119,7 +161,7 @@ struct PhiloxSchedule {
     uint32_t k0[10], k1[10];
 };
 
-__device__ __forceinline__ PhiloxSchedule philox_schedule(PhiloxKey key) {
+__host__ __device__ __forceinline__ PhiloxSchedule philox_schedule(PhiloxKey key) {
     constexpr uint32_t W0 = 0x9E3779B9u, W1 = 0xBB67AE85u;
     PhiloxSchedule s;
 #pragma unroll
@@ -256,14 +298,17 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
                  "r"(bytes)
                  : "memory");
 }
+// Waits for the phase with the given parity to complete; the thread sleeps
+// (up to kWaitHintNs) instead of spinning.  Returns whether it completed.
+constexpr uint32_t kWaitHintNs = 2000;
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t done;
     asm volatile(
         "{\n\t.reg .pred p;\n\t"
-        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n\t"
         "selp.u32 %0, 1, 0, p;\n\t}"
         : "=r"(done)
-        : "r"(smem_u32(bar)), "r"(parity)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(kWaitHintNs)
         : "memory");
     return done != 0;
 }
@@ -312,10 +357,10 @@ static inline cudaError_t take_device_error_word(unsigned int* out) {
     return e;
 }
 
-// Polls of an mbarrier before a wait is declared failed.  Each poll may
-// suspend the thread for a hardware-defined interval, so this bounds a wait to
-// well under a second on a healthy GPU while never firing on a slow copy.
-constexpr uint32_t kWaitPolls = 1u << 22;
+// Polls of an mbarrier before a wait is declared failed.  Each poll sleeps up
+// to kWaitHintNs, so a wait is bounded to about a second, and even polls that
+// return at once span milliseconds -- far beyond any bulk copy's latency.
+constexpr uint32_t kWaitPolls = 1u << 19;
 
 // An S-stage ring of shared-memory buffers owned by one warp.  Lane 0 arms a
 // stage and issues its bulk copies; all lanes wait on the stage's barrier; the

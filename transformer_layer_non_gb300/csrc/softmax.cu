@@ -30,24 +30,24 @@ constexpr float kLog2e = 1.4426950408889634f;
 
 struct RowMask {
     const int32_t* key_len;  // [batch] or nullptr
-    int64_t heads_q;         // heads * q_len
-    int q_len;
+    FastDiv heads_q;         // row / (heads * q_len) = batch index
+    FastDiv q_len;           // row % q_len = query index
     int shift;               // k_len - q_len (causal diagonal offset)
     int causal;
 };
 
 // Number of leading valid keys of a row (0..k_len).
-// Rows number fewer than 2^31 (checked on the host), so 32-bit division.
+// Rows number fewer than 2^31 (checked on the host), so the batch and query
+// indices come from multiply-shift division.
 __device__ __forceinline__ int valid_len(int64_t row, int k_len, const RowMask& m) {
     int v = k_len;
     const uint32_t r32 = static_cast<uint32_t>(row);
     if (m.key_len) {
-        const uint32_t b = r32 / static_cast<uint32_t>(m.heads_q);
-        const int kl = m.key_len[b];
+        const int kl = m.key_len[fdiv(r32, m.heads_q)];
         v = min(v, max(kl, 0));
     }
     if (m.causal) {
-        const int q = static_cast<int>(r32 % static_cast<uint32_t>(m.q_len));
+        const int q = static_cast<int>(fmod_(r32, m.q_len));
         v = min(v, max(q + m.shift + 1, 0));
     }
     return v;
@@ -85,6 +85,11 @@ __device__ __forceinline__ void sm_load(RowBuf<T, LPR, VPT>& buf, const T* p, co
     }
 }
 
+// The forward row is branch-free across the valid/masked boundary: element j
+// of vector v is valid iff j < cnt(v) = clamp(vlen - 8v, 0, 8); invalid
+// elements are replaced by selects (vectors that were not loaded hold
+// arbitrary bits, which a select discards).  Divergent branches at the
+// boundary would run the full, partial and empty paths one after another.
 template <typename T, int LPR, int VPT>
 __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y, int64_t row,
                                            int64_t nrows, int k_len, int gl) {
@@ -95,30 +100,27 @@ __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y,
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = gl + k * LPR;
-        if (v * kVec < vlen) {
-            unpack(buf.a[k], f[k]);
+        const int cnt = min(max(vlen - v * kVec, 0), kVec);
+        unpack(buf.a[k], f[k]);
 #pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                if (v * kVec + j < vlen) m = fmaxf(m, f[k][j]);
+        for (int j = 0; j < kVec; ++j) {
+            f[k][j] = j < cnt ? f[k][j] : -INFINITY;
+            m = fmaxf(m, f[k][j]);
         }
     }
     m = group_max<LPR>(m);
-    const float ml = m * kLog2e;
+    const float ml = m == -INFINITY ? 0.f : m * kLog2e;  // empty row: every e is 0
     float s = 0.f;
 #pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        const int v = gl + k * LPR;
+    for (int k = 0; k < VPT; ++k)
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
-            const bool on = v * kVec + j < vlen;
-            const float e = on ? exp2f(fmaf(f[k][j], kLog2e, -ml)) : 0.f;
-            f[k][j] = e;
-            s += e;
+            f[k][j] = exp2_approx(fmaf(f[k][j], kLog2e, -ml));  // -inf -> 0
+            s += f[k][j];
         }
-    }
     s = group_sum<LPR>(s);
     if (row >= nrows) return;
-    const float inv = s > 0.f ? 1.f / s : 0.f;
+    const float inv = s > 0.f ? __fdividef(1.f, s) : 0.f;
     const int64_t base = row * k_len;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -126,12 +128,14 @@ __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y,
         if (v < nvec) {
             float o[kVec];
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) o[j] = f[k][j] * inv;  // masked: 0 * inv = 0
+            for (int j = 0; j < kVec; ++j) o[j] = f[k][j] * inv;  // masked: 0 * inv = +0
             store8f<T>(y + base + v * kVec, o);
         }
     }
 }
 
+// The backward keeps per-lane branches: it moves twice the bytes per row and
+// measured faster this way than branch-free (which needs more registers).
 template <typename T, int LPR, int VPT>
 __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx, int64_t row,
                                            int64_t nrows, int k_len, int gl) {
@@ -264,10 +268,12 @@ softmax_tma_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, Row
             ring.issue(s, p + r * k_len, n, BWD ? q + r * k_len : nullptr, BWD ? n : 0, row_bytes);
         }
     }
-    for (int64_t k = 0;; ++k) {
-        const int64_t r = first + k * W;
-        if (r >= nrows) break;
-        const int s = static_cast<int>(k % S);
+    // Unrolled by the stage count so that the stage index is a constant.
+    for (int64_t k0 = 0;; k0 += S) {
+#pragma unroll
+    for (int s = 0; s < S; ++s) {
+        const int64_t r = first + (k0 + s) * W;
+        if (r >= nrows) return;
         const bool ok = ring.wait(s, parity[s]);
         if (!__all_sync(0xffffffffu, ok)) {  // the warp leaves together
             ring.drain(parity);
@@ -275,103 +281,62 @@ softmax_tma_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, Row
         }
         parity[s] ^= 1u;
         const int vlen = vlen_of[s];
-        const int nfull = vlen / kVec;   // vectors whose 8 keys are all valid
-        const int tail = vlen % kVec;    // valid keys of vector nfull (0: none)
         const T* xs = reinterpret_cast<const T*>(ring.stage(s));
-        const T* ds = reinterpret_cast<const T*>(ring.stage(s) + row_bytes);
         const int64_t base = r * k_len;
+        // No divergent branch over the valid/masked boundary: element j of
+        // vector v is valid iff j < cnt(v) = clamp(vlen - 8v, 0, 8).  A slot
+        // of 32 vectors (one per lane) is wholly valid, straddles vlen, or lies
+        // past it -- the same case in every lane.  Wholly valid slots take the
+        // packed maximum; in the straddling slot invalid elements become -inf
+        // before the maximum, so their exponentials are exactly 0 with no
+        // further test; slots past vlen are stored as zeros.
         float f[VPT][kVec];
-        if (BWD) {
-            float dot = 0.f;
+        float m = -INFINITY;
 #pragma unroll
-            for (int k2 = 0; k2 < VPT; ++k2) {
-                const int v = lane + k2 * 32;
-                if (v < nfull || (v == nfull && tail)) {
-                    float df[kVec];
-                    unpack(load8_smem<T>(xs + v * kVec), f[k2]);
-                    unpack(load8_smem<T>(ds + v * kVec), df);
-                    if (v < nfull) {
+        for (int k2 = 0; k2 < VPT; ++k2) {
+            const int v = lane + k2 * 32;
+            if (vlen >= (k2 + 1) * 32 * kVec) {
+                // every vector of the slot is valid (same test in every lane)
+                const Raw8<T> raw = load8_smem<T>(xs + v * kVec);
+                m = fmaxf(m, vmax8(raw));
+                unpack(raw, f[k2]);
+            } else if (vlen > k2 * 32 * kVec) {
+                const int cnt = min(max(vlen - v * kVec, 0), kVec);
+                unpack(load8_smem<T>(xs + v * kVec), f[k2]);
 #pragma unroll
-                        for (int j = 0; j < kVec; ++j) dot = fmaf(f[k2][j], df[j], dot);
-                    } else {
-#pragma unroll
-                        for (int j = 0; j < kVec; ++j)
-                            if (j < tail) dot = fmaf(f[k2][j], df[j], dot);
-                    }
+                for (int j = 0; j < kVec; ++j) {
+                    f[k2][j] = j < cnt ? f[k2][j] : -INFINITY;
+                    m = fmaxf(m, f[k2][j]);
                 }
             }
-            dot = group_sum<32>(dot);
+        }
+        m = group_max<32>(m);
+        const float ml = m == -INFINITY ? 0.f : m * kLog2e;  // empty row: all e = 0
+        float sum = 0.f;
 #pragma unroll
-            for (int k2 = 0; k2 < VPT; ++k2) {
-                const int v = lane + k2 * 32;
-                if (v >= nvec) continue;
-                T* dst = out + base + v * kVec;
-                if (v < nfull || (v == nfull && tail)) {
-                    float df[kVec], o[kVec];
-                    unpack(load8_smem<T>(ds + v * kVec), df);
+        for (int k2 = 0; k2 < VPT; ++k2) {
+            if (vlen > k2 * 32 * kVec) {
 #pragma unroll
-                    for (int j = 0; j < kVec; ++j) o[j] = f[k2][j] * (df[j] - dot);
-                    if (v == nfull) {
-#pragma unroll
-                        for (int j = 0; j < kVec; ++j)
-                            if (j >= tail) o[j] = 0.f;
-                    }
-                    store8f<T>(dst, o);
-                } else {
-                    store8<T>(dst, zero8<T>());
+                for (int j = 0; j < kVec; ++j) {
+                    f[k2][j] = exp2_approx(fmaf(f[k2][j], kLog2e, -ml));
+                    sum += f[k2][j];
                 }
             }
-        } else {
-            float m = -INFINITY;
+        }
+        sum = group_sum<32>(sum);
+        const float inv = sum > 0.f ? __fdividef(1.f, sum) : 0.f;
 #pragma unroll
-            for (int k2 = 0; k2 < VPT; ++k2) {
-                const int v = lane + k2 * 32;
-                if (v < nfull) {
-                    unpack(load8_smem<T>(xs + v * kVec), f[k2]);
+        for (int k2 = 0; k2 < VPT; ++k2) {
+            const int v = lane + k2 * 32;
+            if (v >= nvec) continue;
+            T* dst = out + base + v * kVec;
+            if (vlen > k2 * 32 * kVec) {
+                float o[kVec];
 #pragma unroll
-                    for (int j = 0; j < kVec; ++j) m = fmaxf(m, f[k2][j]);
-                } else if (v == nfull && tail) {
-                    unpack(load8_smem<T>(xs + v * kVec), f[k2]);
-#pragma unroll
-                    for (int j = 0; j < kVec; ++j)
-                        if (j < tail) m = fmaxf(m, f[k2][j]);
-                }
-            }
-            m = group_max<32>(m);
-            const float ml = m * kLog2e;
-            float sum = 0.f;
-#pragma unroll
-            for (int k2 = 0; k2 < VPT; ++k2) {
-                const int v = lane + k2 * 32;
-                if (v < nfull) {
-#pragma unroll
-                    for (int j = 0; j < kVec; ++j) {
-                        f[k2][j] = exp2_approx(fmaf(f[k2][j], kLog2e, -ml));
-                        sum += f[k2][j];
-                    }
-                } else if (v == nfull && tail) {
-#pragma unroll
-                    for (int j = 0; j < kVec; ++j) {
-                        f[k2][j] = j < tail ? exp2_approx(fmaf(f[k2][j], kLog2e, -ml)) : 0.f;
-                        sum += f[k2][j];
-                    }
-                }
-            }
-            sum = group_sum<32>(sum);
-            const float inv = sum > 0.f ? 1.f / sum : 0.f;
-#pragma unroll
-            for (int k2 = 0; k2 < VPT; ++k2) {
-                const int v = lane + k2 * 32;
-                if (v >= nvec) continue;
-                T* dst = out + base + v * kVec;
-                if (v < nfull || (v == nfull && tail)) {
-                    float o[kVec];
-#pragma unroll
-                    for (int j = 0; j < kVec; ++j) o[j] = f[k2][j] * inv;
-                    store8f<T>(dst, o);
-                } else {
-                    store8<T>(dst, zero8<T>());
-                }
+                for (int j = 0; j < kVec; ++j) o[j] = f[k2][j] * inv;
+                store8f<T>(dst, o);
+            } else {
+                store8<T>(dst, zero8<T>());
             }
         }
         __syncwarp();  // every lane has used its reads of stage s
@@ -383,6 +348,7 @@ softmax_tma_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, Row
             ring.issue(s, p + rn * k_len, n, BWD ? q + rn * k_len : nullptr, BWD ? n : 0,
                        row_bytes);
         }
+    }
     }
 }
 
@@ -552,8 +518,8 @@ SmPlan plan_for(int64_t nrows, int64_t k_len) {
 RowMask make_mask(const SoftmaxShape& sh) {
     RowMask m;
     m.key_len = sh.key_len;
-    m.heads_q = sh.heads * sh.q_len;
-    m.q_len = static_cast<int>(sh.q_len);
+    m.heads_q = make_fastdiv(static_cast<uint32_t>(std::max<int64_t>(1, sh.heads * sh.q_len)));
+    m.q_len = make_fastdiv(static_cast<uint32_t>(std::max<int64_t>(1, sh.q_len)));
     m.shift = static_cast<int>(sh.k_len - sh.q_len);
     m.causal = sh.causal;
     return m;

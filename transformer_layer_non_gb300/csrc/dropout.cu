@@ -9,9 +9,9 @@
 // walks the vectors in rounds: in round k, warp w of CTA b takes the 32
 // consecutive vectors starting at (k * W + b + w * gridDim) * 32, W = all warps.
 // The last, partial round is thus spread over every CTA instead of piling onto
-// a few SMs.  Each thread keeps two register buffers of U rounds: the loads of
-// one buffer are in flight while the other is computed (two Philox calls per
-// vector, FP32 arithmetic) and stored.
+// a few SMs.  A thread handles U rounds at a time: it issues their loads,
+// draws their keep bits (two Philox calls per vector) while the loads are in
+// flight, then computes in FP32 and stores.
 //
 // Backward layout.  The bias gradient needs column sums, so the backward works
 // on 2-D tiles of 128 rows x 64 columns: lane l of an 8-lane row group owns one
@@ -110,7 +110,7 @@ __device__ __forceinline__ void fwd_compute(const Raw8<T> (&xr)[U], const Raw8<T
 }
 
 template <typename T, bool RELU, int U>
-__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 4 : 2)
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 5 : 2)
 dropout_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias,
                    const T* residual, const __grid_constant__ FwdArgs a) {
     const PhiloxSchedule& ks = a.ks;
@@ -126,24 +126,20 @@ dropout_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias
         stepU += a.step_col;
         if (stepU >= a.nvr) stepU -= a.nvr;
     }
-    Raw8<T> xa[U], ra[U], xb[U], rb[U];
-    uint32_t ka[U], kb[U];
-    fwd_load<T, RELU, U>(xa, ra, x, residual, v, S, a.nv);
-    fwd_keep<U>(ka, v, S, a, ks);
+    // One chunk of U rounds at a time: its loads are issued, its keep bits are
+    // drawn while they are in flight, then it is computed and stored.  (Measured
+    // on GB300, two register buffers per thread gain nothing here: the Philox
+    // arithmetic, not memory latency, sets the pace, and five CTAs per SM keep
+    // enough loads in flight.)
+    Raw8<T> xa[U], ra[U];
+    uint32_t ka[U];
     while (v < a.nv) {
-        const uint64_t v1 = v + U * S;
-        uint32_t cv1 = cv + stepU;
-        if (cv1 >= a.nvr) cv1 -= a.nvr;
-        fwd_load<T, RELU, U>(xb, rb, x, residual, v1, S, a.nv);
-        fwd_keep<U>(kb, v1, S, a, ks);
-        fwd_compute<T, RELU, U>(xa, ra, ka, out, mask, bias, v, cv, S, a);
-        if (v1 >= a.nv) break;
-        v = v1 + U * S;
-        cv = cv1 + stepU;
-        if (cv >= a.nvr) cv -= a.nvr;
         fwd_load<T, RELU, U>(xa, ra, x, residual, v, S, a.nv);
         fwd_keep<U>(ka, v, S, a, ks);
-        fwd_compute<T, RELU, U>(xb, rb, kb, out, mask, bias, v1, cv1, S, a);
+        fwd_compute<T, RELU, U>(xa, ra, ka, out, mask, bias, v, cv, S, a);
+        v += U * S;
+        cv += stepU;
+        if (cv >= a.nvr) cv -= a.nvr;
     }
     // Bytes of the last mask word past the last element are defined as 0.
     if (mask && a.mask_tail_bytes > 0 && blockIdx.x == 0 && threadIdx.x == 0)

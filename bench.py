@@ -19,7 +19,6 @@ of the workload (weak scaling; the path has no exchange step).
 from __future__ import annotations
 
 import argparse
-import hashlib
 import json
 import os
 import statistics
@@ -53,8 +52,9 @@ def parse_args():
                     help="seconds of oracle work for the cpu_baseline sample")
     ap.add_argument("--details", default=None, help="also write a per-op JSON report here")
     ap.add_argument("--profile-op", default=None,
-                    help="run the layer once, then only this operator inside the NVTX range "
-                         "'profile' (for ncu --nvtx --nvtx-include profile/); no timing")
+                    help="run the layer once, then only this operator ('all': every operator "
+                         "in layer order) inside the NVTX range 'profile' (for ncu --nvtx "
+                         "--nvtx-include profile/); no timing")
     ap.add_argument("--profile-launches", type=int, default=2)
     a = ap.parse_args()
     if a.warmup < 3:
@@ -284,6 +284,38 @@ def time_graph(g, reps):
     return a.elapsed_time(b) / reps
 
 
+def in_step_times(step, reps=10):
+    """Device time of each operator inside the running layer step, with CUDA
+    events on the launching stream: `reps` consecutive steps with one timing
+    event between every two operators, all queued behind a short device spin so
+    the host never lets the device idle between launches.  The events stop
+    neighbouring kernels from overlapping their prologue and tail, so the
+    headline step time is taken without them."""
+    import torch
+
+    ops = step.ops()
+    for _, fn in ops:
+        fn()
+    torch.cuda.synchronize()
+    evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps * len(ops) + 1)]
+    torch.cuda._sleep(40_000_000)  # ~20 ms of device spin while the launches queue up
+    evs[0].record()
+    k = 1
+    for _ in range(reps):
+        for _, fn in ops:
+            fn()
+            evs[k].record()
+            k += 1
+    torch.cuda.synchronize()
+    acc = {n: 0.0 for n, _ in ops}
+    k = 1
+    for _ in range(reps):
+        for n, _ in ops:
+            acc[n] += evs[k - 1].elapsed_time(evs[k])
+            k += 1
+    return {n: v / reps for n, v in acc.items()}
+
+
 def per_op_isolated(step, reps=10):
     """Device time per launch of each operator, measured alone: one graph
     replays the operator back to back over enough cloned buffer sets that
@@ -310,15 +342,6 @@ def per_op_isolated(step, reps=10):
     return res
 
 
-def kernels_sha():
-    h = hashlib.sha256()
-    csrc = os.path.join(ROOT, "transformer_layer_non_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        h.update(f.encode())
-        h.update(open(os.path.join(csrc, f), "rb").read())
-    return h.hexdigest()[:16]
-
-
 def ncu_traffic(kernel_key, workload):
     """DRAM bytes per launch from a committed ncu summary, if it was taken on
     the current kernel sources; else None."""
@@ -329,6 +352,8 @@ def ncu_traffic(kernel_key, workload):
         d = json.load(open(p))
     except ValueError:
         return None
+    from transformer_layer_non_gb300.ncu_report import kernels_sha
+
     if d.get("kernels_sha") != kernels_sha():
         return None
     e = d.get("ops", {}).get(workload, {}).get(kernel_key)
@@ -493,7 +518,9 @@ def run_ours(args):
     ms_step = ms / args.steps
     t_busy1 = time.time()
 
-    # Per-operator device time, each operator alone and L2-cold.
+    # Per-operator device time: inside the running step (events between the
+    # operators), and each operator alone over L2-cold buffer sets.
+    live = in_step_times(step)
     iso = per_op_isolated(step)
     per_op = {n: iso[n]["ms"] for n in names}
 
@@ -534,16 +561,21 @@ def run_ours(args):
     value = step_bytes * world / (ms_step * 1e-3) / 1e9
     ops_report = {}
     for n in names:
-        gbs = step.bytes[n] / (per_op[n] * 1e-3) / 1e9
-        ops_report[n] = {"us": round(per_op[n] * 1e3, 2), "bytes": int(step.bytes[n]),
+        gbs = step.bytes[n] / (live[n] * 1e-3) / 1e9
+        gbs_iso = step.bytes[n] / (per_op[n] * 1e-3) / 1e9
+        ops_report[n] = {"in_step_us": round(live[n] * 1e3, 2), "bytes": int(step.bytes[n]),
                          "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
-                         "buffer_sets": iso[n]["sets"]}
-    dominant = max(names, key=lambda n: per_op[n])
+                         "launches": step.launches[n],
+                         "alone_us": round(per_op[n] * 1e3, 2),
+                         "alone_GB/s": round(gbs_iso, 1), "alone_buffer_sets": iso[n]["sets"]}
+    dominant = max(names, key=lambda n: live[n])
     dom = ops_report[dominant]
     roofline = {"bound": "hbm", "kernel": dominant,
                 "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
                 "frac": dom["frac"], "traffic": ncu_traffic(dominant, layer.name),
-                "algorithmic_bytes": dom["bytes"], "peak_source": f"{peak_kind} hbm_gbs (copy)"}
+                "algorithmic_bytes": dom["bytes"], "duration_us": dom["in_step_us"],
+                "timing": "CUDA events around each launch inside the running step",
+                "peak_source": f"{peak_kind} hbm_gbs (copy)"}
     clocks = sampler.summary(t_busy0, t_busy1)
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
@@ -562,8 +594,10 @@ def run_ours(args):
         "pct_of_peak": round(value / world / peak * 100, 2),
         "tokens_per_s": round(layer.tokens * world / (ms_step * 1e-3), 1),
         "per_op": ops_report,
-        "per_op_note": "each operator alone, back to back over rotating L2-cold buffer sets",
-        "sum_per_op_us": round(sum(per_op.values()) * 1e3, 2),
+        "per_op_note": "in_step_us: CUDA events between the operators of the running step; "
+                       "alone_us: the operator alone, back to back over rotating L2-cold "
+                       "buffer sets",
+        "sum_in_step_us": round(sum(live.values()) * 1e3, 2),
         "roofline": roofline,
         "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
@@ -585,29 +619,39 @@ def run_ours(args):
 
 
 def run_profile_op(args):
-    """One eager pass of the whole layer (so backward inputs exist), then
-    --profile-launches calls of one operator inside the NVTX range 'profile'."""
+    """One eager pass of the whole layer (so backward inputs exist), then, inside
+    the NVTX range 'profile', --profile-launches calls of one operator, or of
+    every operator in layer order for --profile-op all (the JSON line lists the
+    kernel launches in the order they were made)."""
     import torch
 
     from transformer_layer_non_gb300 import ls_ops, synth
 
     ls_ops.load()
     step = LayerStep(synth.LAYERS[args.workload], args.seed, torch.device("cuda", 0))
-    ops = dict(step.ops())
-    if args.profile_op not in ops:
-        print(json.dumps({"error": f"unknown op {args.profile_op}", "ops": list(ops)}))
+    ops = step.ops()
+    names = [n for n, _ in ops] if args.profile_op == "all" else [args.profile_op]
+    if any(n not in dict(ops) for n in names):
+        print(json.dumps({"error": f"unknown op {args.profile_op}",
+                          "ops": ["all"] + [n for n, _ in ops]}))
         return 2
-    for _, fn in step.ops():
+    for _, fn in ops:
         fn()
     torch.cuda.synchronize()
+    order = []
     torch.cuda.nvtx.range_push("profile")
-    for _ in range(args.profile_launches):
-        ops[args.profile_op]()
+    for n in names:
+        for _ in range(args.profile_launches):
+            dict(ops)[n]()
+            order += [n] * step.launches[n]
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
+    from transformer_layer_non_gb300.ncu_report import kernels_sha
+
     print(json.dumps({"profile_op": args.profile_op, "workload": args.workload,
-                      "launches": args.profile_launches,
-                      "algorithmic_bytes": int(step.bytes[args.profile_op])}))
+                      "kernels_sha": kernels_sha(),
+                      "launches_per_op": args.profile_launches, "launch_order": order,
+                      "algorithmic_bytes": {n: int(step.bytes[n]) for n in names}}))
     return 0
 
 

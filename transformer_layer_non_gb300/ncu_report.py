@@ -112,7 +112,7 @@ def report_launches(a):
             e[2].append(op)
         ops[op] += t
     steps = len(launches) // per_step
-    alone = {n: v["alone_us"] for n, v in per_op.items()}
+    alone = {n: v.get("us", v.get("alone_us")) for n, v in per_op.items()}
     alone_sum = sum(alone.values())
     out = [f"# Kernel launch list: {bench['config']['workload']} layer step "
            "(every fused operator, forward and backward)", "",

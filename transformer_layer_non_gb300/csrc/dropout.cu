@@ -78,28 +78,25 @@ __device__ __forceinline__ void fwd_compute(const Raw8<T> (&xr)[U], const Raw8<T
     for (int u = 0; u < U; ++u) {
         const uint64_t vu = v + u * S;
         if (vu >= a.nv) break;
-        float b[kVec], xf[kVec], o[kVec];
+        float b[kVec], z[kVec], o[kVec];
         load8f<T>(bias + static_cast<size_t>(cv) * kVec, b);
-        unpack(xr[u], xf);
+        add8(xr[u], b, z);  // z = x + bias, exact conversion of x folded in
         const uint32_t keep = kp[u];
         uint32_t bits;
         if (RELU) {
             bits = 0;
 #pragma unroll
             for (int j = 0; j < kVec; ++j) {
-                const float z = xf[j] + b[j];
-                const bool on = (z > 0.f) && ((keep >> j) & 1u);
+                const bool on = (z[j] > 0.f) && ((keep >> j) & 1u);
                 bits |= on ? (1u << j) : 0u;
-                o[j] = on ? z * a.scale : 0.f;
+                o[j] = on ? z[j] * a.scale : 0.f;
             }
         } else {
             float rf[kVec];
             unpack(rr[u], rf);
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const float z = xf[j] + b[j];
-                o[j] = ((keep >> j) & 1u) ? rf[j] + z * a.scale : rf[j];
-            }
+            for (int j = 0; j < kVec; ++j)
+                o[j] = ((keep >> j) & 1u) ? rf[j] + z[j] * a.scale : rf[j];
             bits = keep;
         }
         store8f<T>(out + vu * kVec, o);

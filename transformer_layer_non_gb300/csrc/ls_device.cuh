@@ -128,6 +128,68 @@ __device__ __forceinline__ float vmax8(const Raw8<float>& r) {
                  fmaxf(fmaxf(r.b.x, r.b.y), fmaxf(r.b.z, r.b.w)));
 }
 
+// ---------------------------------------------------------------------------
+// Mixed-precision arithmetic on FP16 operands with FP32 results (PTX
+// fma.rn.f32.f16 and sub.rn.f32.f16, sm_100 and later), which saves the
+// separate conversions.  FP16 values convert to FP32 exactly and a product of
+// two FP16 values is exact in FP32, so each result equals the FP32 operation
+// on the converted operands, rounded once: the same bits as convert-then-
+// compute.
+// ---------------------------------------------------------------------------
+// acc + a[0]*b[0] + ... + a[7]*b[7], accumulated in that order.
+__device__ __forceinline__ float dot8_acc(const Raw8<__half>& a, const Raw8<__half>& b,
+                                          float acc) {
+    const uint32_t aw[4] = {a.v.x, a.v.y, a.v.z, a.v.w};
+    const uint32_t bw[4] = {b.v.x, b.v.y, b.v.z, b.v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
+            "mov.b32 {al, ah}, %1;\n\tmov.b32 {bl, bh}, %2;\n\t"
+            "fma.rn.f32.f16 %0, al, bl, %0;\n\tfma.rn.f32.f16 %0, ah, bh, %0;\n\t}"
+            : "+f"(acc)
+            : "r"(aw[k]), "r"(bw[k]));
+    return acc;
+}
+__device__ __forceinline__ float dot8_acc(const Raw8<float>& a, const Raw8<float>& b,
+                                          float acc) {
+    float x[8], y[8];
+    unpack(a, x);
+    unpack(b, y);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) acc = fmaf(x[j], y[j], acc);
+    return acc;
+}
+// t[j] = a[j] + c[j].
+__device__ __forceinline__ void add8(const Raw8<__half>& a, const float (&c)[8], float (&t)[8]) {
+    const uint32_t aw[4] = {a.v.x, a.v.y, a.v.z, a.v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        asm("{\n\t.reg .f16 al, ah;\n\tmov.b32 {al, ah}, %2;\n\t"
+            "add.rn.f32.f16 %0, al, %3;\n\tadd.rn.f32.f16 %1, ah, %4;\n\t}"
+            : "=f"(t[2 * k]), "=f"(t[2 * k + 1])
+            : "r"(aw[k]), "f"(c[2 * k]), "f"(c[2 * k + 1]));
+}
+__device__ __forceinline__ void add8(const Raw8<float>& a, const float (&c)[8], float (&t)[8]) {
+    unpack(a, t);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] += c[j];
+}
+// t[j] = a[j] - c.
+__device__ __forceinline__ void sub8(const Raw8<__half>& a, float c, float (&t)[8]) {
+    const uint32_t aw[4] = {a.v.x, a.v.y, a.v.z, a.v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        asm("{\n\t.reg .f16 al, ah;\n\tmov.b32 {al, ah}, %2;\n\t"
+            "sub.rn.f32.f16 %0, al, %3;\n\tsub.rn.f32.f16 %1, ah, %3;\n\t}"
+            : "=f"(t[2 * k]), "=f"(t[2 * k + 1])
+            : "r"(aw[k]), "f"(c));
+}
+__device__ __forceinline__ void sub8(const Raw8<float>& a, float c, float (&t)[8]) {
+    unpack(a, t);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] -= c;
+}
+
 template <typename T> __device__ __forceinline__ Raw8<T> zero8();
 template <> __device__ __forceinline__ Raw8<__half> zero8<__half>() {
     return Raw8<__half>{make_uint4(0, 0, 0, 0)};

@@ -135,7 +135,9 @@ __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y,
 }
 
 // The backward keeps per-lane branches: it moves twice the bytes per row and
-// measured faster this way than branch-free (which needs more registers).
+// measured faster this way than branch-free (which needs more registers).  A
+// vector wholly inside the valid prefix takes the unpredicated path, with the
+// FP16 conversions folded into mixed-precision instructions.
 template <typename T, int LPR, int VPT>
 __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx, int64_t row,
                                            int64_t nrows, int k_len, int gl) {
@@ -145,7 +147,9 @@ __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = gl + k * LPR;
-        if (v * kVec < vlen) {
+        if ((v + 1) * kVec <= vlen) {
+            dot = dot8_acc(buf.a[k], buf.b[k], dot);
+        } else if (v * kVec < vlen) {
             float yf[kVec], df[kVec];
             unpack(buf.a[k], yf);
             unpack(buf.b[k], df);
@@ -162,7 +166,13 @@ __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx
         const int v = gl + k * LPR;
         if (v < nvec) {
             float o[kVec];
-            if (v * kVec < vlen) {
+            if ((v + 1) * kVec <= vlen) {
+                float yf[kVec];
+                unpack(buf.a[k], yf);
+                sub8(buf.b[k], dot, o);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) o[j] *= yf[j];
+            } else if (v * kVec < vlen) {
                 float yf[kVec], df[kVec];
                 unpack(buf.a[k], yf);
                 unpack(buf.b[k], df);

@@ -44,40 +44,49 @@ struct FwdArgs {
     int mask_tail_bytes;
 };
 
-template <typename T, bool RELU, int U>
+template <typename T, bool RELU, int U, typename I>
 __device__ __forceinline__ void fwd_load(Raw8<T> (&xr)[U], Raw8<T> (&rr)[U], const T* x,
-                                         const T* residual, uint64_t v, uint64_t S, uint64_t nv) {
+                                         const T* residual, I v, I S, I nv) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const uint64_t vu = v + u * S;
+        const I vu = v + u * S;
         if (vu < nv) {
-            xr[u] = load8<T>(x + vu * kVec);
-            if (!RELU) rr[u] = load8<T>(residual + vu * kVec);
+            xr[u] = load8<T>(x + static_cast<size_t>(vu) * kVec);
+            if (!RELU) rr[u] = load8<T>(residual + static_cast<size_t>(vu) * kVec);
         }
     }
 }
 
 // Keep bits of the U vectors of a chunk; called right after the chunk's loads
 // are issued, so the Philox arithmetic overlaps their latency.
-template <int U>
-__device__ __forceinline__ void fwd_keep(uint32_t (&keep)[U], uint64_t v, uint64_t S,
+// With 32-bit indices (the host picks them when every vector index and its
+// counter block 2 * vector index fit in 32 bits) the block's high word is 0.
+template <int U, typename I>
+__device__ __forceinline__ void fwd_keep(uint32_t (&keep)[U], I v, I S, I nv,
                                          const FwdArgs& a, const PhiloxSchedule& ks) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const uint64_t vu = v + u * S;
-        keep[u] = vu < a.nv ? keep_bits8(vu * kVec, a.thr, ks, a.off_lo, a.off_hi) : 0u;
+        const I vu = v + u * S;
+        if (sizeof(I) == 4)
+            keep[u] = vu < nv ? keep_bits8_blk(static_cast<uint32_t>(vu) * 2u, 0u, a.thr, ks,
+                                               a.off_lo, a.off_hi)
+                              : 0u;
+        else
+            keep[u] = vu < nv ? keep_bits8(static_cast<uint64_t>(vu) * kVec, a.thr, ks, a.off_lo,
+                                           a.off_hi)
+                              : 0u;
     }
 }
 
-template <typename T, bool RELU, int U>
+template <typename T, bool RELU, int U, typename I>
 __device__ __forceinline__ void fwd_compute(const Raw8<T> (&xr)[U], const Raw8<T> (&rr)[U],
                                             const uint32_t (&kp)[U], T* out, uint8_t* mask,
-                                            const T* __restrict__ bias, uint64_t v, uint32_t cv,
-                                            uint64_t S, const FwdArgs& a) {
+                                            const T* __restrict__ bias, I v, uint32_t cv, I S,
+                                            I nv, const FwdArgs& a) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const uint64_t vu = v + u * S;
-        if (vu >= a.nv) break;
+        const I vu = v + u * S;
+        if (vu >= nv) break;
         float b[kVec], z[kVec], o[kVec];
         load8f<T>(bias + static_cast<size_t>(cv) * kVec, b);
         add8(xr[u], b, z);  // z = x + bias, exact conversion of x folded in
@@ -99,22 +108,23 @@ __device__ __forceinline__ void fwd_compute(const Raw8<T> (&xr)[U], const Raw8<T
                 o[j] = ((keep >> j) & 1u) ? rf[j] + z[j] * a.scale : rf[j];
             bits = keep;
         }
-        store8f<T>(out + vu * kVec, o);
+        store8f<T>(out + static_cast<size_t>(vu) * kVec, o);
         if (mask) mask[vu] = static_cast<uint8_t>(bits);
         cv += a.step_col;
         if (cv >= a.nvr) cv -= a.nvr;
     }
 }
 
-template <typename T, bool RELU, int U>
+template <typename T, bool RELU, int U, typename I>
 __global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 5 : 2)
 dropout_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias,
                    const T* residual, const __grid_constant__ FwdArgs a) {
     const PhiloxSchedule& ks = a.ks;
     pdl_enter();
-    const uint64_t S = static_cast<uint64_t>(gridDim.x) * kThreads;  // vectors per round
-    const uint64_t gw = blockIdx.x + static_cast<uint64_t>(threadIdx.x >> 5) * gridDim.x;
-    uint64_t v = gw * 32 + (threadIdx.x & 31);
+    const I nv = static_cast<I>(a.nv);
+    const I S = static_cast<I>(gridDim.x) * kThreads;  // vectors per round
+    const I gw = blockIdx.x + static_cast<I>(threadIdx.x >> 5) * gridDim.x;
+    I v = gw * 32 + (threadIdx.x & 31);
     uint32_t cv = static_cast<uint32_t>(v % a.nvr);
     // (U rounds) mod nvr, from the per-round step.
     uint32_t stepU = 0;
@@ -130,10 +140,10 @@ dropout_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias
     // enough loads in flight.)
     Raw8<T> xa[U], ra[U];
     uint32_t ka[U];
-    while (v < a.nv) {
-        fwd_load<T, RELU, U>(xa, ra, x, residual, v, S, a.nv);
-        fwd_keep<U>(ka, v, S, a, ks);
-        fwd_compute<T, RELU, U>(xa, ra, ka, out, mask, bias, v, cv, S, a);
+    while (v < nv) {
+        fwd_load<T, RELU, U>(xa, ra, x, residual, v, S, nv);
+        fwd_keep<U>(ka, v, S, nv, a, ks);
+        fwd_compute<T, RELU, U>(xa, ra, ka, out, mask, bias, v, cv, S, nv, a);
         v += U * S;
         cv += stepU;
         if (cv >= a.nvr) cv -= a.nvr;
@@ -317,8 +327,7 @@ template <typename T, bool RELU>
 cudaError_t fwd_impl(void* out, uint8_t* mask, const void* x, const void* bias,
                      const void* residual, int64_t rows, int64_t cols, const DropoutRng& rng,
                      cudaStream_t s) {
-    auto kern = dropout_fwd_kernel<T, RELU, kFwdU>;
-    static const int occ = occupancy(kern, kThreads, 0);
+    static const int occ = occupancy(dropout_fwd_kernel<T, RELU, kFwdU, uint64_t>, kThreads, 0);
     FwdArgs a;
     a.nv = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols) / kVec;
     a.nvr = static_cast<uint32_t>(cols / kVec);
@@ -331,6 +340,13 @@ cudaError_t fwd_impl(void* out, uint8_t* mask, const void* x, const void* bias,
     a.off_lo = static_cast<uint32_t>(rng.offset);
     a.off_hi = static_cast<uint32_t>(rng.offset >> 32);
     a.mask_tail_bytes = static_cast<int>(((a.nv + 3) / 4) * 4 - a.nv);
+    // 32-bit indices when no index the loop forms (up to nv + (U+1) rounds) and
+    // no counter block (2 * index) reaches 2^32.
+    const bool narrow =
+        a.nv + static_cast<uint64_t>(kFwdU + 1) * static_cast<uint64_t>(grid) * kThreads <
+        (uint64_t{1} << 31);
+    auto kern = narrow ? dropout_fwd_kernel<T, RELU, kFwdU, uint32_t>
+                       : dropout_fwd_kernel<T, RELU, kFwdU, uint64_t>;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
                       static_cast<T*>(out), mask, static_cast<const T*>(x),
                       static_cast<const T*>(bias), static_cast<const T*>(residual), a);

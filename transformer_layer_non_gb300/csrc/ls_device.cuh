@@ -249,21 +249,24 @@ __device__ __forceinline__ uint4 philox4x32_10(uint4 c, const PhiloxSchedule& ks
 }
 
 // Dropout keep bits of the 8 consecutive elements starting at flat index i
-// (i a multiple of 4): element i+j draws word j&3 of counter block (i>>2)+(j>>2).
-// Bit j of the result is set iff element i+j is kept (word >= thr).
-__device__ __forceinline__ uint32_t keep_bits8(uint64_t i, uint32_t thr, const PhiloxSchedule& ks,
-                                               uint32_t off_lo, uint32_t off_hi) {
-    const uint64_t blk = i >> 2;
-    const uint4 a = philox4x32_10(
-        make_uint4(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), off_lo, off_hi),
-        ks);
-    const uint64_t blk1 = blk + 1;
-    const uint4 b = philox4x32_10(
-        make_uint4(static_cast<uint32_t>(blk1), static_cast<uint32_t>(blk1 >> 32), off_lo, off_hi),
-        ks);
+// (i a multiple of 4), given as its counter block b = i >> 2 = (lo, hi):
+// element i+j draws word j&3 of counter block b+(j>>2).  Bit j of the result is
+// set iff element i+j is kept (word >= thr).
+__device__ __forceinline__ uint32_t keep_bits8_blk(uint32_t lo, uint32_t hi, uint32_t thr,
+                                                   const PhiloxSchedule& ks, uint32_t off_lo,
+                                                   uint32_t off_hi) {
+    const uint4 a = philox4x32_10(make_uint4(lo, hi, off_lo, off_hi), ks);
+    const uint32_t lo1 = lo + 1u;
+    const uint4 b = philox4x32_10(make_uint4(lo1, hi + (lo1 == 0u ? 1u : 0u), off_lo, off_hi), ks);
     return (a.x >= thr ? 1u : 0u) | (a.y >= thr ? 2u : 0u) | (a.z >= thr ? 4u : 0u) |
            (a.w >= thr ? 8u : 0u) | (b.x >= thr ? 16u : 0u) | (b.y >= thr ? 32u : 0u) |
            (b.z >= thr ? 64u : 0u) | (b.w >= thr ? 128u : 0u);
+}
+__device__ __forceinline__ uint32_t keep_bits8(uint64_t i, uint32_t thr, const PhiloxSchedule& ks,
+                                               uint32_t off_lo, uint32_t off_hi) {
+    const uint64_t blk = i >> 2;
+    return keep_bits8_blk(static_cast<uint32_t>(blk), static_cast<uint32_t>(blk >> 32), thr, ks,
+                          off_lo, off_hi);
 }
 
 // e^x as 2^(x * log2 e), with 2^y from the PTX ex2.approx instruction (relative

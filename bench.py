@@ -36,6 +36,7 @@ UNIT = "GB/s"
 DEFAULT_WORKLOAD = "bert-base"
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
+SWEEP_K_LENS = (16, 32, 64, 128, 256, 512, 1024, 2048, 4096)
 
 
 def parse_args():
@@ -56,6 +57,9 @@ def parse_args():
                          "in layer order) inside the NVTX range 'profile' (for ncu --nvtx "
                          "--nvtx-include profile/); no timing")
     ap.add_argument("--profile-launches", type=int, default=2)
+    ap.add_argument("--sweep", action="store_true",
+                    help="time the softmax row-length sweep (k_len 16..4096, 2^22 elements "
+                         "each, random valid lengths) forward and backward; one JSON line")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -656,12 +660,68 @@ def run_profile_op(args):
     return 0
 
 
+def run_sweep(args):
+    """Softmax forward and backward over the row-length sweep: each row length
+    alone, back to back over enough cloned buffer sets that every launch finds
+    its inputs outside L2 (one case is 16 MB, well inside L2)."""
+    import math
+
+    import torch
+
+    from transformer_layer_non_gb300 import accounting, ls_ops, synth
+
+    ls_ops.load()
+    dev = torch.device("cuda", 0)
+    peak, peak_kind = load_peaks()
+    rows_out = {}
+    for k_len in SWEEP_K_LENS:
+        x, dy, kl = synth.sweep_inputs(k_len, args.seed)
+        b, h, q, k = x.shape
+        t = {"x": torch.from_numpy(x).to(dev), "dy": torch.from_numpy(dy).to(dev),
+             "kl": torch.from_numpy(kl).to(dev), "y": torch.empty(x.shape, dtype=torch.float16,
+                                                                   device=dev),
+             "dx": torch.empty(x.shape, dtype=torch.float16, device=dev)}
+        ls_ops.ls_softmax_fwd(t["y"], t["x"], t["kl"], False)
+        nbytes = {"fwd": accounting.softmax_fwd_bytes(b, h, q, k, 2, kl, False),
+                  "bwd": accounting.softmax_bwd_bytes(b, h, q, k, 2, kl, False)}
+        fp = {"fwd": 2 * x.nbytes, "bwd": 3 * x.nbytes}
+        res = {}
+        for d in ("fwd", "bwd"):
+            nsets = max(2, min(64, math.ceil(3 * L2_BYTES / fp[d])))
+            sets = [{n: v.clone() for n, v in t.items()} for _ in range(nsets)]
+            if d == "fwd":
+                thunks = [(lambda s=s: ls_ops.ls_softmax_fwd(s["y"], s["x"], s["kl"], False))
+                          for s in sets]
+            else:
+                thunks = [(lambda s=s: ls_ops.ls_softmax_bwd(s["dx"], s["y"], s["dy"], s["kl"],
+                                                            False)) for s in sets]
+            ms = time_graph(capture(thunks), 20) / nsets
+            gbs = nbytes[d] / (ms * 1e-3) / 1e9
+            res[d] = {"us": round(ms * 1e3, 2), "bytes": int(nbytes[d]), "GB/s": round(gbs, 1),
+                      "frac": round(gbs / peak, 4), "buffer_sets": nsets}
+            del sets, thunks
+        rows_out[str(k_len)] = res
+    line = {"metric": "softmax sweep: achieved HBM GB/s per row length", "unit": "GB/s",
+            "peak": peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
+            "config": {"workload": "softmax-sweep", "elements": synth.SWEEP_ELEMENTS,
+                       "valid_len": "U[1, k_len] per row", "storage": "f16",
+                       "l2": "rotating cloned buffer sets >= 3 x L2"},
+            "k_len": rows_out}
+    print(json.dumps(line), flush=True)
+    if args.details:
+        with open(args.details, "w") as f:
+            json.dump(line, f, indent=1)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
         return run_reference(args)
     if args.profile_op:
         return run_profile_op(args)
+    if args.sweep:
+        return run_sweep(args)
     return run_ours(args)
 
 

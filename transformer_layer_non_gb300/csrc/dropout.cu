@@ -276,20 +276,23 @@ dropout_bwd_kernel(T* dx, float* __restrict__ partial, const T* dout,
 
 // ---------------------------------------------------------------------------
 // Fixed-order column reduction: partial [parts, width] FP32 -> out0/out1.
-// Group g of a CTA adds rows g, g + G, ...; the G group sums are then added in
-// group order.
+// A CTA covers COLS columns with 32 groups; group g adds rows g, g + 32, ... of
+// its column in that order, then the 32 group sums are added in group order.
+// The association depends only on (parts, width).  Few partial rows take
+// narrow 8-column CTAs (more CTAs, one load each); many take 32 columns per
+// CTA (measured on GB300: each faster in its own range).
 // ---------------------------------------------------------------------------
-constexpr int kRedCols = 32;
 constexpr int kRedGroups = 32;
-template <typename T>
-__global__ void __launch_bounds__(kRedCols* kRedGroups)
+constexpr int64_t kRedNarrowMaxParts = 64;
+template <typename T, int COLS>
+__global__ void __launch_bounds__(COLS* kRedGroups)
 colreduce_kernel(T* __restrict__ out0, T* __restrict__ out1, int64_t split,
                  const float* __restrict__ partial, int64_t parts, int64_t width) {
-    __shared__ float sm[kRedGroups][kRedCols + 1];
+    __shared__ float sm[kRedGroups][COLS + 1];
     pdl_enter();
-    const int cx = threadIdx.x % kRedCols;
-    const int gy = threadIdx.x / kRedCols;
-    const int64_t col = static_cast<int64_t>(blockIdx.x) * kRedCols + cx;
+    const int cx = threadIdx.x % COLS;
+    const int gy = threadIdx.x / COLS;
+    const int64_t col = static_cast<int64_t>(blockIdx.x) * COLS + cx;
     float s = 0.f;
     if (col < width) {
 #pragma unroll 4
@@ -384,15 +387,22 @@ ColReducePlan dropout_bwd_plan(int64_t rows, int64_t cols) {
     return ColReducePlan{(rows + kBwdRowsPerTile - 1) / kBwdRowsPerTile, cols};
 }
 
+template <typename T, int COLS>
+cudaError_t colreduce_impl(void* out0, void* out1, int64_t split, const float* partial,
+                           int64_t parts, int64_t width, cudaStream_t s) {
+    const dim3 grid(static_cast<unsigned>((width + COLS - 1) / COLS));
+    return launch_pdl(colreduce_kernel<T, COLS>, grid, dim3(COLS * kRedGroups), 0, s,
+                      static_cast<T*>(out0), static_cast<T*>(out1), split, partial, parts, width);
+}
+
 cudaError_t launch_colreduce(DType dt, void* out0, void* out1, int64_t split,
                              const float* partial, int64_t parts, int64_t width, cudaStream_t s) {
-    const dim3 grid(static_cast<unsigned>((width + kRedCols - 1) / kRedCols));
-    const dim3 block(kRedCols * kRedGroups);
+    const bool narrow = parts <= kRedNarrowMaxParts;
     if (dt == DType::F16)
-        return launch_pdl(colreduce_kernel<__half>, grid, block, 0, s, static_cast<__half*>(out0),
-                          static_cast<__half*>(out1), split, partial, parts, width);
-    return launch_pdl(colreduce_kernel<float>, grid, block, 0, s, static_cast<float*>(out0),
-                      static_cast<float*>(out1), split, partial, parts, width);
+        return narrow ? colreduce_impl<__half, 8>(out0, out1, split, partial, parts, width, s)
+                      : colreduce_impl<__half, 32>(out0, out1, split, partial, parts, width, s);
+    return narrow ? colreduce_impl<float, 8>(out0, out1, split, partial, parts, width, s)
+                  : colreduce_impl<float, 32>(out0, out1, split, partial, parts, width, s);
 }
 
 cudaError_t launch_dropout_fwd(DType dt, bool relu, void* out, uint8_t* mask, const void* x,

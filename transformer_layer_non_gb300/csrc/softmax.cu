@@ -69,11 +69,17 @@ struct RowBuf {
     int vlen;
 };
 
+// Valid length of a row, 0 past the last row.  With per-batch key lengths it
+// costs a dependent load, so the kernels fetch it one row ahead of the row's
+// data loads.
+__device__ __forceinline__ int row_vlen(int64_t row, int64_t nrows, int k_len, const RowMask& mk) {
+    return row < nrows ? valid_len(row, k_len, mk) : 0;
+}
+
 template <typename T, int LPR, int VPT, bool BWD>
 __device__ __forceinline__ void sm_load(RowBuf<T, LPR, VPT>& buf, const T* p, const T* q,
-                                        int64_t row, int64_t nrows, int k_len,
-                                        const RowMask& mk, int gl) {
-    buf.vlen = row < nrows ? valid_len(row, k_len, mk) : 0;
+                                        int64_t row, int vlen, int k_len, int gl) {
+    buf.vlen = vlen;
     const int64_t base = row * k_len;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -201,26 +207,32 @@ softmax_group_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, R
     RowBuf<T, LPR, VPT> ba, bb;
     if (VPT > 2) {
         // Wide rows: one buffer (a second would cost occupancy).
+        int vl = row_vlen(r, nrows, k_len, mk);
         for (; __any_sync(0xffffffffu, r < nrows); r += stride) {
-            sm_load<T, LPR, VPT, BWD>(ba, p, q, r, nrows, k_len, mk, gl);
+            const int vln = row_vlen(r + stride, nrows, k_len, mk);
+            sm_load<T, LPR, VPT, BWD>(ba, p, q, r, vl, k_len, gl);
             if (BWD)
                 sm_bwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
             else
                 sm_fwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
+            vl = vln;
         }
         return;
     }
-    sm_load<T, LPR, VPT, BWD>(ba, p, q, r, nrows, k_len, mk, gl);
+    sm_load<T, LPR, VPT, BWD>(ba, p, q, r, row_vlen(r, nrows, k_len, mk), k_len, gl);
+    int vl_next = row_vlen(r + stride, nrows, k_len, mk);  // the row bb takes next
     while (__any_sync(0xffffffffu, r < nrows)) {
         const int64_t r1 = r + stride;
-        sm_load<T, LPR, VPT, BWD>(bb, p, q, r1, nrows, k_len, mk, gl);
+        sm_load<T, LPR, VPT, BWD>(bb, p, q, r1, vl_next, k_len, gl);
+        vl_next = row_vlen(r1 + stride, nrows, k_len, mk);
         if (BWD)
             sm_bwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
         else
             sm_fwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
         if (!__any_sync(0xffffffffu, r1 < nrows)) break;
         r = r1 + stride;
-        sm_load<T, LPR, VPT, BWD>(ba, p, q, r, nrows, k_len, mk, gl);
+        sm_load<T, LPR, VPT, BWD>(ba, p, q, r, vl_next, k_len, gl);
+        vl_next = row_vlen(r + stride, nrows, k_len, mk);
         if (BWD)
             sm_bwd_row<T, LPR, VPT>(bb, out, r1, nrows, k_len, gl);
         else

@@ -302,25 +302,26 @@ ln_bwd_group_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
 }
 
 // ----------------------------------------------------------------------------
-// Backward, warp per row, rows fed by bulk copies (256 <= H <= 1280).  CTA b
-// owns rows [b*R, (b+1)*R) (R from the shape-only plan); warp w takes rows
-// b*R + w + 8k.  Each warp's x and dy rows arrive in a two-stage ring of shared
-// memory (cp.async.bulk, bounded mbarrier waits), so both of a warp's rows are
-// in flight at once without holding them in registers.  dgamma/dbeta partial
+// Backward, warp per row, rows fed by bulk copies (136 <= H <= 1280 while the
+// ring fits in 200 KB).  One 16-warp CTA per SM: CTA b owns rows [b*R,
+// (b+1)*R) (R from the shape-only plan, about rows/152); warp w takes rows
+// b*R + w + 16k.  Each warp's x and dy rows arrive in a two-stage ring of
+// shared memory (cp.async.bulk, bounded mbarrier waits), so both of a warp's
+// rows are in flight at once without holding them in registers.  dgamma/dbeta partial
 // sums stay in registers (each lane owns the same columns in every row); when
 // all rows are done the warps' sums are added in warp order through the
 // (now free) stage memory into partial[b, 0:2H].
 // ----------------------------------------------------------------------------
-constexpr int kLnTmaWarps = 8;
+constexpr int kLnTmaWarps = 16;
 constexpr int kLnTmaStages = 2;
-constexpr uint32_t kLnTmaBarBytes = 128;  // 8 warps x 2 stages x 8 bytes
+constexpr uint32_t kLnTmaBarBytes = 256;  // 16 warps x 2 stages x 8 bytes
 // Shared-memory layout: barriers | gamma (cols, rounded to 128 B) | stages.
 __host__ __device__ inline size_t ln_tma_gamma_bytes(int cols, size_t esize) {
     return ((static_cast<size_t>(cols) * esize + 127) / 128) * 128;
 }
 
 template <typename T, int VPT>
-__global__ void __launch_bounds__(kLnTmaWarps * 32, 2)
+__global__ void __launch_bounds__(kLnTmaWarps * 32, 1)
 ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
                   const T* __restrict__ gamma, const float* __restrict__ mean,
                   const float* __restrict__ rstd, int64_t rows, int cols, int rows_per_cta) {
@@ -564,8 +565,24 @@ struct LnPlan {
 // constant, not the device's SM count, so that the partial sums -- and with
 // them the bits of dgamma/dbeta -- do not depend on which GPU runs the call.
 constexpr int64_t kBwdTargetCtas = 304;
+// The bulk-copy backward runs one 16-warp CTA per SM (measured on GB300: faster
+// than two 8-warp CTAs per SM, and half the partial rows).
+constexpr int64_t kBwdTmaTargetCtas = 152;
+constexpr size_t kLnTmaMaxSmem = 200 * 1024;
 
-LnPlan plan_for(int64_t rows, int64_t cols, bool bwd) {
+size_t ln_tma_smem(int64_t cols, size_t esize) {
+    return kLnTmaBarBytes + ln_tma_gamma_bytes(static_cast<int>(cols), esize) +
+           static_cast<size_t>(kLnTmaWarps) * kLnTmaStages * 2 * static_cast<size_t>(cols) * esize;
+}
+
+// Whether the backward of rows of `cols` elements of `esize` bytes takes the
+// bulk-copy kernel (warp per row, 1..5 vectors per lane, its ring fits).
+bool ln_bwd_uses_tma(int64_t cols, size_t esize) {
+    const int64_t nvec = cols / kVec;
+    return nvec > 16 && nvec <= 5 * 32 && ln_tma_smem(cols, esize) <= kLnTmaMaxSmem;
+}
+
+LnPlan plan_for(int64_t rows, int64_t cols, bool bwd, size_t esize) {
     const int nvec = static_cast<int>(cols / kVec);
     LnPlan p{};
     if (nvec <= kCtaRowThreshold) {
@@ -579,8 +596,9 @@ LnPlan plan_for(int64_t rows, int64_t cols, bool bwd) {
         }
         const int64_t rpc = kThreads / p.lpr;
         if (bwd) {
-            p.steps = static_cast<int>(
-                std::max<int64_t>(1, (rows + kBwdTargetCtas - 1) / kBwdTargetCtas));
+            const int64_t target = ln_bwd_uses_tma(cols, esize) ? kBwdTmaTargetCtas
+                                                                : kBwdTargetCtas;
+            p.steps = static_cast<int>(std::max<int64_t>(1, (rows + target - 1) / target));
             p.grid = (rows + p.steps - 1) / p.steps;
         } else {
             p.steps = 1;
@@ -646,10 +664,8 @@ cudaError_t bwd_group(void* dx, float* partial, const void* dy, const void* x, c
                       const float* mean, const float* rstd, int64_t rows, int64_t cols,
                       const LnPlan& p, cudaStream_t s) {
     if constexpr (LPR == 32 && VPT >= 1 && VPT <= 5) {
-        const size_t smem = kLnTmaBarBytes + ln_tma_gamma_bytes(static_cast<int>(cols), sizeof(T)) +
-                            static_cast<size_t>(kLnTmaWarps) * kLnTmaStages * 2 *
-                                static_cast<size_t>(cols) * sizeof(T);
-        if (smem <= 110 * 1024) {
+        if (ln_bwd_uses_tma(cols, sizeof(T))) {
+            const size_t smem = ln_tma_smem(cols, sizeof(T));
             auto kern = ln_bwd_tma_kernel<T, VPT>;
             cudaError_t e = set_smem(kern, smem);
             if (e != cudaSuccess) return e;
@@ -730,7 +746,7 @@ template <typename T>
 cudaError_t fwd_dispatch(void* y, float* mean, float* rstd, const void* x, const void* gamma,
                          const void* beta, int64_t rows, int64_t cols, float eps,
                          cudaStream_t s) {
-    const LnPlan p = plan_for(rows, cols, false);
+    const LnPlan p = plan_for(rows, cols, false, sizeof(T));
     if (!p.cta) {
         LS_GROUP_CASES(fwd_group, T, y, mean, rstd, x, gamma, beta, rows, cols, eps, p, s)
     } else {
@@ -742,7 +758,7 @@ template <typename T>
 cudaError_t bwd_dispatch(void* dx, float* partial, const void* dy, const void* x,
                          const void* gamma, const float* mean, const float* rstd, int64_t rows,
                          int64_t cols, cudaStream_t s) {
-    const LnPlan p = plan_for(rows, cols, true);
+    const LnPlan p = plan_for(rows, cols, true, sizeof(T));
     if (!p.cta) {
         LS_GROUP_CASES(bwd_group, T, dx, partial, dy, x, gamma, mean, rstd, rows, cols, p, s)
     } else {
@@ -752,8 +768,8 @@ cudaError_t bwd_dispatch(void* dx, float* partial, const void* dy, const void* x
 
 }  // namespace
 
-ColReducePlan layernorm_bwd_plan(int64_t rows, int64_t cols) {
-    const LnPlan p = plan_for(rows, cols, true);
+ColReducePlan layernorm_bwd_plan(int64_t rows, int64_t cols, size_t esize) {
+    const LnPlan p = plan_for(rows, cols, true, esize);
     return ColReducePlan{p.grid, 2 * cols};
 }
 

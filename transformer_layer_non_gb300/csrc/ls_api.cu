@@ -191,7 +191,10 @@ ls_status ls_check_device_errors(uint32_t* flags) {
 size_t ls_colreduce_workspace_bytes(int64_t rows, int64_t cols) {
     if (rows <= 0 || cols <= 0 || cols % 8 != 0) return 0;
     const size_t a = ls::dropout_bwd_plan(rows, cols).bytes();
-    const size_t b = cols <= ls::kMaxRowLen ? ls::layernorm_bwd_plan(rows, cols).bytes() : 0;
+    const size_t b = cols <= ls::kMaxRowLen
+                         ? std::max(ls::layernorm_bwd_plan(rows, cols, 2).bytes(),
+                                    ls::layernorm_bwd_plan(rows, cols, 4).bytes())
+                         : 0;
     return std::max(a, b);
 }
 
@@ -363,7 +366,7 @@ ls_status ls_layernorm_bwd(ls_dtype dtype, void* dx, void* dgamma, void* dbeta, 
     LS_TRY(check_ptr(gamma, "gamma", true));
     LS_TRY(check_ptr(mean, "mean", true));
     LS_TRY(check_ptr(rstd, "rstd", true));
-    const ls::ColReducePlan plan = ls::layernorm_bwd_plan(rows, cols);
+    const ls::ColReducePlan plan = ls::layernorm_bwd_plan(rows, cols, elem_size(dt));
     if (dgamma) {
         LS_TRY(check_ptr(workspace, "workspace", true));
         if (workspace_bytes < plan.bytes())

@@ -27,7 +27,7 @@ struct ColReducePlan {
     size_t bytes() const { return static_cast<size_t>(parts * width) * sizeof(float); }
 };
 ColReducePlan dropout_bwd_plan(int64_t rows, int64_t cols);
-ColReducePlan layernorm_bwd_plan(int64_t rows, int64_t cols);
+ColReducePlan layernorm_bwd_plan(int64_t rows, int64_t cols, size_t esize);  // esize: 2 or 4
 
 // Sum `parts` FP32 rows of `width` columns in a fixed order; columns
 // [0, split) go to out0[0..split) and columns [split, width) to

@@ -67,7 +67,7 @@ extern "C" ls_status ls_layernorm_bwd_noalloc(ls_dtype dtype, void* dx, void* dg
                                 nullptr, 0, stream);
     // Reject shapes whose partial sums do not fit, before touching the GPU.
     if (rows > 0 && cols > 0 && cols % 8 == 0 && cols <= ls::kMaxRowLen) {
-        const size_t need = ls::layernorm_bwd_plan(rows, cols).bytes();
+        const size_t need = ls::layernorm_bwd_plan(rows, cols, dtype == LS_F32 ? 4 : 2).bytes();
         if (need > kNoAllocScratchBytes) {
             ls::set_last_error_message(
                 "ls_layernorm_bwd_noalloc: rows=%lld cols=%lld need %zu bytes of scratch; the "

@@ -74,6 +74,21 @@ def load_peaks():
     return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(value: float, dist, device) -> float:
+    """The largest of every rank's value (all ranks get it)."""
+    import torch
+
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbs(step_bytes: float, world: int, ms_step: float) -> float:
+    """Bytes all ranks moved per step (each rank runs its own replica) over the
+    slowest rank's step time."""
+    return step_bytes * world / (ms_step * 1e-3) / 1e9
+
+
 def dist_env():
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -421,15 +436,43 @@ def calibrated_oracle(layer, budget_s, seed=0):
     return oracle_sample_step(layer, frac, seed)
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu), else the machine type."""
+    import platform
+
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except (OSError, subprocess.SubprocessError):
+        pass
+    return platform.machine()
+
+
 def cpu_baseline(layer, budget_s):
+    """The oracle on the host cores (all of them, rows spread by OpenMP), then
+    on one core over a sample sized for about a third of the budget."""
     import oracle
 
+    cores = oracle.num_threads()
     run, nbytes, frac, sample = calibrated_oracle(layer, budget_s)
     t0 = time.perf_counter()
     run()
     dt = time.perf_counter() - t0
-    return {"value": round(nbytes / dt / 1e9, 3), "unit": UNIT, "cores": oracle.num_threads(),
-            "kind": "oracle", "sample": sample, "seconds": round(dt, 2)}
+    res = {"value": round(nbytes / dt / 1e9, 3), "unit": UNIT, "cores": cores,
+           "kind": "oracle", "sample": sample, "seconds": round(dt, 2), "cpu": cpu_model()}
+    try:
+        oracle.set_num_threads(1)
+        run1, nbytes1, _, sample1 = calibrated_oracle(layer, budget_s / 3)
+        t0 = time.perf_counter()
+        run1()
+        dt1 = time.perf_counter() - t0
+        res["single_core"] = {"value": round(nbytes1 / dt1 / 1e9, 4), "sample": sample1,
+                              "seconds": round(dt1, 2)}
+    finally:
+        oracle.set_num_threads(cores)
+    return res
 
 
 def run_reference(args):
@@ -597,9 +640,7 @@ def run_ours(args):
         pg.barrier()
     ms = e0.elapsed_time(e1)
     if pg:
-        t = torch.tensor([ms], device=device)
-        pg.all_reduce(t, op=pg.ReduceOp.MAX)
-        ms = float(t.item())
+        ms = max_over_ranks(ms, pg, device)
     ms_step = ms / args.steps
     t_busy1 = time.time()
 
@@ -626,7 +667,7 @@ def run_ours(args):
             pg.destroy_process_group()
         return 0
     peak, peak_kind = load_peaks()
-    value = step_bytes * world / (ms_step * 1e-3) / 1e9
+    value = whole_job_gbs(step_bytes, world, ms_step)
     ops_report = {}
     for n in names:
         gbs = step.bytes[n] / (per_op[n] * 1e-3) / 1e9
@@ -634,6 +675,13 @@ def run_ours(args):
                          "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
                          "launches": step.launches[n], "buffer_sets": iso[n]["sets"],
                          "in_step_events_us": round(live[n] * 1e3, 2)}
+        if n.startswith("softmax"):
+            # as if masked scores were read too: one read and one write per
+            # element forward, two reads and one write backward
+            dense = layer.batch * layer.heads * layer.seq * layer.seq * step.esize * (
+                2 if n == "softmax_fwd" else 3)
+            ops_report[n]["dense_bytes"] = int(dense)
+            ops_report[n]["dense_GB/s"] = round(dense / (per_op[n] * 1e-3) / 1e9, 1)
     dominant = max(names, key=lambda n: per_op[n])
     dom = ops_report[dominant]
     roofline = {"bound": "hbm", "kernel": dominant,

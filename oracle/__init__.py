@@ -64,6 +64,7 @@ def _load():
         "or_softmax_fwd": (None, [i64, i64, i64, i64, P, P, cint, P]),
         "or_softmax_bwd": (None, [i64, i64, i64, i64, P, P, P, cint, P]),
         "or_num_threads": (cint, []),
+        "or_set_num_threads": (None, [cint]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -88,6 +89,11 @@ def mask_words(n: int) -> int:
 
 def num_threads() -> int:
     return _load().or_num_threads()
+
+
+def set_num_threads(n: int) -> None:
+    """Threads for the row loops of later calls (OpenMP)."""
+    _load().or_set_num_threads(int(n))
 
 
 def philox4x32_10(ctr, key) -> np.ndarray:

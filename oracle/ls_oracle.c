@@ -324,3 +324,11 @@ int or_num_threads(void) {
     return 1;
 #endif
 }
+
+void or_set_num_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}

@@ -71,8 +71,9 @@ void or_softmax_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
                     const double* y, const double* dy, const int32_t* key_len, int causal,
                     double* dx);
 
-/* OpenMP threads the row loops use. */
+/* OpenMP threads the row loops use, and setting them (n > 0). */
 int or_num_threads(void);
+void or_set_num_threads(int n);
 
 #ifdef __cplusplus
 }

@@ -65,6 +65,7 @@ def _load():
         "or_softmax_bwd": (None, [i64, i64, i64, i64, P, P, P, cint, P]),
         "or_num_threads": (cint, []),
         "or_set_num_threads": (None, [cint]),
+        "or_adam_update": (None, [i64, P, P, P, P, f64, f64, f64, f64, f64, i64, f64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -207,3 +208,16 @@ def softmax_bwd(y, dy, key_len=None, causal=False):
     dx = np.empty_like(y)
     _load().or_softmax_bwd(b, h, lq, lk, _ptr(y), _ptr(dy), _ptr(kl), int(bool(causal)), _ptr(dx))
     return dx
+
+
+def adam_update(p, g, m, v, lr, beta1, beta2, eps, weight_decay, step, grad_scale=1.0):
+    """One trainer update of a flat workspace: returns (p', m', v') in float64.
+    Hyperparameters are taken as given (pass the FP32 values the GPU gets)."""
+    p, g, m, v = (_f64(a).ravel() for a in (p, g, m, v))
+    n = p.size
+    assert g.size == n and m.size == n and v.size == n
+    po, mo, vo = np.empty(n), np.empty(n), np.empty(n)
+    _load().or_adam_update(n, _ptr(p), _ptr(g), _ptr(m), _ptr(v), float(lr), float(beta1),
+                           float(beta2), float(eps), float(weight_decay), int(step),
+                           float(grad_scale), _ptr(po), _ptr(mo), _ptr(vo))
+    return po, mo, vo

@@ -22,6 +22,12 @@
  *         score matrix) and section 6.2 (the max-subtracted softmax).
  *  Philox-4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
  *         Easy as 1, 2, 3", SC'11 (the pages name no generator).
+ *  Trainer update: [L10] section "Technique 3: mixed precision" (slide p.29)
+ *         and [LS2] section 2.3 (one update over the FP16 parameter/gradient
+ *         workspace, computed in FP32 registers); the update rule is Adam
+ *         (Kingma & Ba, ICLR 2015, Algorithm 1) with decoupled weight decay
+ *         (Loshchilov & Hutter, ICLR 2019), which the pages name only as
+ *         "e.g. Adam".
  */
 #include "ls_oracle.h"
 
@@ -331,4 +337,27 @@ void or_set_num_threads(int n) {
 #else
     (void)n;
 #endif
+}
+
+/* ------------------------------------------------------------------------- */
+/* Trainer update ([LS2] 2.3): Adam with bias correction and decoupled weight */
+/* decay, by the definitions, one element at a time.                          */
+/* ------------------------------------------------------------------------- */
+void or_adam_update(int64_t n, const double* p, const double* g, const double* m,
+                    const double* v, double lr, double beta1, double beta2, double eps,
+                    double weight_decay, int64_t step, double grad_scale, double* p_out,
+                    double* m_out, double* v_out) {
+    const double bc1 = 1.0 - pow(beta1, (double)step); /* bias corrections */
+    const double bc2 = 1.0 - pow(beta2, (double)step);
+    for (int64_t i = 0; i < n; ++i) {
+        const double gi = g[i] * grad_scale;                  /* unscaled gradient */
+        const double mi = beta1 * m[i] + (1.0 - beta1) * gi;  /* first moment */
+        const double vi = beta2 * v[i] + (1.0 - beta2) * gi * gi; /* second moment */
+        const double m_hat = mi / bc1;
+        const double v_hat = vi / bc2;
+        const double decayed = p[i] - lr * weight_decay * p[i]; /* decoupled decay */
+        p_out[i] = decayed - lr * m_hat / (sqrt(v_hat) + eps);
+        m_out[i] = mi;
+        v_out[i] = vi;
+    }
 }

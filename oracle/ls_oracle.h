@@ -71,6 +71,18 @@ void or_softmax_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
                     const double* y, const double* dy, const int32_t* key_len, int causal,
                     double* dx);
 
+/* Trainer update over a flat parameter workspace of n elements: Adam (Kingma &
+ * Ba, ICLR 2015, Algorithm 1) with bias correction at step `step` (>= 1),
+ * decoupled weight decay (Loshchilov & Hutter, ICLR 2019) and the gradient
+ * multiplied by grad_scale first (1 / loss scale):
+ *   g' = g*grad_scale;  m' = b1*m + (1-b1)*g';  v' = b2*v + (1-b2)*g'^2;
+ *   p' = p - lr*wd*p - lr * (m'/(1-b1^t)) / (sqrt(v'/(1-b2^t)) + eps).
+ * Outputs may alias the inputs. */
+void or_adam_update(int64_t n, const double* p, const double* g, const double* m,
+                    const double* v, double lr, double beta1, double beta2, double eps,
+                    double weight_decay, int64_t step, double grad_scale, double* p_out,
+                    double* m_out, double* v_out);
+
 /* OpenMP threads the row loops use, and setting them (n > 0). */
 int or_num_threads(void);
 void or_set_num_threads(int n);

@@ -207,6 +207,27 @@ ls_status ls_softmax_bwd(ls_dtype dtype, void* dx, const void* y, const void* dy
                          int64_t heads, int64_t q_len, int64_t k_len, const int32_t* key_len,
                          int causal, void* stream);
 
+/* Fused trainer update over a flat workspace ("CMU 11-868 L10 (LightSeq)",
+ * technique 3 "mixed precision", slide p.29; "LightSeq2", section 2.3): the
+ * parameters and gradients of a whole model in one contiguous workspace are
+ * updated by one launch, read in the storage dtype, converted to FP32 in
+ * registers and written back -- no FP32 copy of either is kept.  The rule (the
+ * pages say "e.g. Adam") is Adam with bias correction (Kingma & Ba, ICLR 2015)
+ * and decoupled weight decay (Loshchilov & Hutter, ICLR 2019), at step t >= 1:
+ *   g' = grad * grad_scale                  (grad_scale = 1 / loss scale)
+ *   exp_avg'    = beta1 * exp_avg + (1 - beta1) * g'
+ *   exp_avg_sq' = beta2 * exp_avg_sq + (1 - beta2) * g'^2
+ *   param' = param * (1 - lr * weight_decay)
+ *            - lr * (exp_avg' / (1 - beta1^t)) / (sqrt(exp_avg_sq' / (1 - beta2^t)) + eps)
+ * param, grad: [n] in the storage dtype; exp_avg, exp_avg_sq: [n] FP32, all
+ * updated in place (none may overlap another or grad).  Any n >= 0 (n == 0 is
+ * a no-op); 0 <= beta < 1; lr, eps, weight_decay >= 0 and finite; grad_scale
+ * finite.  Every pointer 16-byte aligned. */
+ls_status ls_adam_update(ls_dtype dtype, void* param, const void* grad, float* exp_avg,
+                         float* exp_avg_sq, int64_t n, float lr, float beta1, float beta2,
+                         float eps, float weight_decay, int64_t step, float grad_scale,
+                         void* stream);
+
 #ifdef __cplusplus
 }
 #endif

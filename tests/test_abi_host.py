@@ -43,7 +43,7 @@ def lib():
 
 def test_library_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 14
+    assert len(names) == 15
     assert set(names) == set(ls_ops.EXPORTS)
     out = subprocess.run(["nm", "-D", "--defined-only", lsbuild.LIB], capture_output=True,
                          text=True, check=True).stdout
@@ -177,3 +177,27 @@ def test_error_message_is_per_thread(lib):
     t.join()
     assert seen["msg"] == ""
     assert "out is NULL" in ls_ops.last_error()
+
+
+def test_adam_update_argument_errors(lib):
+    def adam(p=A, g=B, m=C, v=D, n=1000, lr=1e-3, b1=0.9, b2=0.999, eps=1e-8, wd=0.0, step=1,
+             gs=1.0, dtype=F16):
+        return st("ls_adam_update", dtype, p, g, m, v, n, lr, b1, b2, eps, wd, step, gs, S)
+
+    assert adam(n=-1) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(step=0) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(b1=1.0) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(b2=-0.1) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(lr=float("nan")) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(eps=-1e-8) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(wd=float("inf")) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(gs=float("inf")) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(dtype=3) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(m=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert adam(v=D + 4) == ls_ops.LS_ERR_MISALIGNED
+    assert adam(g=A) == ls_ops.LS_ERR_INVALID_ARGUMENT                 # grad is param
+    assert adam(m=A + 512) == ls_ops.LS_ERR_INVALID_ARGUMENT           # exp_avg inside param
+    assert adam(g=C + 16) == ls_ops.LS_ERR_INVALID_ARGUMENT            # grad inside exp_avg
+    assert adam(n=1 << 47) == ls_ops.LS_ERR_UNSUPPORTED_SHAPE
+    assert adam(n=0, p=None, g=None) == ls_ops.LS_OK
+    assert ls_ops.last_error() == ""

@@ -452,5 +452,47 @@ ls_status ls_softmax_bwd(ls_dtype dtype, void* dx, const void* y, const void* dy
                      "ls_softmax_bwd launch");
 }
 
+ls_status ls_adam_update(ls_dtype dtype, void* param, const void* grad, float* exp_avg,
+                         float* exp_avg_sq, int64_t n, float lr, float beta1, float beta2,
+                         float eps, float weight_decay, int64_t step, float grad_scale,
+                         void* stream) {
+    ls::DType dt;
+    LS_TRY(check_dtype(dtype, &dt));
+    if (n < 0) return fail(LS_ERR_INVALID_ARGUMENT, "n = %lld < 0", (long long)n);
+    if (n > (int64_t{1} << 46))
+        return fail(LS_ERR_UNSUPPORTED_SHAPE, "n = %lld is too large", (long long)n);
+    if (step < 1) return fail(LS_ERR_INVALID_ARGUMENT, "step = %lld < 1", (long long)step);
+    if (!(lr >= 0.f) || !isfinite(lr))
+        return fail(LS_ERR_INVALID_ARGUMENT, "lr = %g is not finite and >= 0", (double)lr);
+    if (!(beta1 >= 0.f && beta1 < 1.f) || !(beta2 >= 0.f && beta2 < 1.f))
+        return fail(LS_ERR_INVALID_ARGUMENT, "betas (%g, %g) are not in [0, 1)", (double)beta1,
+                    (double)beta2);
+    if (!(eps >= 0.f) || !isfinite(eps))
+        return fail(LS_ERR_INVALID_ARGUMENT, "eps = %g is not finite and >= 0", (double)eps);
+    if (!(weight_decay >= 0.f) || !isfinite(weight_decay))
+        return fail(LS_ERR_INVALID_ARGUMENT, "weight_decay = %g is not finite and >= 0",
+                    (double)weight_decay);
+    if (!isfinite(grad_scale))
+        return fail(LS_ERR_INVALID_ARGUMENT, "grad_scale = %g is not finite", (double)grad_scale);
+    if (n == 0) return ok();
+    LS_TRY(check_ptr(param, "param", true));
+    LS_TRY(check_ptr(grad, "grad", true));
+    LS_TRY(check_ptr(exp_avg, "exp_avg", true));
+    LS_TRY(check_ptr(exp_avg_sq, "exp_avg_sq", true));
+    const size_t pb = static_cast<size_t>(n) * elem_size(dt);
+    const size_t fb = static_cast<size_t>(n) * sizeof(float);
+    // param, exp_avg and exp_avg_sq are updated in place: none may overlap
+    // another or the gradient.
+    if (param == grad) return fail(LS_ERR_INVALID_ARGUMENT, "param and grad are the same buffer");
+    const Span outs[] = {{"param", param, pb}, {"exp_avg", exp_avg, fb},
+                         {"exp_avg_sq", exp_avg_sq, fb}};
+    const Span ins[] = {{"grad", grad, pb}};
+    LS_TRY(check_overlaps(outs, 3, ins, 1));
+    const ls::AdamHyper h{lr, beta1, beta2, eps, weight_decay, grad_scale, step};
+    return from_cuda(ls::launch_adam(dt, param, grad, exp_avg, exp_avg_sq, n, h,
+                                     static_cast<cudaStream_t>(stream)),
+                     "ls_adam_update launch");
+}
+
 }  // extern "C"
 #pragma GCC visibility pop

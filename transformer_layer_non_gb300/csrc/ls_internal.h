@@ -64,6 +64,14 @@ constexpr int64_t kMaxRowLen = 16384;
 
 // Read and clear the device-side failure flags of one translation unit's
 // kernels (synchronous).
+// Trainer update (Adam with decoupled weight decay) over a flat workspace.
+struct AdamHyper {
+    float lr, beta1, beta2, eps, weight_decay, grad_scale;
+    int64_t step;
+};
+cudaError_t launch_adam(DType dt, void* param, const void* grad, float* m, float* v, int64_t n,
+                        const AdamHyper& h, cudaStream_t s);
+
 cudaError_t softmax_take_device_error(unsigned int* flags);
 cudaError_t dropout_take_device_error(unsigned int* flags);
 cudaError_t layernorm_take_device_error(unsigned int* flags);

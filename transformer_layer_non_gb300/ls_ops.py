@@ -34,7 +34,7 @@ EXPORTS = (
     "ls_bias_dropout_residual_fwd", "ls_bias_dropout_residual_bwd",
     "ls_bias_relu_dropout_fwd", "ls_bias_relu_dropout_bwd",
     "ls_layernorm_fwd", "ls_layernorm_bwd", "ls_softmax_fwd", "ls_softmax_bwd",
-    "ls_layernorm_bwd_noalloc", "ls_check_device_errors",
+    "ls_layernorm_bwd_noalloc", "ls_check_device_errors", "ls_adam_update",
 )
 
 
@@ -67,6 +67,8 @@ _SIGNATURES = {
     "ls_layernorm_bwd_noalloc": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
     "ls_softmax_fwd": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
+    "ls_adam_update": (_INT, [_INT, _P, _P, _P, _P, _I64, _F32, _F32, _F32, _F32, _F32, _I64,
+                              _F32, _P]),
 }
 
 
@@ -240,3 +242,18 @@ def ls_softmax_bwd(dx, y, dy, key_len=None, causal: bool = False, stream=None):
     b, h, lq, lk = y.shape
     _check(load().ls_softmax_bwd(_dtype_code(y), _ptr(dx), _ptr(y), _ptr(dy), b, h, lq, lk,
                                  _ptr(key_len), int(bool(causal)), _stream(stream)))
+
+
+def ls_adam_update(param, grad, exp_avg, exp_avg_sq, lr: float, beta1: float, beta2: float,
+                   eps: float, weight_decay: float, step: int, grad_scale: float = 1.0,
+                   stream=None):
+    """One trainer update of a flat workspace, in place: param and grad in the
+    storage dtype, exp_avg and exp_avg_sq FP32, all with param.numel() elements."""
+    n = param.numel()
+    for t in (grad, exp_avg, exp_avg_sq):
+        if t.numel() != n:
+            raise ValueError("param, grad, exp_avg and exp_avg_sq must have the same size")
+    _check(load().ls_adam_update(_dtype_code(param), _ptr(param), _ptr(grad), _ptr(exp_avg),
+                                 _ptr(exp_avg_sq), n, lr, beta1, beta2, eps, weight_decay,
+                                 int(step), grad_scale, _stream(stream)))
+

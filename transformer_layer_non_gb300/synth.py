@@ -119,3 +119,40 @@ def sweep_inputs(k_len: int, seed: int = 0, elements: int = SWEEP_ELEMENTS):
     dy = normal(seed, f"sweep{k_len}/scores_dy", shape, 0.0, 1.0, "f16")
     kl = key_lengths(seed, f"sweep{k_len}/key_len", rows, 1, k_len)
     return x, dy, kl
+
+
+# The trainer update's workload: the parameters of a BERT-base encoder (12
+# layers of H = 768, FFN = 3072, with token/position/segment embeddings, the
+# embedding LayerNorm and the pooler), 109,482,240 values in one flat
+# workspace.
+def bert_base_param_count(layers: int = 12, hidden: int = 768, ffn: int = 3072,
+                          vocab: int = 30522, positions: int = 512, segments: int = 2) -> int:
+    h, f = hidden, ffn
+    per_layer = 4 * h * h + 4 * h + 2 * h * f + f + h + 4 * h  # QKV+out, FFN, two LayerNorms
+    embeddings = (vocab + positions + segments) * h + 2 * h
+    pooler = h * h + h
+    return layers * per_layer + embeddings + pooler
+
+
+TRAINER_N = bert_base_param_count()
+
+
+def trainer_state(n: int, seed: int = 0, dtype: str = "f16", device="cpu"):
+    """Seeded trainer state of n elements, drawn with torch on `device`:
+    parameters N(0, 0.02) and gradients N(0, 0.01) in the storage dtype, first
+    moments N(0, 1e-3) and second moments N(0, 1e-2)^2 in FP32 (as after a few
+    steps).  Returns (param, grad, exp_avg, exp_avg_sq)."""
+    import torch
+
+    g = torch.Generator(device=device)
+    g.manual_seed(zlib.crc32(f"trainer/{seed}".encode()))
+    dt = {"f16": torch.float16, "f32": torch.float32}[dtype]
+
+    def draw(std):
+        return torch.randn(n, generator=g, device=device, dtype=torch.float32) * std
+
+    p = draw(0.02).to(dt)
+    gr = draw(0.01).to(dt)
+    m = draw(1e-3)
+    v = draw(1e-2) ** 2
+    return p, gr, m, v

@@ -66,6 +66,8 @@ def _load():
         "or_num_threads": (cint, []),
         "or_set_num_threads": (None, [cint]),
         "or_adam_update": (None, [i64, P, P, P, P, f64, f64, f64, f64, f64, i64, f64, P, P, P]),
+        "or_bias_reshape_qkv_fwd": (None, [i64, i64, i64, i64, P, P, P]),
+        "or_bias_reshape_qkv_bwd": (None, [i64, i64, i64, i64, P, P, P]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(lib, name)
@@ -221,3 +223,23 @@ def adam_update(p, g, m, v, lr, beta1, beta2, eps, weight_decay, step, grad_scal
                            float(beta2), float(eps), float(weight_decay), int(step),
                            float(grad_scale), _ptr(po), _ptr(mo), _ptr(vo))
     return po, mo, vo
+
+
+def bias_reshape_qkv_fwd(qkv, bias, batch, seq, heads, d):
+    """qkv [batch*seq, 3*heads*d] + bias -> [3, batch, heads, seq, d] (float64)."""
+    x, b = _f64(qkv), _f64(bias)
+    assert x.size == batch * seq * 3 * heads * d and b.size == 3 * heads * d
+    out = np.empty((3, batch, heads, seq, d))
+    _load().or_bias_reshape_qkv_fwd(batch, seq, heads, d, _ptr(x), _ptr(b), _ptr(out))
+    return out
+
+
+def bias_reshape_qkv_bwd(dout, batch, seq, heads, d):
+    """dout [3, batch, heads, seq, d] -> (dqkv [batch*seq, 3*heads*d], dbias [3*heads*d])."""
+    g = _f64(dout)
+    assert g.size == 3 * batch * heads * seq * d
+    dqkv = np.empty((batch * seq, 3 * heads * d))
+    dbias = np.empty(3 * heads * d)
+    _load().or_bias_reshape_qkv_bwd(batch, seq, heads, d, _ptr(g), _ptr(dqkv), _ptr(dbias))
+    return dqkv, dbias
+

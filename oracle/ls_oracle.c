@@ -22,6 +22,9 @@
  *         score matrix) and section 6.2 (the max-subtracted softmax).
  *  Philox-4x32-10: Salmon, Moraes, Dror, Shaw, "Parallel Random Numbers: As
  *         Easy as 1, 2, 3", SC'11 (the pages name no generator).
+ *  Bias + reshape of Q, K, V: [L10] section "Technique 1: kernel fusion"
+ *         (slide p.12 lists "add bias + reshape Q, K, V" as one fused
+ *         elementwise kernel next to the QKV projection GEMM).
  *  Trainer update: [L10] section "Technique 3: mixed precision" (slide p.29)
  *         and [LS2] section 2.3 (one update over the FP16 parameter/gradient
  *         workspace, computed in FP32 registers); the update rule is Adam
@@ -361,3 +364,39 @@ void or_adam_update(int64_t n, const double* p, const double* g, const double* m
         v_out[i] = vi;
     }
 }
+
+/* ------------------------------------------------------------------------- */
+/* Bias + reshape Q, K, V ([L10] technique 1, slide p.12).  The fused QKV     */
+/* projection writes one row of 3*H values per token (row = b*seq + l), the   */
+/* H = heads*d columns of Q, then of K, then of V, each split into heads of d */
+/* columns.  The kernel adds the bias and moves every value to the head-major */
+/* layout [3, batch, heads, seq, d] that the attention GEMMs read.            */
+/* ------------------------------------------------------------------------- */
+static int64_t qkv_out_index(int64_t batch, int64_t seq, int64_t heads, int64_t d, int64_t row,
+                             int64_t c) {
+    const int64_t H = heads * d;
+    const int64_t s = c / H, h = (c % H) / d, j = c % d; /* which of Q/K/V, head, lane */
+    const int64_t b = row / seq, l = row % seq;
+    return (((s * batch + b) * heads + h) * seq + l) * d + j;
+}
+
+void or_bias_reshape_qkv_fwd(int64_t batch, int64_t seq, int64_t heads, int64_t d,
+                             const double* qkv, const double* bias, double* out) {
+    const int64_t rows = batch * seq, cols = 3 * heads * d;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c)
+            out[qkv_out_index(batch, seq, heads, d, r, c)] = qkv[r * cols + c] + bias[c];
+}
+
+void or_bias_reshape_qkv_bwd(int64_t batch, int64_t seq, int64_t heads, int64_t d,
+                             const double* dout, double* dqkv, double* dbias) {
+    const int64_t rows = batch * seq, cols = 3 * heads * d;
+    for (int64_t c = 0; c < cols; ++c) dbias[c] = 0.0;
+    for (int64_t r = 0; r < rows; ++r)
+        for (int64_t c = 0; c < cols; ++c) {
+            const double g = dout[qkv_out_index(batch, seq, heads, d, r, c)];
+            dqkv[r * cols + c] = g;
+            dbias[c] += g; /* rows added in order */
+        }
+}
+

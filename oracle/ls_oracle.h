@@ -71,6 +71,17 @@ void or_softmax_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
                     const double* y, const double* dy, const int32_t* key_len, int causal,
                     double* dx);
 
+/* Bias + reshape of the fused QKV projection output: qkv [batch*seq, 3*heads*d]
+ * (per row: Q, K, V, each heads x d) plus bias [3*heads*d] into
+ * out [3, batch, heads, seq, d]:
+ *   out[s, b, h, l, j] = qkv[b*seq + l, s*H + h*d + j] + bias[s*H + h*d + j],  H = heads*d.
+ * The backward moves dout [3, batch, heads, seq, d] back to dqkv
+ * [batch*seq, 3*heads*d] and sums it over rows into dbias [3*heads*d]. */
+void or_bias_reshape_qkv_fwd(int64_t batch, int64_t seq, int64_t heads, int64_t d,
+                             const double* qkv, const double* bias, double* out);
+void or_bias_reshape_qkv_bwd(int64_t batch, int64_t seq, int64_t heads, int64_t d,
+                             const double* dout, double* dqkv, double* dbias);
+
 /* Trainer update over a flat parameter workspace of n elements: Adam (Kingma &
  * Ba, ICLR 2015, Algorithm 1) with bias correction at step `step` (>= 1),
  * decoupled weight decay (Loshchilov & Hutter, ICLR 2019) and the gradient

@@ -207,6 +207,26 @@ ls_status ls_softmax_bwd(ls_dtype dtype, void* dx, const void* y, const void* dy
                          int64_t heads, int64_t q_len, int64_t k_len, const int32_t* key_len,
                          int causal, void* stream);
 
+/* Bias + reshape of Q, K, V ("CMU 11-868 L10 (LightSeq)", technique 1,
+ * slide p.12: one fused elementwise kernel after the QKV projection GEMM).
+ * qkv: [batch*seq, 3*H] row-major, H = heads*head_dim, row b*seq + l holding
+ * Q, K, V in that order, each split into heads of head_dim; bias: [3*H].
+ *   q_k_v[s, b, h, l, j] = qkv[b*seq + l, s*H + h*head_dim + j] + bias[s*H + h*head_dim + j]
+ * q_k_v: [3, batch, heads, seq, head_dim] (Q at offset 0, K, V after it).
+ * head_dim must be a multiple of 8.  q_k_v may not overlap qkv or bias.  No
+ * 1/sqrt(head_dim) scaling (the score GEMM applies it). */
+ls_status ls_bias_reshape_qkv_fwd(ls_dtype dtype, void* q_k_v, const void* qkv, const void* bias,
+                                  int64_t batch, int64_t seq, int64_t heads, int64_t head_dim,
+                                  void* stream);
+
+/* Backward of the above: dqkv[b*seq + l, s*H + h*head_dim + j] = dq_k_v[s, b, h, l, j];
+ * dbias[c] = sum over rows of dqkv[., c] (deterministic; workspace of at least
+ * ls_colreduce_workspace_bytes(batch*seq, 3*H) bytes when dbias is not NULL).
+ * dqkv may not overlap dq_k_v. */
+ls_status ls_bias_reshape_qkv_bwd(ls_dtype dtype, void* dqkv, void* dbias, const void* dq_k_v,
+                                  int64_t batch, int64_t seq, int64_t heads, int64_t head_dim,
+                                  void* workspace, size_t workspace_bytes, void* stream);
+
 /* Fused trainer update over a flat workspace ("CMU 11-868 L10 (LightSeq)",
  * technique 3 "mixed precision", slide p.29; "LightSeq2", section 2.3): the
  * parameters and gradients of a whole model in one contiguous workspace are

@@ -43,7 +43,7 @@ def lib():
 
 def test_library_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 15
+    assert len(names) == 17
     assert set(names) == set(ls_ops.EXPORTS)
     out = subprocess.run(["nm", "-D", "--defined-only", lsbuild.LIB], capture_output=True,
                          text=True, check=True).stdout
@@ -201,3 +201,25 @@ def test_adam_update_argument_errors(lib):
     assert adam(n=1 << 47) == ls_ops.LS_ERR_UNSUPPORTED_SHAPE
     assert adam(n=0, p=None, g=None) == ls_ops.LS_OK
     assert ls_ops.last_error() == ""
+
+
+def test_bias_reshape_qkv_argument_errors(lib):
+    def fwd(out=A, qkv=B, bias=C, b=2, s=16, h=4, d=64, dtype=F16):
+        return st("ls_bias_reshape_qkv_fwd", dtype, out, qkv, bias, b, s, h, d, S)
+
+    def bwd(dqkv=A, db=B, dout=C, b=2, s=16, h=4, d=64, ws=D, wsb=1 << 20):
+        return st("ls_bias_reshape_qkv_bwd", F16, dqkv, db, dout, b, s, h, d, ws, wsb, S)
+
+    assert fwd(d=60) == ls_ops.LS_ERR_MISALIGNED
+    assert fwd(d=0) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(b=-1) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(bias=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(out=B) == ls_ops.LS_ERR_INVALID_ARGUMENT          # no in-place reshape
+    assert fwd(qkv=B + 8) == ls_ops.LS_ERR_MISALIGNED
+    assert fwd(h=1 << 20) == ls_ops.LS_ERR_UNSUPPORTED_SHAPE
+    assert fwd(b=0, out=None) == ls_ops.LS_OK
+    # 32 rows of 3 x 4 x 64 columns -> one 128-row partial row of 768 FP32 sums.
+    assert bwd(wsb=768 * 4 - 4) == ls_ops.LS_ERR_WORKSPACE_TOO_SMALL
+    assert bwd(ws=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert bwd(dout=A) == ls_ops.LS_ERR_INVALID_ARGUMENT         # no in-place reshape
+    assert ls_ops.colreduce_workspace_bytes(32, 768) >= 768 * 4

@@ -494,5 +494,85 @@ ls_status ls_adam_update(ls_dtype dtype, void* param, const void* grad, float* e
                      "ls_adam_update launch");
 }
 
+static ls_status qkv_common(ls_dtype dtype, int64_t batch, int64_t seq, int64_t heads,
+                            int64_t head_dim, ls::DType* dt, int64_t* rows, int64_t* cols) {
+    LS_TRY(check_dtype(dtype, dt));
+    if (batch < 0 || seq < 0 || heads < 0)
+        return fail(LS_ERR_INVALID_ARGUMENT, "batch, seq and heads must be >= 0");
+    if (head_dim <= 0) return fail(LS_ERR_INVALID_ARGUMENT, "head_dim = %lld <= 0", (long long)head_dim);
+    if (head_dim % 8 != 0)
+        return fail(LS_ERR_MISALIGNED, "head_dim = %lld is not a multiple of 8", (long long)head_dim);
+    if (seq > INT32_MAX || heads > INT32_MAX || heads * head_dim > kMaxDropoutCols)
+        return fail(LS_ERR_UNSUPPORTED_SHAPE, "seq = %lld, heads x head_dim = %lld x %lld too large",
+                    (long long)seq, (long long)heads, (long long)head_dim);
+    *rows = batch * seq;
+    *cols = 3 * heads * head_dim;
+    if (*cols == 0) *cols = 8;  // heads == 0: nothing to move; keep the shape checks happy
+    return check_shape(*rows, *cols, 3 * kMaxDropoutCols);
+}
+
+ls_status ls_bias_reshape_qkv_fwd(ls_dtype dtype, void* q_k_v, const void* qkv, const void* bias,
+                                  int64_t batch, int64_t seq, int64_t heads, int64_t head_dim,
+                                  void* stream) {
+    ls::DType dt;
+    int64_t rows, cols;
+    LS_TRY(qkv_common(dtype, batch, seq, heads, head_dim, &dt, &rows, &cols));
+    if (rows == 0 || heads == 0) return ok();
+    LS_TRY(check_ptr(q_k_v, "q_k_v", true));
+    LS_TRY(check_ptr(qkv, "qkv", true));
+    LS_TRY(check_ptr(bias, "bias", true));
+    const size_t nb = static_cast<size_t>(rows * cols) * elem_size(dt);
+    const size_t bb = static_cast<size_t>(cols) * elem_size(dt);
+    // The reshape moves every element: the output may not overlap an input at all.
+    const Span out{"q_k_v", q_k_v, nb}, in0{"qkv", qkv, nb}, in1{"bias", bias, bb};
+    if (overlaps(out, in0) || overlaps(out, in1))
+        return fail(LS_ERR_INVALID_ARGUMENT, "q_k_v overlaps qkv or bias (no in-place reshape)");
+    return from_cuda(ls::launch_qkv_fwd(dt, q_k_v, qkv, bias, batch, seq, heads, head_dim,
+                                        static_cast<cudaStream_t>(stream)),
+                     "ls_bias_reshape_qkv_fwd launch");
+}
+
+ls_status ls_bias_reshape_qkv_bwd(ls_dtype dtype, void* dqkv, void* dbias, const void* dq_k_v,
+                                  int64_t batch, int64_t seq, int64_t heads, int64_t head_dim,
+                                  void* workspace, size_t workspace_bytes, void* stream) {
+    ls::DType dt;
+    int64_t rows, cols;
+    LS_TRY(qkv_common(dtype, batch, seq, heads, head_dim, &dt, &rows, &cols));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const size_t bb = static_cast<size_t>(cols) * elem_size(dt);
+    if (rows == 0 || heads == 0) {
+        if (dbias && heads > 0) {
+            LS_TRY(check_ptr(dbias, "dbias", true));
+            return from_cuda(cudaMemsetAsync(dbias, 0, bb, s), "ls_bias_reshape_qkv_bwd");
+        }
+        return ok();
+    }
+    LS_TRY(check_ptr(dqkv, "dqkv", true));
+    LS_TRY(check_ptr(dbias, "dbias", false));
+    LS_TRY(check_ptr(dq_k_v, "dq_k_v", true));
+    const ls::ColReducePlan plan = ls::dropout_bwd_plan(rows, cols);
+    if (dbias) {
+        LS_TRY(check_ptr(workspace, "workspace", true));
+        if (workspace_bytes < plan.bytes())
+            return fail(LS_ERR_WORKSPACE_TOO_SMALL,
+                        "ls_bias_reshape_qkv_bwd: workspace of %zu bytes, need %zu",
+                        workspace_bytes, plan.bytes());
+    }
+    const size_t nb = static_cast<size_t>(rows * cols) * elem_size(dt);
+    const Span outs[] = {{"dqkv", dqkv, nb}, {"dbias", dbias, bb},
+                         {"workspace", dbias ? workspace : nullptr, plan.bytes()}};
+    const Span in{"dq_k_v", dq_k_v, nb};
+    for (const Span& o : outs)
+        if (overlaps(o, in))
+            return fail(LS_ERR_INVALID_ARGUMENT, "%s overlaps dq_k_v (no in-place reshape)",
+                        o.name);
+    LS_TRY(check_overlaps(outs, 3, nullptr, 0));
+    float* partial = dbias ? static_cast<float*>(workspace) : nullptr;
+    cudaError_t e = ls::launch_qkv_bwd(dt, dqkv, partial, dq_k_v, batch, seq, heads, head_dim, s);
+    if (e == cudaSuccess && dbias)
+        e = ls::launch_colreduce(dt, dbias, nullptr, cols, partial, plan.parts, cols, s);
+    return from_cuda(e, "ls_bias_reshape_qkv_bwd launch");
+}
+
 }  // extern "C"
 #pragma GCC visibility pop

@@ -64,6 +64,15 @@ constexpr int64_t kMaxRowLen = 16384;
 
 // Read and clear the device-side failure flags of one translation unit's
 // kernels (synchronous).
+// Bias + reshape of Q, K, V: [batch*seq, 3*heads*d] (+ bias) <-> [3, batch,
+// heads, seq, d].  The backward writes one FP32 partial row of the bias
+// gradient per 128 rows (dropout_bwd_plan(batch*seq, 3*heads*d)) when partial
+// is not null.
+cudaError_t launch_qkv_fwd(DType dt, void* out, const void* qkv, const void* bias, int64_t batch,
+                           int64_t seq, int64_t heads, int64_t d, cudaStream_t s);
+cudaError_t launch_qkv_bwd(DType dt, void* dqkv, float* partial, const void* dout, int64_t batch,
+                           int64_t seq, int64_t heads, int64_t d, cudaStream_t s);
+
 // Trainer update (Adam with decoupled weight decay) over a flat workspace.
 struct AdamHyper {
     float lr, beta1, beta2, eps, weight_decay, grad_scale;

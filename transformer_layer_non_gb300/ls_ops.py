@@ -35,6 +35,7 @@ EXPORTS = (
     "ls_bias_relu_dropout_fwd", "ls_bias_relu_dropout_bwd",
     "ls_layernorm_fwd", "ls_layernorm_bwd", "ls_softmax_fwd", "ls_softmax_bwd",
     "ls_layernorm_bwd_noalloc", "ls_check_device_errors", "ls_adam_update",
+    "ls_bias_reshape_qkv_fwd", "ls_bias_reshape_qkv_bwd",
 )
 
 
@@ -67,6 +68,8 @@ _SIGNATURES = {
     "ls_layernorm_bwd_noalloc": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
     "ls_softmax_fwd": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
+    "ls_bias_reshape_qkv_fwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
+    "ls_bias_reshape_qkv_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _SZ, _P]),
     "ls_adam_update": (_INT, [_INT, _P, _P, _P, _P, _I64, _F32, _F32, _F32, _F32, _F32, _I64,
                               _F32, _P]),
 }
@@ -256,4 +259,21 @@ def ls_adam_update(param, grad, exp_avg, exp_avg_sq, lr: float, beta1: float, be
     _check(load().ls_adam_update(_dtype_code(param), _ptr(param), _ptr(grad), _ptr(exp_avg),
                                  _ptr(exp_avg_sq), n, lr, beta1, beta2, eps, weight_decay,
                                  int(step), grad_scale, _stream(stream)))
+
+
+def ls_bias_reshape_qkv_fwd(q_k_v, qkv, bias, batch: int, seq: int, heads: int,
+                            stream=None):
+    """qkv [batch*seq, 3*H] + bias [3*H] -> q_k_v [3, batch, heads, seq, H/heads]."""
+    d = q_k_v.shape[-1]
+    _check(load().ls_bias_reshape_qkv_fwd(_dtype_code(qkv), _ptr(q_k_v), _ptr(qkv), _ptr(bias),
+                                          batch, seq, heads, d, _stream(stream)))
+
+
+def ls_bias_reshape_qkv_bwd(dqkv, dbias, dq_k_v, batch: int, seq: int, heads: int,
+                            workspace=None, stream=None):
+    """dq_k_v [3, batch, heads, seq, d] -> dqkv [batch*seq, 3*H] and dbias [3*H]."""
+    d = dq_k_v.shape[-1]
+    _check(load().ls_bias_reshape_qkv_bwd(_dtype_code(dq_k_v), _ptr(dqkv), _ptr(dbias),
+                                          _ptr(dq_k_v), batch, seq, heads, d, _ptr(workspace),
+                                          _nbytes(workspace), _stream(stream)))
 

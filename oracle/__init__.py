@@ -67,6 +67,8 @@ def _load():
         "or_set_num_threads": (None, [cint]),
         "or_adam_update": (None, [i64, P, P, P, P, f64, f64, f64, f64, f64, i64, f64, P, P, P]),
         "or_bias_reshape_qkv_fwd": (None, [i64, i64, i64, i64, P, P, P]),
+        "or_softmax_dropout_fwd": (None, [i64, i64, i64, i64, P, P, cint, f32, u64, u64, P, P, P]),
+        "or_softmax_dropout_bwd": (None, [i64, i64, i64, i64, P, P, P, P, cint, f32, P]),
         "or_bias_reshape_qkv_bwd": (None, [i64, i64, i64, i64, P, P, P]),
     }
     for name, (res, args) in sig.items():
@@ -242,4 +244,27 @@ def bias_reshape_qkv_bwd(dout, batch, seq, heads, d):
     dbias = np.empty(3 * heads * d)
     _load().or_bias_reshape_qkv_bwd(batch, seq, heads, d, _ptr(g), _ptr(dqkv), _ptr(dbias))
     return dqkv, dbias
+
+
+def softmax_dropout_fwd(x, key_len, causal, p, seed, offset):
+    """Returns (y, y_drop, mask_words) for scores x [batch, heads, q_len, k_len]."""
+    xx = _f64(x)
+    b, h, lq, lk = xx.shape
+    kl = _key_len(key_len)
+    y, yd = np.empty_like(xx), np.empty_like(xx)
+    w = np.zeros(mask_words(xx.size), dtype=np.uint32)
+    _load().or_softmax_dropout_fwd(b, h, lq, lk, _ptr(xx), _ptr(kl), int(bool(causal)),
+                                   float(p), int(seed), int(offset), _ptr(y), _ptr(yd), _ptr(w))
+    return y, yd, w
+
+
+def softmax_dropout_bwd(y, dy_drop, mask, key_len, causal, p):
+    yy, dd = _f64(y), _f64(dy_drop)
+    b, h, lq, lk = yy.shape
+    kl = _key_len(key_len)
+    w = np.ascontiguousarray(np.asarray(mask, dtype=np.uint32))
+    dx = np.empty_like(yy)
+    _load().or_softmax_dropout_bwd(b, h, lq, lk, _ptr(yy), _ptr(dd), _ptr(w), _ptr(kl),
+                                   int(bool(causal)), float(p), _ptr(dx))
+    return dx
 

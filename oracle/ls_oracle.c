@@ -400,3 +400,53 @@ void or_bias_reshape_qkv_bwd(int64_t batch, int64_t seq, int64_t heads, int64_t 
         }
 }
 
+/* ------------------------------------------------------------------------- */
+/* Softmax with dropout on the probabilities ([L10] technique 1: the dropout  */
+/* after the attention softmax joins the softmax kernel).  bit = keep on      */
+/* valid entries, 0 on masked ones; y_drop = bit * y / (1 - p).               */
+/* ------------------------------------------------------------------------- */
+void or_softmax_dropout_fwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
+                            const double* x, const int32_t* key_len, int causal, float p,
+                            uint64_t seed, uint64_t offset, double* y, double* y_drop,
+                            uint32_t* mask_words) {
+    or_softmax_fwd(batch, heads, q_len, k_len, x, key_len, causal, y);
+    const uint32_t thr = or_dropout_threshold(p);
+    const double scale = 1.0 / (1.0 - (double)p);
+    const int64_t nrows = batch * heads * q_len;
+    memset(mask_words, 0, (size_t)mask_word_count(nrows * k_len) * sizeof(uint32_t));
+    for (int64_t row = 0; row < nrows; ++row) {
+        const int64_t v = valid_len(row / (heads * q_len), row % q_len, q_len, k_len, key_len,
+                                    causal);
+        for (int64_t j = 0; j < k_len; ++j) {
+            const int64_t i = row * k_len + j;
+            const int bit = j < v && keep_bit(seed, offset, (uint64_t)i, thr);
+            if (bit) mask_words[i >> 5] |= 1u << (i & 31);
+            y_drop[i] = bit ? y[i] * scale : 0.0;
+        }
+    }
+}
+
+/* g = bit * dy_drop / (1 - p);  dx = y * (g - <y, g>) on valid keys, 0 on masked. */
+void or_softmax_dropout_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
+                            const double* y, const double* dy_drop, const uint32_t* mask_words,
+                            const int32_t* key_len, int causal, float p, double* dx) {
+    const double scale = 1.0 / (1.0 - (double)p);
+    const int64_t nrows = batch * heads * q_len;
+    for (int64_t row = 0; row < nrows; ++row) {
+        const int64_t v = valid_len(row / (heads * q_len), row % q_len, q_len, k_len, key_len,
+                                    causal);
+        const double* yr = y + row * k_len;
+        double dot = 0.0;
+        for (int64_t j = 0; j < v; ++j) {
+            const int64_t i = row * k_len + j;
+            const double g = get_bit(mask_words, i) ? dy_drop[i] * scale : 0.0;
+            dot += yr[j] * g;
+        }
+        for (int64_t j = 0; j < k_len; ++j) {
+            const int64_t i = row * k_len + j;
+            const double g = get_bit(mask_words, i) ? dy_drop[i] * scale : 0.0;
+            dx[i] = (j < v) ? yr[j] * (g - dot) : 0.0;
+        }
+    }
+}
+

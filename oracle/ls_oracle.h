@@ -71,6 +71,19 @@ void or_softmax_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
                     const double* y, const double* dy, const int32_t* key_len, int causal,
                     double* dx);
 
+/* Softmax (as or_softmax_fwd) with dropout on the probabilities: bit(i) =
+ * keep(i) on valid entries and 0 on masked ones (mask_words: ceil(n/32)
+ * words), y_drop = bit * y / (1 - p).  The backward takes the bits and the
+ * gradient of y_drop: g = bit * dy_drop / (1 - p), dx = y * (g - <y, g>) on
+ * valid entries, 0 on masked ones. */
+void or_softmax_dropout_fwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
+                            const double* x, const int32_t* key_len, int causal, float p,
+                            uint64_t seed, uint64_t offset, double* y, double* y_drop,
+                            uint32_t* mask_words);
+void or_softmax_dropout_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t k_len,
+                            const double* y, const double* dy_drop, const uint32_t* mask_words,
+                            const int32_t* key_len, int causal, float p, double* dx);
+
 /* Bias + reshape of the fused QKV projection output: qkv [batch*seq, 3*heads*d]
  * (per row: Q, K, V, each heads x d) plus bias [3*heads*d] into
  * out [3, batch, heads, seq, d]:

@@ -207,6 +207,27 @@ ls_status ls_softmax_bwd(ls_dtype dtype, void* dx, const void* y, const void* dy
                          int64_t heads, int64_t q_len, int64_t k_len, const int32_t* key_len,
                          int causal, void* stream);
 
+/* Softmax fused with dropout on the attention probabilities ("CMU 11-868 L10
+ * (LightSeq)", technique 1: the elementwise step after the softmax reduce
+ * kernel joins it).  Same mask arguments and softmax y as ls_softmax_fwd, and
+ *   bit(i) = keep(i) on valid entries, 0 on masked ones   (i = flat index of
+ *            [batch, heads, q_len, k_len]; keep as for the other dropouts)
+ *   y_drop = bit(i) * y / (1 - p)
+ * y (needed by the backward), y_drop (fed to the next GEMM) and mask_bits
+ * (ceil(n/32) words) are written.  None may overlap x or another output. */
+ls_status ls_softmax_dropout_fwd(ls_dtype dtype, void* y, void* y_drop, uint32_t* mask_bits,
+                                 const void* x, int64_t batch, int64_t heads, int64_t q_len,
+                                 int64_t k_len, const int32_t* key_len, int causal, float p,
+                                 uint64_t seed, uint64_t offset, void* stream);
+
+/* Backward of the above: g = bit(i) * dy_drop / (1 - p), then
+ *   dx = y * (g - sum_valid(y * g)) on valid entries, 0 on masked ones.
+ * dx may be dy_drop. */
+ls_status ls_softmax_dropout_bwd(ls_dtype dtype, void* dx, const void* y, const void* dy_drop,
+                                 const uint32_t* mask_bits, int64_t batch, int64_t heads,
+                                 int64_t q_len, int64_t k_len, const int32_t* key_len, int causal,
+                                 float p, void* stream);
+
 /* Bias + reshape of Q, K, V ("CMU 11-868 L10 (LightSeq)", technique 1,
  * slide p.12: one fused elementwise kernel after the QKV projection GEMM).
  * qkv: [batch*seq, 3*H] row-major, H = heads*head_dim, row b*seq + l holding

@@ -43,7 +43,7 @@ def lib():
 
 def test_library_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 17
+    assert len(names) == 19
     assert set(names) == set(ls_ops.EXPORTS)
     out = subprocess.run(["nm", "-D", "--defined-only", lsbuild.LIB], capture_output=True,
                          text=True, check=True).stdout
@@ -223,3 +223,23 @@ def test_bias_reshape_qkv_argument_errors(lib):
     assert bwd(ws=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
     assert bwd(dout=A) == ls_ops.LS_ERR_INVALID_ARGUMENT         # no in-place reshape
     assert ls_ops.colreduce_workspace_bytes(32, 768) >= 768 * 4
+
+
+def test_softmax_dropout_argument_errors(lib):
+    def fwd(y=A, yd=B, m=C, x=D, b=2, h=2, lq=4, lk=64, kl=None, p=0.1):
+        return st("ls_softmax_dropout_fwd", F16, y, yd, m, x, b, h, lq, lk, kl, 0, p, 0, 0, S)
+
+    def bwd(dx=A, y=B, dyd=C, m=D, b=2, h=2, lq=4, lk=64, p=0.1):
+        return st("ls_softmax_dropout_bwd", F16, dx, y, dyd, m, b, h, lq, lk, None, 0, p, S)
+
+    assert fwd(p=1.0) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(m=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(yd=A) == ls_ops.LS_ERR_INVALID_ARGUMENT          # y_drop is y
+    assert fwd(m=D + 64) == ls_ops.LS_ERR_INVALID_ARGUMENT      # mask inside x
+    assert fwd(lk=60) == ls_ops.LS_ERR_MISALIGNED
+    assert fwd(kl=E + 2) == ls_ops.LS_ERR_MISALIGNED
+    assert fwd(b=0, y=None) == ls_ops.LS_OK
+    assert bwd(p=-0.5) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert bwd(m=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert bwd(dx=B + 16) == ls_ops.LS_ERR_INVALID_ARGUMENT     # dx partly over y
+    assert bwd(lq=0) == ls_ops.LS_OK

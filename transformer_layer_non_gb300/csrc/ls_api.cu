@@ -574,5 +574,61 @@ ls_status ls_bias_reshape_qkv_bwd(ls_dtype dtype, void* dqkv, void* dbias, const
     return from_cuda(e, "ls_bias_reshape_qkv_bwd launch");
 }
 
+ls_status ls_softmax_dropout_fwd(ls_dtype dtype, void* y, void* y_drop, uint32_t* mask_bits,
+                                 const void* x, int64_t batch, int64_t heads, int64_t q_len,
+                                 int64_t k_len, const int32_t* key_len, int causal, float p,
+                                 uint64_t seed, uint64_t offset, void* stream) {
+    ls::DType dt;
+    int64_t nrows;
+    LS_TRY(softmax_common("ls_softmax_dropout_fwd", dtype, batch, heads, q_len, k_len, key_len,
+                          &dt, &nrows));
+    ls::DropoutRng rng;
+    LS_TRY(check_p(p, &rng, seed, offset));
+    if (nrows == 0) return ok();
+    LS_TRY(check_ptr(y, "y", true));
+    LS_TRY(check_ptr(y_drop, "y_drop", true));
+    LS_TRY(check_ptr(mask_bits, "mask_bits", true));
+    LS_TRY(check_ptr(x, "x", true));
+    const size_t nb = static_cast<size_t>(nrows * k_len) * elem_size(dt);
+    const Span outs[] = {{"y", y, nb}, {"y_drop", y_drop, nb},
+                         {"mask_bits", mask_bits, mask_bytes(nrows, k_len)}};
+    const Span ins[] = {{"x", x, nb}, {"key_len", key_len, static_cast<size_t>(batch) * 4}};
+    LS_TRY(check_overlaps(outs, 3, ins, 2));
+    const ls::SoftmaxShape sh{batch, heads, q_len, k_len, key_len, causal ? 1 : 0};
+    return from_cuda(ls::launch_softmax_dropout_fwd(dt, y, y_drop,
+                                                    reinterpret_cast<uint8_t*>(mask_bits), x, sh,
+                                                    rng, static_cast<cudaStream_t>(stream)),
+                     "ls_softmax_dropout_fwd launch");
+}
+
+ls_status ls_softmax_dropout_bwd(ls_dtype dtype, void* dx, const void* y, const void* dy_drop,
+                                 const uint32_t* mask_bits, int64_t batch, int64_t heads,
+                                 int64_t q_len, int64_t k_len, const int32_t* key_len, int causal,
+                                 float p, void* stream) {
+    ls::DType dt;
+    int64_t nrows;
+    LS_TRY(softmax_common("ls_softmax_dropout_bwd", dtype, batch, heads, q_len, k_len, key_len,
+                          &dt, &nrows));
+    ls::DropoutRng rng;
+    LS_TRY(check_p(p, &rng, 0, 0));
+    if (nrows == 0) return ok();
+    LS_TRY(check_ptr(dx, "dx", true));
+    LS_TRY(check_ptr(y, "y", true));
+    LS_TRY(check_ptr(dy_drop, "dy_drop", true));
+    LS_TRY(check_ptr(mask_bits, "mask_bits", true));
+    const size_t nb = static_cast<size_t>(nrows * k_len) * elem_size(dt);
+    const Span outs[] = {{"dx", dx, nb}};
+    const Span ins[] = {{"y", y, nb}, {"dy_drop", dy_drop, nb},
+                        {"mask_bits", mask_bits, mask_bytes(nrows, k_len)},
+                        {"key_len", key_len, static_cast<size_t>(batch) * 4}};
+    LS_TRY(check_overlaps(outs, 1, ins, 4));
+    const ls::SoftmaxShape sh{batch, heads, q_len, k_len, key_len, causal ? 1 : 0};
+    return from_cuda(ls::launch_softmax_dropout_bwd(dt, dx, y, dy_drop,
+                                                    reinterpret_cast<const uint8_t*>(mask_bits),
+                                                    sh, rng.scale,
+                                                    static_cast<cudaStream_t>(stream)),
+                     "ls_softmax_dropout_bwd launch");
+}
+
 }  // extern "C"
 #pragma GCC visibility pop

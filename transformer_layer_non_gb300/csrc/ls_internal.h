@@ -59,11 +59,18 @@ cudaError_t launch_softmax_fwd(DType dt, void* y, const void* x, const SoftmaxSh
                                cudaStream_t s);
 cudaError_t launch_softmax_bwd(DType dt, void* dx, const void* y, const void* dy,
                                const SoftmaxShape& sh, cudaStream_t s);
+// Softmax fused with dropout on the probabilities: the forward also writes
+// y_drop = bit * y / (1-p) and the bits (keep on valid entries, 0 on masked
+// ones); the backward takes the gradient of y_drop and the bits.
+cudaError_t launch_softmax_dropout_fwd(DType dt, void* y, void* y_drop, uint8_t* mask,
+                                       const void* x, const SoftmaxShape& sh,
+                                       const DropoutRng& rng, cudaStream_t s);
+cudaError_t launch_softmax_dropout_bwd(DType dt, void* dx, const void* y, const void* dy_drop,
+                                       const uint8_t* mask, const SoftmaxShape& sh, float scale,
+                                       cudaStream_t s);
 
 constexpr int64_t kMaxRowLen = 16384;
 
-// Read and clear the device-side failure flags of one translation unit's
-// kernels (synchronous).
 // Bias + reshape of Q, K, V: [batch*seq, 3*heads*d] (+ bias) <-> [3, batch,
 // heads, seq, d].  The backward writes one FP32 partial row of the bias
 // gradient per 128 rows (dropout_bwd_plan(batch*seq, 3*heads*d)) when partial
@@ -81,6 +88,8 @@ struct AdamHyper {
 cudaError_t launch_adam(DType dt, void* param, const void* grad, float* m, float* v, int64_t n,
                         const AdamHyper& h, cudaStream_t s);
 
+// Read and clear the device-side failure flags of one translation unit's
+// kernels (synchronous).
 cudaError_t softmax_take_device_error(unsigned int* flags);
 cudaError_t dropout_take_device_error(unsigned int* flags);
 cudaError_t layernorm_take_device_error(unsigned int* flags);

@@ -66,8 +66,31 @@ template <typename T, int LPR, int VPT>
 struct RowBuf {
     Raw8<T> a[VPT];  // x (forward) or y (backward)
     Raw8<T> b[VPT];  // dy (backward only)
+    uint32_t mb[VPT];  // dropout bits of each vector (fused dropout backward only)
     int vlen;
 };
+
+// Dropout on the probabilities, fused into the softmax ("CMU 11-868 L10
+// (LightSeq)", technique 1: the elementwise step after a reduce kernel joins
+// it).  Forward: y_drop = bit * y * scale, with bit = keep on valid entries
+// and 0 on masked ones, one mask byte per 8-element vector (bit j = element
+// 8v + j); backward: the mask is read.  Unused by the plain softmax.
+struct DropArgs {
+    void* y_drop;
+    uint8_t* mask;
+    uint32_t thr;
+    float scale;
+    PhiloxSchedule ks;
+    uint32_t off_lo, off_hi;
+    uint64_t tail_at;  // forward: the bytes [tail_at, tail_at + tail) of the last
+    int tail;          // mask word lie past the last element and are written as 0
+};
+
+// The forward's one-thread duty: zero the mask bytes past the last element.
+__device__ __forceinline__ void drop_tail(const DropArgs& d) {
+    if (blockIdx.x == 0 && threadIdx.x == 0)
+        for (int k = 0; k < d.tail; ++k) d.mask[d.tail_at + k] = 0;
+}
 
 // Valid length of a row, 0 past the last row.  With per-batch key lengths it
 // costs a dependent load, so the kernels fetch it one row ahead of the row's
@@ -76,9 +99,10 @@ __device__ __forceinline__ int row_vlen(int64_t row, int64_t nrows, int k_len, c
     return row < nrows ? valid_len(row, k_len, mk) : 0;
 }
 
-template <typename T, int LPR, int VPT, bool BWD>
+template <typename T, int LPR, int VPT, bool BWD, bool DROP>
 __device__ __forceinline__ void sm_load(RowBuf<T, LPR, VPT>& buf, const T* p, const T* q,
-                                        int64_t row, int vlen, int k_len, int gl) {
+                                        int64_t row, int vlen, int k_len, int gl,
+                                        const DropArgs& d) {
     buf.vlen = vlen;
     const int64_t base = row * k_len;
 #pragma unroll
@@ -87,8 +111,27 @@ __device__ __forceinline__ void sm_load(RowBuf<T, LPR, VPT>& buf, const T* p, co
         if (v * kVec < buf.vlen) {
             buf.a[k] = load8<T>(p + base + v * kVec);
             if (BWD) buf.b[k] = load8<T>(q + base + v * kVec);
+            if (BWD && DROP) buf.mb[k] = d.mask[(base >> 3) + v];
         }
     }
+}
+
+// Fused dropout epilogue of one output vector v of a row (forward): the keep
+// bits of its valid elements, the dropped probabilities and the mask byte.
+template <typename T>
+__device__ __forceinline__ void drop_store(const float (&o)[kVec], int64_t base, int v, int vlen,
+                                           const DropArgs& d) {
+    const int cnt = min(max(vlen - v * kVec, 0), kVec);
+    uint32_t bits = 0;
+    if (cnt > 0)
+        bits = keep_bits8(static_cast<uint64_t>(base + v * kVec), d.thr, d.ks, d.off_lo,
+                          d.off_hi) &
+               ((1u << cnt) - 1u);
+    float od[kVec];
+#pragma unroll
+    for (int j = 0; j < kVec; ++j) od[j] = ((bits >> j) & 1u) ? o[j] * d.scale : 0.f;
+    store8f<T>(static_cast<T*>(d.y_drop) + base + v * kVec, od);
+    d.mask[(base >> 3) + v] = static_cast<uint8_t>(bits);
 }
 
 // The forward row is branch-free across the valid/masked boundary: element j
@@ -96,9 +139,9 @@ __device__ __forceinline__ void sm_load(RowBuf<T, LPR, VPT>& buf, const T* p, co
 // elements are replaced by selects (vectors that were not loaded hold
 // arbitrary bits, which a select discards).  Divergent branches at the
 // boundary would run the full, partial and empty paths one after another.
-template <typename T, int LPR, int VPT>
+template <typename T, int LPR, int VPT, bool DROP>
 __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y, int64_t row,
-                                           int64_t nrows, int k_len, int gl) {
+                                           int64_t nrows, int k_len, int gl, const DropArgs& d) {
     const int nvec = k_len / kVec;
     const int vlen = buf.vlen;
     float f[VPT][kVec];
@@ -136,6 +179,7 @@ __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y,
 #pragma unroll
             for (int j = 0; j < kVec; ++j) o[j] = f[k][j] * inv;  // masked: 0 * inv = +0
             store8f<T>(y + base + v * kVec, o);
+            if (DROP) drop_store<T>(o, base, v, vlen, d);
         }
     }
 }
@@ -144,11 +188,55 @@ __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y,
 // measured faster this way than branch-free (which needs more registers).  A
 // vector wholly inside the valid prefix takes the unpredicated path, with the
 // FP16 conversions folded into mixed-precision instructions.
-template <typename T, int LPR, int VPT>
+template <typename T, int LPR, int VPT, bool DROP>
 __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx, int64_t row,
-                                           int64_t nrows, int k_len, int gl) {
+                                           int64_t nrows, int k_len, int gl, const DropArgs& d) {
     const int nvec = k_len / kVec;
     const int vlen = buf.vlen;
+    if (DROP) {
+        // g = bit * dy_drop * scale, then the softmax backward of g.
+        float dot = 0.f;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = gl + k * LPR;
+            if (v * kVec < vlen) {
+                float yf[kVec], df[kVec];
+                unpack(buf.a[k], yf);
+                unpack(buf.b[k], df);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) {
+                    const bool on = v * kVec + j < vlen && ((buf.mb[k] >> j) & 1u);
+                    dot = fmaf(yf[j], on ? df[j] * d.scale : 0.f, dot);
+                }
+            }
+        }
+        dot = group_sum<LPR>(dot);
+        if (row >= nrows) return;
+        const int64_t base = row * k_len;
+#pragma unroll
+        for (int k = 0; k < VPT; ++k) {
+            const int v = gl + k * LPR;
+            if (v < nvec) {
+                float o[kVec];
+                if (v * kVec < vlen) {
+                    float yf[kVec], df[kVec];
+                    unpack(buf.a[k], yf);
+                    unpack(buf.b[k], df);
+#pragma unroll
+                    for (int j = 0; j < kVec; ++j) {
+                        const bool valid = v * kVec + j < vlen;
+                        const float g = valid && ((buf.mb[k] >> j) & 1u) ? df[j] * d.scale : 0.f;
+                        o[j] = valid ? yf[j] * (g - dot) : 0.f;
+                    }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < kVec; ++j) o[j] = 0.f;
+                }
+                store8f<T>(dx + base + v * kVec, o);
+            }
+        }
+        return;
+    }
     float dot = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -195,11 +283,15 @@ __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx
 }
 
 // BWD = false: out = y, p = x.   BWD = true: out = dx, p = y, q = dy.
-template <typename T, int LPR, int VPT, bool BWD>
+// DROP: dropout on the probabilities fused in (forward writes d.y_drop and
+// d.mask; backward reads d.mask and q = dy_drop).
+template <typename T, int LPR, int VPT, bool BWD, bool DROP>
 __global__ void __launch_bounds__(kThreads, min_ctas<T>((VPT == 1 || (BWD && VPT == 2)) ? 4 : 3))
-softmax_group_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, RowMask mk) {
+softmax_group_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, RowMask mk,
+                     const __grid_constant__ DropArgs d) {
     constexpr int RPC = kThreads / LPR;
     pdl_enter();
+    if (DROP && !BWD) drop_tail(d);
     const int gl = threadIdx.x % LPR;
     const int slot = threadIdx.x / LPR;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * RPC;
@@ -210,33 +302,33 @@ softmax_group_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, R
         int vl = row_vlen(r, nrows, k_len, mk);
         for (; __any_sync(0xffffffffu, r < nrows); r += stride) {
             const int vln = row_vlen(r + stride, nrows, k_len, mk);
-            sm_load<T, LPR, VPT, BWD>(ba, p, q, r, vl, k_len, gl);
+            sm_load<T, LPR, VPT, BWD, DROP>(ba, p, q, r, vl, k_len, gl, d);
             if (BWD)
-                sm_bwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
+                sm_bwd_row<T, LPR, VPT, DROP>(ba, out, r, nrows, k_len, gl, d);
             else
-                sm_fwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
+                sm_fwd_row<T, LPR, VPT, DROP>(ba, out, r, nrows, k_len, gl, d);
             vl = vln;
         }
         return;
     }
-    sm_load<T, LPR, VPT, BWD>(ba, p, q, r, row_vlen(r, nrows, k_len, mk), k_len, gl);
+    sm_load<T, LPR, VPT, BWD, DROP>(ba, p, q, r, row_vlen(r, nrows, k_len, mk), k_len, gl, d);
     int vl_next = row_vlen(r + stride, nrows, k_len, mk);  // the row bb takes next
     while (__any_sync(0xffffffffu, r < nrows)) {
         const int64_t r1 = r + stride;
-        sm_load<T, LPR, VPT, BWD>(bb, p, q, r1, vl_next, k_len, gl);
+        sm_load<T, LPR, VPT, BWD, DROP>(bb, p, q, r1, vl_next, k_len, gl, d);
         vl_next = row_vlen(r1 + stride, nrows, k_len, mk);
         if (BWD)
-            sm_bwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
+            sm_bwd_row<T, LPR, VPT, DROP>(ba, out, r, nrows, k_len, gl, d);
         else
-            sm_fwd_row<T, LPR, VPT>(ba, out, r, nrows, k_len, gl);
+            sm_fwd_row<T, LPR, VPT, DROP>(ba, out, r, nrows, k_len, gl, d);
         if (!__any_sync(0xffffffffu, r1 < nrows)) break;
         r = r1 + stride;
-        sm_load<T, LPR, VPT, BWD>(ba, p, q, r, vl_next, k_len, gl);
+        sm_load<T, LPR, VPT, BWD, DROP>(ba, p, q, r, vl_next, k_len, gl, d);
         vl_next = row_vlen(r + stride, nrows, k_len, mk);
         if (BWD)
-            sm_bwd_row<T, LPR, VPT>(bb, out, r1, nrows, k_len, gl);
+            sm_bwd_row<T, LPR, VPT, DROP>(bb, out, r1, nrows, k_len, gl, d);
         else
-            sm_fwd_row<T, LPR, VPT>(bb, out, r1, nrows, k_len, gl);
+            sm_fwd_row<T, LPR, VPT, DROP>(bb, out, r1, nrows, k_len, gl, d);
     }
 }
 
@@ -400,12 +492,14 @@ __device__ __forceinline__ float cta_sum(float v, float* red) {
     return r;
 }
 
-template <typename T, int WARPS, int VPT>
+template <typename T, int WARPS, int VPT, bool DROP>
 __global__ void __launch_bounds__(WARPS * 32)
-softmax_fwd_cta_kernel(T* y, const T* x, int k_len, RowMask mk) {
+softmax_fwd_cta_kernel(T* y, const T* x, int k_len, RowMask mk,
+                       const __grid_constant__ DropArgs d) {
     constexpr int NT = WARPS * 32;
     __shared__ float red[WARPS];
     pdl_enter();
+    if (DROP) drop_tail(d);
     const int64_t row = blockIdx.x;
     const int vlen = valid_len(row, k_len, mk);
     const int nvec = k_len / kVec;
@@ -446,13 +540,15 @@ softmax_fwd_cta_kernel(T* y, const T* x, int k_len, RowMask mk) {
 #pragma unroll
             for (int j = 0; j < kVec; ++j) o[j] = f[k][j] * inv;
             store8f<T>(y + base + v * kVec, o);
+            if (DROP) drop_store<T>(o, base, v, vlen, d);
         }
     }
 }
 
-template <typename T, int WARPS, int VPT>
+template <typename T, int WARPS, int VPT, bool DROP>
 __global__ void __launch_bounds__(WARPS * 32)
-softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk) {
+softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
+                       const __grid_constant__ DropArgs d) {
     constexpr int NT = WARPS * 32;
     __shared__ float red[WARPS];
     pdl_enter();
@@ -461,14 +557,21 @@ softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk) {
     const int nvec = k_len / kVec;
     const int64_t base = row * k_len;
     Raw8<T> yr[VPT], dr[VPT];
+    uint32_t mb[VPT];
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = threadIdx.x + k * NT;
+        mb[k] = 0;
         if (v * kVec < vlen) {
             yr[k] = load8<T>(y + base + v * kVec);
             dr[k] = load8<T>(dy + base + v * kVec);
+            if (DROP) mb[k] = d.mask[(base >> 3) + v];
         }
     }
+    // With fused dropout the incoming gradient is g = bit * dy_drop * scale.
+    auto grad = [&](int k, const float (&df)[kVec], int j) {
+        return DROP ? (((mb[k] >> j) & 1u) ? df[j] * d.scale : 0.f) : df[j];
+    };
     float dot = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
@@ -479,7 +582,7 @@ softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk) {
             unpack(dr[k], df);
 #pragma unroll
             for (int j = 0; j < kVec; ++j)
-                if (v * kVec + j < vlen) dot = fmaf(yf[j], df[j], dot);
+                if (v * kVec + j < vlen) dot = fmaf(yf[j], grad(k, df, j), dot);
         }
     }
     dot = cta_sum<WARPS>(dot, red);
@@ -494,7 +597,7 @@ softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk) {
                 unpack(dr[k], df);
 #pragma unroll
                 for (int j = 0; j < kVec; ++j)
-                    o[j] = (v * kVec + j < vlen) ? yf[j] * (df[j] - dot) : 0.f;
+                    o[j] = (v * kVec + j < vlen) ? yf[j] * (grad(k, df, j) - dot) : 0.f;
             } else {
 #pragma unroll
                 for (int j = 0; j < kVec; ++j) o[j] = 0.f;
@@ -556,14 +659,14 @@ int occupancy(K kernel, int threads, size_t smem) {
     return n;
 }
 
-template <typename T, int LPR, int VPT, bool BWD>
+template <typename T, int LPR, int VPT, bool BWD, bool DROP>
 cudaError_t group_launch(T* out, const T* p, const T* q, int64_t nrows, int k_len,
-                         const RowMask& m, const SmPlan& pl, cudaStream_t s) {
-    auto kern = softmax_group_kernel<T, LPR, VPT, BWD>;
+                         const RowMask& m, const DropArgs& d, const SmPlan& pl, cudaStream_t s) {
+    auto kern = softmax_group_kernel<T, LPR, VPT, BWD, DROP>;
     static const int occ = occupancy(kern, kThreads, 0);
     const int64_t grid = std::min<int64_t>(pl.grid, int64_t{sm_count()} * occ);
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s, out, p, q,
-                      nrows, k_len, m);
+                      nrows, k_len, m, d);
 }
 template <typename T, int VPT, bool BWD>
 cudaError_t tma_launch(T* out, const T* p, const T* q, int64_t nrows, int k_len,
@@ -583,37 +686,43 @@ cudaError_t tma_launch(T* out, const T* p, const T* q, int64_t nrows, int k_len,
                       p, q, nrows, k_len, m);
 }
 
-template <typename T, int LPR, int VPT>
+// The plain forward of warp-per-row lengths takes the bulk-copy kernel; the
+// fused-dropout forward stays on the register kernel.
+template <typename T, bool DROP, int LPR, int VPT>
 cudaError_t fwd_group(void* y, const void* x, int64_t nrows, int k_len, const RowMask& m,
-                      const SmPlan& p, cudaStream_t s) {
-    if constexpr (LPR == 32)
+                      const DropArgs& d, const SmPlan& p, cudaStream_t s) {
+    if constexpr (LPR == 32 && !DROP)
         return tma_launch<T, VPT, false>(static_cast<T*>(y), static_cast<const T*>(x),
                                          static_cast<const T*>(nullptr), nrows, k_len, m, s);
     else
-    return group_launch<T, LPR, VPT, false>(static_cast<T*>(y), static_cast<const T*>(x),
-                                            static_cast<const T*>(nullptr), nrows, k_len, m, p, s);
+        return group_launch<T, LPR, VPT, false, DROP>(static_cast<T*>(y), static_cast<const T*>(x),
+                                                      static_cast<const T*>(nullptr), nrows,
+                                                      k_len, m, d, p, s);
 }
-template <typename T, int LPR, int VPT>
+template <typename T, bool DROP, int LPR, int VPT>
 cudaError_t bwd_group(void* dx, const void* y, const void* dy, int64_t nrows, int k_len,
-                      const RowMask& m, const SmPlan& p, cudaStream_t s) {
-    return group_launch<T, LPR, VPT, true>(static_cast<T*>(dx), static_cast<const T*>(y),
-                                           static_cast<const T*>(dy), nrows, k_len, m, p, s);
+                      const RowMask& m, const DropArgs& d, const SmPlan& p, cudaStream_t s) {
+    return group_launch<T, LPR, VPT, true, DROP>(static_cast<T*>(dx), static_cast<const T*>(y),
+                                                 static_cast<const T*>(dy), nrows, k_len, m, d,
+                                                 p, s);
 }
-template <typename T, int WARPS, int VPT>
+template <typename T, bool DROP, int WARPS, int VPT>
 cudaError_t fwd_cta(void* y, const void* x, int64_t nrows, int k_len, const RowMask& m,
-                    const SmPlan& p, cudaStream_t s) {
-    return launch_pdl(softmax_fwd_cta_kernel<T, WARPS, VPT>, dim3(static_cast<unsigned>(p.grid)),
-                      dim3(WARPS * 32), 0, s, static_cast<T*>(y), static_cast<const T*>(x), k_len,
-                      m);
+                    const DropArgs& d, const SmPlan& p, cudaStream_t s) {
+    return launch_pdl(softmax_fwd_cta_kernel<T, WARPS, VPT, DROP>,
+                      dim3(static_cast<unsigned>(p.grid)), dim3(WARPS * 32), 0, s,
+                      static_cast<T*>(y), static_cast<const T*>(x), k_len, m, d);
 }
-template <typename T, int WARPS, int VPT>
+template <typename T, bool DROP, int WARPS, int VPT>
 cudaError_t bwd_cta(void* dx, const void* y, const void* dy, int64_t nrows, int k_len,
-                    const RowMask& m, const SmPlan& p, cudaStream_t s) {
-    return launch_pdl(softmax_bwd_cta_kernel<T, WARPS, VPT>, dim3(static_cast<unsigned>(p.grid)),
-                      dim3(WARPS * 32), 0, s, static_cast<T*>(dx), static_cast<const T*>(y),
-                      static_cast<const T*>(dy), k_len, m);
+                    const RowMask& m, const DropArgs& d, const SmPlan& p, cudaStream_t s) {
+    return launch_pdl(softmax_bwd_cta_kernel<T, WARPS, VPT, DROP>,
+                      dim3(static_cast<unsigned>(p.grid)), dim3(WARPS * 32), 0, s,
+                      static_cast<T*>(dx), static_cast<const T*>(y), static_cast<const T*>(dy),
+                      k_len, m, d);
 }
 
+#define LS_SM_T_DROP T, DROP
 #define LS_SM_GROUP_CASES(FN, T, ...)                                    \
     switch (p.lpr) {                                                     \
         case 1: return FN<T, 1, 1>(__VA_ARGS__);                         \
@@ -650,31 +759,52 @@ cudaError_t bwd_cta(void* dx, const void* y, const void* dy, int64_t nrows, int 
     }                                                                    \
     return cudaErrorInvalidConfiguration;
 
-template <typename T>
-cudaError_t fwd_dispatch(void* y, const void* x, const SoftmaxShape& sh, cudaStream_t s) {
-    const int64_t nrows = sh.batch * sh.heads * sh.q_len;
-    const int k_len = static_cast<int>(sh.k_len);
-    const SmPlan p = plan_for(nrows, sh.k_len);
-    const RowMask m = make_mask(sh);
-    if (!p.cta) {
-        LS_SM_GROUP_CASES(fwd_group, T, y, x, nrows, k_len, m, p, s)
-    } else {
-        LS_SM_CTA_CASES(fwd_cta, T, y, x, nrows, k_len, m, p, s)
-    }
-}
-
-template <typename T>
-cudaError_t bwd_dispatch(void* dx, const void* y, const void* dy, const SoftmaxShape& sh,
+template <typename T, bool DROP>
+cudaError_t fwd_dispatch(void* y, const void* x, const SoftmaxShape& sh, const DropArgs& d,
                          cudaStream_t s) {
     const int64_t nrows = sh.batch * sh.heads * sh.q_len;
     const int k_len = static_cast<int>(sh.k_len);
     const SmPlan p = plan_for(nrows, sh.k_len);
     const RowMask m = make_mask(sh);
     if (!p.cta) {
-        LS_SM_GROUP_CASES(bwd_group, T, dx, y, dy, nrows, k_len, m, p, s)
+        LS_SM_GROUP_CASES(fwd_group, LS_SM_T_DROP, y, x, nrows, k_len, m, d, p, s)
     } else {
-        LS_SM_CTA_CASES(bwd_cta, T, dx, y, dy, nrows, k_len, m, p, s)
+        LS_SM_CTA_CASES(fwd_cta, LS_SM_T_DROP, y, x, nrows, k_len, m, d, p, s)
     }
+}
+
+template <typename T, bool DROP>
+cudaError_t bwd_dispatch(void* dx, const void* y, const void* dy, const SoftmaxShape& sh,
+                         const DropArgs& d, cudaStream_t s) {
+    const int64_t nrows = sh.batch * sh.heads * sh.q_len;
+    const int k_len = static_cast<int>(sh.k_len);
+    const SmPlan p = plan_for(nrows, sh.k_len);
+    const RowMask m = make_mask(sh);
+    if (!p.cta) {
+        LS_SM_GROUP_CASES(bwd_group, LS_SM_T_DROP, dx, y, dy, nrows, k_len, m, d, p, s)
+    } else {
+        LS_SM_CTA_CASES(bwd_cta, LS_SM_T_DROP, dx, y, dy, nrows, k_len, m, d, p, s)
+    }
+}
+
+DropArgs no_drop() {
+    DropArgs d{};
+    return d;
+}
+
+DropArgs make_drop(void* y_drop, uint8_t* mask, const DropoutRng& rng, uint64_t n) {
+    DropArgs d{};
+    d.tail_at = n / 8;  // n is a multiple of 8
+    d.tail = static_cast<int>(((n + 31) / 32) * 4 - n / 8);
+    d.y_drop = y_drop;
+    d.mask = mask;
+    d.thr = rng.thr;
+    d.scale = rng.scale;
+    d.ks = philox_schedule(PhiloxKey{static_cast<uint32_t>(rng.seed),
+                                     static_cast<uint32_t>(rng.seed >> 32)});
+    d.off_lo = static_cast<uint32_t>(rng.offset);
+    d.off_hi = static_cast<uint32_t>(rng.offset >> 32);
+    return d;
 }
 
 }  // namespace
@@ -685,14 +815,33 @@ cudaError_t softmax_take_device_error(unsigned int* flags) {
 
 cudaError_t launch_softmax_fwd(DType dt, void* y, const void* x, const SoftmaxShape& sh,
                                cudaStream_t s) {
-    if (dt == DType::F16) return fwd_dispatch<__half>(y, x, sh, s);
-    return fwd_dispatch<float>(y, x, sh, s);
+    if (dt == DType::F16) return fwd_dispatch<__half, false>(y, x, sh, no_drop(), s);
+    return fwd_dispatch<float, false>(y, x, sh, no_drop(), s);
 }
 
 cudaError_t launch_softmax_bwd(DType dt, void* dx, const void* y, const void* dy,
                                const SoftmaxShape& sh, cudaStream_t s) {
-    if (dt == DType::F16) return bwd_dispatch<__half>(dx, y, dy, sh, s);
-    return bwd_dispatch<float>(dx, y, dy, sh, s);
+    if (dt == DType::F16) return bwd_dispatch<__half, false>(dx, y, dy, sh, no_drop(), s);
+    return bwd_dispatch<float, false>(dx, y, dy, sh, no_drop(), s);
+}
+
+cudaError_t launch_softmax_dropout_fwd(DType dt, void* y, void* y_drop, uint8_t* mask,
+                                       const void* x, const SoftmaxShape& sh,
+                                       const DropoutRng& rng, cudaStream_t s) {
+    const DropArgs d = make_drop(y_drop, mask, rng,
+                                 static_cast<uint64_t>(sh.batch * sh.heads * sh.q_len * sh.k_len));
+    if (dt == DType::F16) return fwd_dispatch<__half, true>(y, x, sh, d, s);
+    return fwd_dispatch<float, true>(y, x, sh, d, s);
+}
+
+cudaError_t launch_softmax_dropout_bwd(DType dt, void* dx, const void* y, const void* dy_drop,
+                                       const uint8_t* mask, const SoftmaxShape& sh, float scale,
+                                       cudaStream_t s) {
+    DropArgs d{};
+    d.mask = const_cast<uint8_t*>(mask);  // read only in the backward
+    d.scale = scale;
+    if (dt == DType::F16) return bwd_dispatch<__half, true>(dx, y, dy_drop, sh, d, s);
+    return bwd_dispatch<float, true>(dx, y, dy_drop, sh, d, s);
 }
 
 }  // namespace ls

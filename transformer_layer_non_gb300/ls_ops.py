@@ -36,6 +36,7 @@ EXPORTS = (
     "ls_layernorm_fwd", "ls_layernorm_bwd", "ls_softmax_fwd", "ls_softmax_bwd",
     "ls_layernorm_bwd_noalloc", "ls_check_device_errors", "ls_adam_update",
     "ls_bias_reshape_qkv_fwd", "ls_bias_reshape_qkv_bwd",
+    "ls_softmax_dropout_fwd", "ls_softmax_dropout_bwd",
 )
 
 
@@ -68,6 +69,10 @@ _SIGNATURES = {
     "ls_layernorm_bwd_noalloc": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
     "ls_softmax_fwd": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
+    "ls_softmax_dropout_fwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT,
+                                      _F32, _U64, _U64, _P]),
+    "ls_softmax_dropout_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT,
+                                      _F32, _P]),
     "ls_bias_reshape_qkv_fwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P]),
     "ls_bias_reshape_qkv_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _SZ, _P]),
     "ls_adam_update": (_INT, [_INT, _P, _P, _P, _P, _I64, _F32, _F32, _F32, _F32, _F32, _I64,
@@ -276,4 +281,22 @@ def ls_bias_reshape_qkv_bwd(dqkv, dbias, dq_k_v, batch: int, seq: int, heads: in
     _check(load().ls_bias_reshape_qkv_bwd(_dtype_code(dq_k_v), _ptr(dqkv), _ptr(dbias),
                                           _ptr(dq_k_v), batch, seq, heads, d, _ptr(workspace),
                                           _nbytes(workspace), _stream(stream)))
+
+
+def ls_softmax_dropout_fwd(y, y_drop, mask_bits, x, key_len=None, causal: bool = False,
+                           p: float = 0.1, seed: int = 0, offset: int = 0, stream=None):
+    """Softmax of x [batch, heads, q_len, k_len] into y, then dropout on the
+    probabilities into y_drop with its bits in mask_bits (int32 words)."""
+    b, h, lq, lk = x.shape
+    _check(load().ls_softmax_dropout_fwd(_dtype_code(x), _ptr(y), _ptr(y_drop), _ptr(mask_bits),
+                                         _ptr(x), b, h, lq, lk, _ptr(key_len), int(bool(causal)),
+                                         p, seed, offset, _stream(stream)))
+
+
+def ls_softmax_dropout_bwd(dx, y, dy_drop, mask_bits, key_len=None, causal: bool = False,
+                           p: float = 0.1, stream=None):
+    b, h, lq, lk = y.shape
+    _check(load().ls_softmax_dropout_bwd(_dtype_code(y), _ptr(dx), _ptr(y), _ptr(dy_drop),
+                                         _ptr(mask_bits), b, h, lq, lk, _ptr(key_len),
+                                         int(bool(causal)), p, _stream(stream)))
 

@@ -57,6 +57,9 @@ def parse_args():
                          "in layer order) inside the NVTX range 'profile' (for ncu --nvtx "
                          "--nvtx-include profile/); no timing")
     ap.add_argument("--profile-launches", type=int, default=2)
+    ap.add_argument("--next-ops", action="store_true",
+                    help="time the operators beyond the layer step (bias + reshape of Q/K/V, "
+                         "softmax with fused dropout) at the workload's shapes; one JSON line")
     ap.add_argument("--trainer", action="store_true",
                     help="time the fused trainer update (Adam) over the BERT-base parameter "
                          "workspace; one JSON line")
@@ -880,6 +883,95 @@ def run_trainer(args):
     return 0
 
 
+def time_alone(t, keys, make_thunk, reps=20):
+    """ms per launch of one operator alone: a graph of back-to-back launches
+    over enough cloned buffer sets (keys of t) that every launch finds its
+    inputs outside L2."""
+    import math
+
+    fp = sum(t[k].numel() * t[k].element_size() for k in keys)
+    nsets = max(2, min(48, math.ceil(3 * L2_BYTES / max(fp, 1))))
+    sets = []
+    for _ in range(nsets):
+        c = dict(t)
+        for k in keys:
+            c[k] = t[k].clone()
+        sets.append(c)
+    g = capture([make_thunk(c) for c in sets])
+    ms = time_graph(g, reps) / nsets
+    del g, sets
+    return ms, nsets
+
+
+def run_next_ops(args):
+    """Bias + reshape of Q, K, V and softmax with fused dropout, forward and
+    backward, at the workload's shapes, each operator alone."""
+    import numpy as np
+    import torch
+
+    from transformer_layer_non_gb300 import accounting, ls_ops, synth
+
+    ls_ops.load()
+    L = synth.LAYERS[args.workload]
+    T, H, B, S, h = L.tokens, L.hidden, L.batch, L.seq, L.heads
+    d = H // h
+    dt = {"f16": torch.float16, "f32": torch.float32}[L.dtype]
+    es = 2 if L.dtype == "f16" else 4
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(args.seed)
+    rn = lambda *shape, std=1.0: (torch.randn(*shape, generator=g, device=dev) * std).to(dt)  # noqa: E731
+    host = synth.layer_inputs(L, args.seed, which={"key_len"})
+    kl_np = host.get("key_len")
+    t = {"qkv": rn(T, 3 * H), "bias": rn(3 * H, std=0.02), "q_k_v": torch.empty(3, B, h, S, d, dtype=dt, device=dev),
+         "dq_k_v": rn(3, B, h, S, d), "dqkv": torch.empty(T, 3 * H, dtype=dt, device=dev),
+         "dbias": torch.empty(3 * H, dtype=dt, device=dev),
+         "scores": rn(B, h, S, S, std=3.0), "y": torch.empty(B, h, S, S, dtype=dt, device=dev),
+         "y_drop": torch.empty(B, h, S, S, dtype=dt, device=dev),
+         "mask": torch.empty((B * h * S * S + 31) // 32, dtype=torch.int32, device=dev),
+         "dy_drop": rn(B, h, S, S), "dx": torch.empty(B, h, S, S, dtype=dt, device=dev),
+         "key_len": torch.from_numpy(kl_np).to(dev) if kl_np is not None else None}
+    ws = ls_ops.new_workspace([(T, 3 * H)], device=dev)
+    p = L.p
+    ls_ops.ls_softmax_dropout_fwd(t["y"], t["y_drop"], t["mask"], t["scores"], t["key_len"],
+                                  L.causal, p, 0, 9)
+    torch.cuda.synchronize()
+    sm = dict(batch=B, heads=h, q_len=S, k_len=S, esize=es, key_len=kl_np, causal=L.causal)
+    ops = {
+        "qkv_fwd": (["qkv", "q_k_v"], lambda c: lambda: ls_ops.ls_bias_reshape_qkv_fwd(
+            c["q_k_v"], c["qkv"], c["bias"], B, S, h), accounting.qkv_fwd_bytes(T, 3 * H, es)),
+        "qkv_bwd": (["dq_k_v", "dqkv"], lambda c: lambda: ls_ops.ls_bias_reshape_qkv_bwd(
+            c["dqkv"], c["dbias"], c["dq_k_v"], B, S, h, workspace=ws),
+            accounting.qkv_bwd_bytes(T, 3 * H, es)),
+        "softmax_dropout_fwd": (["scores", "y", "y_drop", "mask"], lambda c: lambda:
+            ls_ops.ls_softmax_dropout_fwd(c["y"], c["y_drop"], c["mask"], c["scores"],
+                                          c["key_len"], L.causal, p, 0, 9),
+            accounting.softmax_dropout_fwd_bytes(**sm)),
+        "softmax_dropout_bwd": (["y", "dy_drop", "mask", "dx"], lambda c: lambda:
+            ls_ops.ls_softmax_dropout_bwd(c["dx"], c["y"], c["dy_drop"], c["mask"],
+                                          c["key_len"], L.causal, p),
+            accounting.softmax_dropout_bwd_bytes(**sm)),
+    }
+    peak, peak_kind = load_peaks()
+    rep = {}
+    for name, (keys, mk, nbytes) in ops.items():
+        ms, nsets = time_alone(t, keys, mk)
+        gbs = nbytes / (ms * 1e-3) / 1e9
+        rep[name] = {"us": round(ms * 1e3, 2), "bytes": int(nbytes), "GB/s": round(gbs, 1),
+                     "frac": round(gbs / peak, 4), "buffer_sets": nsets}
+    line = {"metric": "next operators: achieved HBM GB/s per operator", "unit": "GB/s",
+            "peak": peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
+            "config": {"workload": L.name, "tokens": T, "hidden": H, "heads": h, "seq_len": S,
+                       "dropout_p": p, "storage": L.dtype,
+                       "l2": "rotating cloned buffer sets >= 3 x L2"},
+            "per_op": rep}
+    print(json.dumps(line), flush=True)
+    if args.details:
+        with open(args.details, "w") as f:
+            json.dump(line, f, indent=1)
+    return 0
+
+
 def main():
     args = parse_args()
     if args.impl == "reference":
@@ -890,6 +982,8 @@ def main():
         return run_sweep(args)
     if args.trainer:
         return run_trainer(args)
+    if args.next_ops:
+        return run_next_ops(args)
     return run_ours(args)
 
 

@@ -79,3 +79,17 @@ def test_softmax_valid_counts():
     v = acc.softmax_valid_count(1, 1, 1, 16, np.array([7]), False)
     assert acc.softmax_fwd_bytes(1, 1, 1, 16, 2, np.array([7])) == v * 2 + 4 + 16 * 2
     assert acc.softmax_bwd_bytes(1, 1, 1, 16, 2, np.array([7])) == v * 4 + 4 + 16 * 2
+
+
+def test_next_operator_bytes_by_hand():
+    # [4, 96] QKV rows: 384 values in and out, plus the 96-value bias.
+    assert acc.qkv_fwd_bytes(4, 96, 2) == 384 * 2 * 2 + 96 * 2
+    assert acc.qkv_bwd_bytes(4, 96, 2) == 384 * 2 * 2 + 96 * 2
+    # Trainer: 22 bytes per FP16 element (2+2+4+4 in, 2+4+4 out).
+    assert acc.adam_bytes(1000, 2) == 22000
+    # Softmax+dropout over [1, 1, 2, 16] with 8 valid keys per row: 16 valid
+    # values in; 2 x 32 values and 32 mask bits out.
+    kl = np.array([8], dtype=np.int32)
+    assert acc.softmax_dropout_fwd_bytes(1, 1, 2, 16, 2, kl) == 16 * 2 + 4 + 2 * 32 * 2 + 4
+    assert acc.softmax_dropout_bwd_bytes(1, 1, 2, 16, 2, kl) == 2 * 16 * 2 + 2 + 4 + 32 * 2
+

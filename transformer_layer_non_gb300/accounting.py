@@ -98,6 +98,41 @@ def softmax_bwd_bytes(batch, heads, q_len, k_len, esize, key_len=None, causal=Fa
                    [rows * k_len * esize])
 
 
+def softmax_dropout_fwd_bytes(batch, heads, q_len, k_len, esize, key_len=None,
+                              causal=False) -> float:
+    """Softmax with dropout on the probabilities: the valid scores in; y and
+    y_drop (whole rows) and one mask bit per element out."""
+    valid = softmax_valid_count(batch, heads, q_len, k_len, key_len, causal)
+    n = batch * heads * q_len * k_len
+    return traffic([valid * esize] + ([4 * batch] if key_len is not None else []),
+                   [2 * n * esize, n * MASK_BYTES_PER_ELEM])
+
+
+def softmax_dropout_bwd_bytes(batch, heads, q_len, k_len, esize, key_len=None,
+                              causal=False) -> float:
+    """Its backward: y, dy_drop and the mask bits of the valid entries in; dx out."""
+    valid = softmax_valid_count(batch, heads, q_len, k_len, key_len, causal)
+    n = batch * heads * q_len * k_len
+    return traffic([2 * valid * esize, valid * MASK_BYTES_PER_ELEM] +
+                   ([4 * batch] if key_len is not None else []), [n * esize])
+
+
+def qkv_fwd_bytes(rows: int, cols: int, esize: int) -> float:
+    """Bias + reshape of Q, K, V over [rows, cols = 3H]: each value read and written once."""
+    n = rows * cols
+    return traffic([n * esize, cols * esize], [n * esize])
+
+
+def qkv_bwd_bytes(rows: int, cols: int, esize: int) -> float:
+    n = rows * cols
+    return traffic([n * esize], [n * esize, cols * esize])
+
+
+def adam_bytes(n: int, esize: int) -> float:
+    """Trainer update: parameters and gradients in the storage dtype, FP32 moments."""
+    return traffic([n * esize, n * esize, 4 * n, 4 * n], [n * esize, 4 * n, 4 * n])
+
+
 def layer_step_bytes(tokens: int, hidden: int, ffn: int, batch: int, heads: int, seq: int,
                      esize: int, key_len=None, causal=False) -> Dict[str, float]:
     """Algorithmic bytes of every operator of one layer's forward and backward

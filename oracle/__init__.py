@@ -67,6 +67,8 @@ def _load():
         "or_set_num_threads": (None, [cint]),
         "or_adam_update": (None, [i64, P, P, P, P, f64, f64, f64, f64, f64, i64, f64, P, P, P]),
         "or_bias_reshape_qkv_fwd": (None, [i64, i64, i64, i64, P, P, P]),
+        "or_cross_entropy_fwd": (None, [i64, i64, P, P, f64, ctypes.c_int32, P, P]),
+        "or_cross_entropy_bwd": (None, [i64, i64, P, P, P, f64, ctypes.c_int32, P]),
         "or_softmax_dropout_fwd": (None, [i64, i64, i64, i64, P, P, cint, f32, u64, u64, P, P, P]),
         "or_softmax_dropout_bwd": (None, [i64, i64, i64, i64, P, P, P, P, cint, f32, P]),
         "or_bias_reshape_qkv_bwd": (None, [i64, i64, i64, i64, P, P, P]),
@@ -267,4 +269,26 @@ def softmax_dropout_bwd(y, dy_drop, mask, key_len, causal, p):
     _load().or_softmax_dropout_bwd(b, h, lq, lk, _ptr(yy), _ptr(dd), _ptr(w), _ptr(kl),
                                    int(bool(causal)), float(p), _ptr(dx))
     return dx
+
+
+def cross_entropy_fwd(logits, target, eps=0.0, ignore_index=-100):
+    """Returns (loss [rows], lse [rows]) for logits [rows, V] and int targets."""
+    z = _f64(logits)
+    rows, V = z.shape
+    t = np.ascontiguousarray(np.asarray(target, dtype=np.int32))
+    loss, lse = np.empty(rows), np.empty(rows)
+    _load().or_cross_entropy_fwd(rows, V, _ptr(z), _ptr(t), float(eps), int(ignore_index),
+                                 _ptr(loss), _ptr(lse))
+    return loss, lse
+
+
+def cross_entropy_bwd(logits, target, dloss=None, eps=0.0, ignore_index=-100):
+    z = _f64(logits)
+    rows, V = z.shape
+    t = np.ascontiguousarray(np.asarray(target, dtype=np.int32))
+    g = None if dloss is None else _f64(dloss)
+    dz = np.empty_like(z)
+    _load().or_cross_entropy_bwd(rows, V, _ptr(z), _ptr(t), _ptr(g), float(eps),
+                                 int(ignore_index), _ptr(dz))
+    return dz
 

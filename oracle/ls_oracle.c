@@ -25,6 +25,11 @@
  *  Bias + reshape of Q, K, V: [L10] section "Technique 1: kernel fusion"
  *         (slide p.12 lists "add bias + reshape Q, K, V" as one fused
  *         elementwise kernel next to the QKV projection GEMM).
+ *  Cross entropy: [L10] section "Technique 1: kernel fusion" (slide p.12 names
+ *         cross entropy among the custom reduce kernels); its single-pass
+ *         normaliser is the online softmax of [CS336] section 6.2 (the pages
+ *         give no criterion formula: the oracle writes the textbook one, with
+ *         optional label smoothing, Szegedy et al., CVPR 2016).
  *  Trainer update: [L10] section "Technique 3: mixed precision" (slide p.29)
  *         and [LS2] section 2.3 (one update over the FP16 parameter/gradient
  *         workspace, computed in FP32 registers); the update rule is Adam
@@ -446,6 +451,64 @@ void or_softmax_dropout_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t
             const int64_t i = row * k_len + j;
             const double g = get_bit(mask_words, i) ? dy_drop[i] * scale : 0.0;
             dx[i] = (j < v) ? yr[j] * (g - dot) : 0.0;
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Cross entropy over vocabulary rows ([L10] technique 1, the criterion      */
+/* reduce kernel), by the definitions.  Row t with target y:                  */
+/*   lse = log sum_j exp(z_j);  p_j = exp(z_j - lse);                         */
+/*   loss = (1-eps) (lse - z_y) + eps (lse - mean_j z_j);                     */
+/*   dz_j = dloss * (p_j - (1-eps) [j == y] - eps / V).                        */
+/* A target equal to ignore_index, or outside [0, V), gives loss 0 and dz 0. */
+/* ------------------------------------------------------------------------- */
+static double row_lse(const double* z, int64_t V) {
+    double m = -INFINITY;
+    for (int64_t j = 0; j < V; ++j)
+        if (z[j] > m) m = z[j];
+    double s = 0.0;
+    for (int64_t j = 0; j < V; ++j) s += exp(z[j] - m);
+    return m + log(s);
+}
+
+static int target_ok(int32_t y, int64_t V, int32_t ignore_index) {
+    return y != ignore_index && y >= 0 && (int64_t)y < V;
+}
+
+void or_cross_entropy_fwd(int64_t rows, int64_t V, const double* logits, const int32_t* target,
+                          double eps, int32_t ignore_index, double* loss, double* lse) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < rows; ++t) {
+        const double* z = logits + t * V;
+        const double l = row_lse(z, V);
+        if (lse) lse[t] = l;
+        if (!target_ok(target[t], V, ignore_index)) {
+            loss[t] = 0.0;
+            continue;
+        }
+        double mean = 0.0;
+        for (int64_t j = 0; j < V; ++j) mean += z[j];
+        mean /= (double)V;
+        loss[t] = (1.0 - eps) * (l - z[target[t]]) + eps * (l - mean);
+    }
+}
+
+void or_cross_entropy_bwd(int64_t rows, int64_t V, const double* logits, const int32_t* target,
+                          const double* dloss, double eps, int32_t ignore_index, double* dlogits) {
+#pragma omp parallel for schedule(static)
+    for (int64_t t = 0; t < rows; ++t) {
+        const double* z = logits + t * V;
+        double* dz = dlogits + t * V;
+        if (!target_ok(target[t], V, ignore_index)) {
+            for (int64_t j = 0; j < V; ++j) dz[j] = 0.0;
+            continue;
+        }
+        const double l = row_lse(z, V);
+        const double g = dloss ? dloss[t] : 1.0;
+        for (int64_t j = 0; j < V; ++j) {
+            const double q = (j == target[t] ? 1.0 - eps : 0.0) + eps / (double)V;
+            dz[j] = g * (exp(z[j] - l) - q);
         }
     }
 }

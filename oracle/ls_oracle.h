@@ -84,6 +84,16 @@ void or_softmax_dropout_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t
                             const double* y, const double* dy_drop, const uint32_t* mask_words,
                             const int32_t* key_len, int causal, float p, double* dx);
 
+/* Cross entropy over rows of V logits with integer targets and label
+ * smoothing eps: loss[t] = (1-eps)(lse - z[y]) + eps(lse - mean(z)), lse =
+ * log sum exp(z) (also returned when lse != NULL); the backward gives
+ * dz = dloss[t] (softmax(z) - (1-eps) onehot(y) - eps/V) (dloss NULL: 1).
+ * Targets equal to ignore_index or outside [0, V) give loss 0 and dz 0. */
+void or_cross_entropy_fwd(int64_t rows, int64_t V, const double* logits, const int32_t* target,
+                          double eps, int32_t ignore_index, double* loss, double* lse);
+void or_cross_entropy_bwd(int64_t rows, int64_t V, const double* logits, const int32_t* target,
+                          const double* dloss, double eps, int32_t ignore_index, double* dlogits);
+
 /* Bias + reshape of the fused QKV projection output: qkv [batch*seq, 3*heads*d]
  * (per row: Q, K, V, each heads x d) plus bias [3*heads*d] into
  * out [3, batch, heads, seq, d]:

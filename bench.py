@@ -931,10 +931,18 @@ def run_next_ops(args):
          "mask": torch.empty((B * h * S * S + 31) // 32, dtype=torch.int32, device=dev),
          "dy_drop": rn(B, h, S, S), "dx": torch.empty(B, h, S, S, dtype=dt, device=dev),
          "key_len": torch.from_numpy(kl_np).to(dev) if kl_np is not None else None}
+    V = synth.CRITERION_VOCAB[L.name]
+    t["logits"] = rn(T, V, std=2.0)
+    t["target"] = torch.randint(0, V, (T,), generator=g, device=dev, dtype=torch.int32)
+    t["loss"] = torch.empty(T, dtype=torch.float32, device=dev)
+    t["lse"] = torch.empty(T, dtype=torch.float32, device=dev)
+    t["dloss"] = torch.ones(T, dtype=torch.float32, device=dev)
+    t["dlogits"] = torch.empty(T, V, dtype=dt, device=dev)
     ws = ls_ops.new_workspace([(T, 3 * H)], device=dev)
     p = L.p
     ls_ops.ls_softmax_dropout_fwd(t["y"], t["y_drop"], t["mask"], t["scores"], t["key_len"],
                                   L.causal, p, 0, 9)
+    ls_ops.ls_cross_entropy_fwd(t["loss"], t["lse"], t["logits"], t["target"], 0.1)
     torch.cuda.synchronize()
     sm = dict(batch=B, heads=h, q_len=S, k_len=S, esize=es, key_len=kl_np, causal=L.causal)
     ops = {
@@ -951,6 +959,13 @@ def run_next_ops(args):
             ls_ops.ls_softmax_dropout_bwd(c["dx"], c["y"], c["dy_drop"], c["mask"],
                                           c["key_len"], L.causal, p),
             accounting.softmax_dropout_bwd_bytes(**sm)),
+        "cross_entropy_fwd": (["logits", "loss", "lse"], lambda c: lambda:
+            ls_ops.ls_cross_entropy_fwd(c["loss"], c["lse"], c["logits"], c["target"], 0.1),
+            accounting.cross_entropy_fwd_bytes(T, V, es)),
+        "cross_entropy_bwd": (["logits", "dlogits"], lambda c: lambda:
+            ls_ops.ls_cross_entropy_bwd(c["dlogits"], c["logits"], c["target"], c["lse"],
+                                        c["dloss"], 0.1),
+            accounting.cross_entropy_bwd_bytes(T, V, es)),
     }
     peak, peak_kind = load_peaks()
     rep = {}
@@ -962,7 +977,7 @@ def run_next_ops(args):
     line = {"metric": "next operators: achieved HBM GB/s per operator", "unit": "GB/s",
             "peak": peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
             "config": {"workload": L.name, "tokens": T, "hidden": H, "heads": h, "seq_len": S,
-                       "dropout_p": p, "storage": L.dtype,
+                       "vocab": V, "dropout_p": p, "storage": L.dtype,
                        "l2": "rotating cloned buffer sets >= 3 x L2"},
             "per_op": rep}
     print(json.dumps(line), flush=True)

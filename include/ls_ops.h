@@ -228,6 +228,28 @@ ls_status ls_softmax_dropout_bwd(ls_dtype dtype, void* dx, const void* y, const 
                                  int64_t q_len, int64_t k_len, const int32_t* key_len, int causal,
                                  float p, void* stream);
 
+/* Cross entropy over vocabulary rows ("CMU 11-868 L10 (LightSeq)", technique 1,
+ * slide p.12: one of the custom reduce kernels; its normaliser is the online
+ * softmax of "CS336 Lecture 5: GPU", section 6.2, so each row is read once).
+ * logits: [rows, vocab] (vocab a multiple of 8; pad the vocabulary), target:
+ * int32 [rows] on the device.  Per row, with lse = log sum_j exp(z_j) and label
+ * smoothing eps in [0, 1):
+ *   loss = (1 - eps) * (lse - z[target]) + eps * (lse - mean_j z_j)
+ * loss and lse (nullable; the backward needs it) are FP32 [rows].  A target
+ * equal to ignore_index, or outside [0, vocab), gives loss 0. */
+ls_status ls_cross_entropy_fwd(ls_dtype dtype, float* loss, float* lse, const void* logits,
+                               const int32_t* target, int64_t rows, int64_t vocab,
+                               float label_smoothing, int32_t ignore_index, void* stream);
+
+/* Backward of the above, from the forward's lse:
+ *   dlogits = dloss[row] * (exp(z - lse) - (1 - eps) * onehot(target) - eps / vocab)
+ * dloss: FP32 [rows], or NULL for 1.  Ignored rows get a zero gradient.
+ * dlogits may be logits (in place). */
+ls_status ls_cross_entropy_bwd(ls_dtype dtype, void* dlogits, const void* logits,
+                               const int32_t* target, const float* lse, const float* dloss,
+                               int64_t rows, int64_t vocab, float label_smoothing,
+                               int32_t ignore_index, void* stream);
+
 /* Bias + reshape of Q, K, V ("CMU 11-868 L10 (LightSeq)", technique 1,
  * slide p.12: one fused elementwise kernel after the QKV projection GEMM).
  * qkv: [batch*seq, 3*H] row-major, H = heads*head_dim, row b*seq + l holding

@@ -43,7 +43,7 @@ def lib():
 
 def test_library_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 19
+    assert len(names) == 21
     assert set(names) == set(ls_ops.EXPORTS)
     out = subprocess.run(["nm", "-D", "--defined-only", lsbuild.LIB], capture_output=True,
                          text=True, check=True).stdout
@@ -243,3 +243,22 @@ def test_softmax_dropout_argument_errors(lib):
     assert bwd(m=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
     assert bwd(dx=B + 16) == ls_ops.LS_ERR_INVALID_ARGUMENT     # dx partly over y
     assert bwd(lq=0) == ls_ops.LS_OK
+
+
+def test_cross_entropy_argument_errors(lib):
+    def fwd(loss=A, lse=B, z=C, t=D, rows=4, V=64, eps=0.0, dtype=F16):
+        return st("ls_cross_entropy_fwd", dtype, loss, lse, z, t, rows, V, eps, -100, S)
+
+    def bwd(dz=A, z=B, t=C, lse=D, g=E, rows=4, V=64, eps=0.1):
+        return st("ls_cross_entropy_bwd", F16, dz, z, t, lse, g, rows, V, eps, -100, S)
+
+    assert fwd(V=60) == ls_ops.LS_ERR_MISALIGNED
+    assert fwd(V=0) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(eps=1.0) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(t=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(t=D + 2) == ls_ops.LS_ERR_MISALIGNED
+    assert fwd(lse=A) == ls_ops.LS_ERR_INVALID_ARGUMENT          # lse is loss
+    assert fwd(rows=0, loss=None) == ls_ops.LS_OK
+    assert bwd(lse=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert bwd(dz=B + 16) == ls_ops.LS_ERR_INVALID_ARGUMENT       # dlogits partly over logits
+    assert bwd(rows=-1) == ls_ops.LS_ERR_INVALID_ARGUMENT

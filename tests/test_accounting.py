@@ -92,4 +92,7 @@ def test_next_operator_bytes_by_hand():
     kl = np.array([8], dtype=np.int32)
     assert acc.softmax_dropout_fwd_bytes(1, 1, 2, 16, 2, kl) == 16 * 2 + 4 + 2 * 32 * 2 + 4
     assert acc.softmax_dropout_bwd_bytes(1, 1, 2, 16, 2, kl) == 2 * 16 * 2 + 2 + 4 + 32 * 2
+    # Cross entropy over [3, 64]: the logits once (+ per-row FP32/int32 values).
+    assert acc.cross_entropy_fwd_bytes(3, 64, 2) == 3 * 64 * 2 + 12 + 24
+    assert acc.cross_entropy_bwd_bytes(3, 64, 2) == 2 * 3 * 64 * 2 + 36
 

@@ -128,6 +128,16 @@ def qkv_bwd_bytes(rows: int, cols: int, esize: int) -> float:
     return traffic([n * esize], [n * esize, cols * esize])
 
 
+def cross_entropy_fwd_bytes(rows: int, vocab: int, esize: int) -> float:
+    """Logits and targets in; loss and lse (FP32) out."""
+    return traffic([rows * vocab * esize, 4 * rows], [8 * rows])
+
+
+def cross_entropy_bwd_bytes(rows: int, vocab: int, esize: int) -> float:
+    """Logits, targets, lse and the upstream gradient in; logit gradients out."""
+    return traffic([rows * vocab * esize, 12 * rows], [rows * vocab * esize])
+
+
 def adam_bytes(n: int, esize: int) -> float:
     """Trainer update: parameters and gradients in the storage dtype, FP32 moments."""
     return traffic([n * esize, n * esize, 4 * n, 4 * n], [n * esize, 4 * n, 4 * n])

@@ -630,5 +630,72 @@ ls_status ls_softmax_dropout_bwd(ls_dtype dtype, void* dx, const void* y, const 
                      "ls_softmax_dropout_bwd launch");
 }
 
+static ls_status ce_common(const char* fn, ls_dtype dtype, int64_t rows, int64_t vocab,
+                           float eps, ls::DType* dt) {
+    LS_TRY(check_dtype(dtype, dt));
+    if (rows < 0) return fail(LS_ERR_INVALID_ARGUMENT, "%s: rows = %lld < 0", fn, (long long)rows);
+    if (vocab <= 0)
+        return fail(LS_ERR_INVALID_ARGUMENT, "%s: vocab = %lld <= 0", fn, (long long)vocab);
+    if (vocab % 8 != 0)
+        return fail(LS_ERR_MISALIGNED, "%s: vocab = %lld is not a multiple of 8", fn,
+                    (long long)vocab);
+    if (vocab > (int64_t{1} << 28) || rows >= (int64_t{1} << 31))
+        return fail(LS_ERR_UNSUPPORTED_SHAPE, "%s: %lld rows of %lld logits too large", fn,
+                    (long long)rows, (long long)vocab);
+    if (!(eps >= 0.f && eps < 1.f))
+        return fail(LS_ERR_INVALID_ARGUMENT, "%s: label_smoothing = %g is not in [0, 1)", fn,
+                    (double)eps);
+    return LS_OK;
+}
+
+ls_status ls_cross_entropy_fwd(ls_dtype dtype, float* loss, float* lse, const void* logits,
+                               const int32_t* target, int64_t rows, int64_t vocab,
+                               float label_smoothing, int32_t ignore_index, void* stream) {
+    ls::DType dt;
+    LS_TRY(ce_common("ls_cross_entropy_fwd", dtype, rows, vocab, label_smoothing, &dt));
+    if (rows == 0) return ok();
+    LS_TRY(check_ptr(loss, "loss", true));
+    LS_TRY(check_ptr(lse, "lse", false));
+    LS_TRY(check_ptr(logits, "logits", true));
+    if (!target) return fail(LS_ERR_INVALID_ARGUMENT, "target is NULL");
+    if (reinterpret_cast<uintptr_t>(target) & 3u)
+        return fail(LS_ERR_MISALIGNED, "target is not 4-byte aligned");
+    const size_t rb = static_cast<size_t>(rows) * 4;
+    const Span outs[] = {{"loss", loss, rb}, {"lse", lse, rb}};
+    const Span ins[] = {{"logits", logits, static_cast<size_t>(rows * vocab) * elem_size(dt)},
+                        {"target", target, rb}};
+    LS_TRY(check_overlaps(outs, 2, ins, 2));
+    return from_cuda(ls::launch_cross_entropy_fwd(dt, loss, lse, logits, target, rows, vocab,
+                                                  label_smoothing, ignore_index,
+                                                  static_cast<cudaStream_t>(stream)),
+                     "ls_cross_entropy_fwd launch");
+}
+
+ls_status ls_cross_entropy_bwd(ls_dtype dtype, void* dlogits, const void* logits,
+                               const int32_t* target, const float* lse, const float* dloss,
+                               int64_t rows, int64_t vocab, float label_smoothing,
+                               int32_t ignore_index, void* stream) {
+    ls::DType dt;
+    LS_TRY(ce_common("ls_cross_entropy_bwd", dtype, rows, vocab, label_smoothing, &dt));
+    if (rows == 0) return ok();
+    LS_TRY(check_ptr(dlogits, "dlogits", true));
+    LS_TRY(check_ptr(logits, "logits", true));
+    LS_TRY(check_ptr(lse, "lse", true));
+    LS_TRY(check_ptr(dloss, "dloss", false));
+    if (!target) return fail(LS_ERR_INVALID_ARGUMENT, "target is NULL");
+    if (reinterpret_cast<uintptr_t>(target) & 3u)
+        return fail(LS_ERR_MISALIGNED, "target is not 4-byte aligned");
+    const size_t rb = static_cast<size_t>(rows) * 4;
+    const size_t nb = static_cast<size_t>(rows * vocab) * elem_size(dt);
+    const Span outs[] = {{"dlogits", dlogits, nb}};
+    const Span ins[] = {{"logits", logits, nb}, {"target", target, rb}, {"lse", lse, rb},
+                        {"dloss", dloss, rb}};
+    LS_TRY(check_overlaps(outs, 1, ins, 4));
+    return from_cuda(ls::launch_cross_entropy_bwd(dt, dlogits, logits, target, lse, dloss, rows,
+                                                  vocab, label_smoothing, ignore_index,
+                                                  static_cast<cudaStream_t>(stream)),
+                     "ls_cross_entropy_bwd launch");
+}
+
 }  // extern "C"
 #pragma GCC visibility pop

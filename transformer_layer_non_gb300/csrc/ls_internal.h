@@ -80,6 +80,15 @@ cudaError_t launch_qkv_fwd(DType dt, void* out, const void* qkv, const void* bia
 cudaError_t launch_qkv_bwd(DType dt, void* dqkv, float* partial, const void* dout, int64_t batch,
                            int64_t seq, int64_t heads, int64_t d, cudaStream_t s);
 
+// Cross entropy over rows of `vocab` logits (vocab % 8 == 0), one CTA per row.
+cudaError_t launch_cross_entropy_fwd(DType dt, float* loss, float* lse, const void* logits,
+                                     const int32_t* target, int64_t rows, int64_t vocab,
+                                     float eps, int32_t ignore_index, cudaStream_t s);
+cudaError_t launch_cross_entropy_bwd(DType dt, void* dlogits, const void* logits,
+                                     const int32_t* target, const float* lse, const float* dloss,
+                                     int64_t rows, int64_t vocab, float eps, int32_t ignore_index,
+                                     cudaStream_t s);
+
 // Trainer update (Adam with decoupled weight decay) over a flat workspace.
 struct AdamHyper {
     float lr, beta1, beta2, eps, weight_decay, grad_scale;

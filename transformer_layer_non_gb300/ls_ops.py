@@ -37,6 +37,7 @@ EXPORTS = (
     "ls_layernorm_bwd_noalloc", "ls_check_device_errors", "ls_adam_update",
     "ls_bias_reshape_qkv_fwd", "ls_bias_reshape_qkv_bwd",
     "ls_softmax_dropout_fwd", "ls_softmax_dropout_bwd",
+    "ls_cross_entropy_fwd", "ls_cross_entropy_bwd",
 )
 
 
@@ -69,6 +70,9 @@ _SIGNATURES = {
     "ls_layernorm_bwd_noalloc": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
     "ls_softmax_fwd": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
+    "ls_cross_entropy_fwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _F32, ctypes.c_int32, _P]),
+    "ls_cross_entropy_bwd": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _F32, ctypes.c_int32,
+                                    _P]),
     "ls_softmax_dropout_fwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT,
                                       _F32, _U64, _U64, _P]),
     "ls_softmax_dropout_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT,
@@ -299,4 +303,22 @@ def ls_softmax_dropout_bwd(dx, y, dy_drop, mask_bits, key_len=None, causal: bool
     _check(load().ls_softmax_dropout_bwd(_dtype_code(y), _ptr(dx), _ptr(y), _ptr(dy_drop),
                                          _ptr(mask_bits), b, h, lq, lk, _ptr(key_len),
                                          int(bool(causal)), p, _stream(stream)))
+
+
+def ls_cross_entropy_fwd(loss, lse, logits, target, label_smoothing: float = 0.0,
+                         ignore_index: int = -100, stream=None):
+    """Per-row loss (FP32 [rows]) and lse (FP32 [rows] or None) of logits
+    [rows, vocab] against int32 targets [rows]."""
+    rows, vocab = logits.shape
+    _check(load().ls_cross_entropy_fwd(_dtype_code(logits), _ptr(loss), _ptr(lse), _ptr(logits),
+                                       _ptr(target), rows, vocab, label_smoothing, ignore_index,
+                                       _stream(stream)))
+
+
+def ls_cross_entropy_bwd(dlogits, logits, target, lse, dloss=None, label_smoothing: float = 0.0,
+                         ignore_index: int = -100, stream=None):
+    rows, vocab = logits.shape
+    _check(load().ls_cross_entropy_bwd(_dtype_code(logits), _ptr(dlogits), _ptr(logits),
+                                       _ptr(target), _ptr(lse), _ptr(dloss), rows, vocab,
+                                       label_smoothing, ignore_index, _stream(stream)))
 

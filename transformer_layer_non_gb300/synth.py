@@ -156,3 +156,10 @@ def trainer_state(n: int, seed: int = 0, dtype: str = "f16", device="cpu"):
     m = draw(1e-3)
     v = draw(1e-2) ** 2
     return p, gr, m, v
+
+
+# Criterion workloads: the BERT-base (30522) and GPT-2 (50257) vocabularies,
+# padded to a multiple of 8 as the vectorised kernels need (30528, 50264).
+CRITERION_VOCAB = {"bert-base": 30528, "gpt2-large": 50264, "transformer-base": 32000,
+                   "tiny": 64}
+

@@ -67,6 +67,8 @@ def _load():
         "or_set_num_threads": (None, [cint]),
         "or_adam_update": (None, [i64, P, P, P, P, f64, f64, f64, f64, f64, i64, f64, P, P, P]),
         "or_bias_reshape_qkv_fwd": (None, [i64, i64, i64, i64, P, P, P]),
+        "or_embedding_fwd": (None, [i64, i64, i64, i64, P, P, P, f64, f32, u64, u64, P, P]),
+        "or_embedding_bwd": (None, [i64, i64, i64, P, P, P, f64, f32, P]),
         "or_cross_entropy_fwd": (None, [i64, i64, P, P, f64, ctypes.c_int32, P, P]),
         "or_cross_entropy_bwd": (None, [i64, i64, P, P, P, f64, ctypes.c_int32, P]),
         "or_softmax_dropout_fwd": (None, [i64, i64, i64, i64, P, P, cint, f32, u64, u64, P, P, P]),
@@ -291,4 +293,30 @@ def cross_entropy_bwd(logits, target, dloss=None, eps=0.0, ignore_index=-100):
     _load().or_cross_entropy_bwd(rows, V, _ptr(z), _ptr(t), _ptr(g), float(eps),
                                  int(ignore_index), _ptr(dz))
     return dz
+
+
+def embedding_fwd(tokens, E, P, batch, seq, s, p, seed, offset):
+    """Returns (y [batch*seq, H], mask words) of the embedding layer."""
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32)).ravel()
+    e, pp = _f64(E), _f64(P)
+    vocab, H = e.shape
+    assert t.size == batch * seq and pp.shape[0] >= seq and pp.shape[1] == H
+    y = np.empty((batch * seq, H))
+    w = np.zeros(mask_words(y.size), dtype=np.uint32)
+    _load().or_embedding_fwd(batch, seq, H, vocab, _ptr(t), _ptr(e), _ptr(pp), float(s),
+                             float(p), int(seed), int(offset), _ptr(y), _ptr(w))
+    return y, w
+
+
+def embedding_bwd(tokens, dy, mask, vocab, s, p, dE=None):
+    """dE [vocab, H] (float64) after adding the gradient of every token
+    (starting from zeros, or from a copy of dE)."""
+    t = np.ascontiguousarray(np.asarray(tokens, dtype=np.int32)).ravel()
+    g = _f64(dy)
+    T, H = g.shape
+    out = np.zeros((vocab, H)) if dE is None else _f64(dE).copy()
+    w = np.ascontiguousarray(np.asarray(mask, dtype=np.uint32))
+    _load().or_embedding_bwd(T, H, vocab, _ptr(t), _ptr(g), _ptr(w), float(s), float(p),
+                             _ptr(out))
+    return out
 

@@ -30,6 +30,9 @@
  *         normaliser is the online softmax of [CS336] section 6.2 (the pages
  *         give no criterion formula: the oracle writes the textbook one, with
  *         optional label smoothing, Szegedy et al., CVPR 2016).
+ *  Embedding: [LS2] section 2.1.2 (token and position embeddings, scaled,
+ *         dropped out; the backward adds every position's gradient of a
+ *         token into its row of the table).
  *  Trainer update: [L10] section "Technique 3: mixed precision" (slide p.29)
  *         and [LS2] section 2.3 (one update over the FP16 parameter/gradient
  *         workspace, computed in FP32 registers); the update rule is Adam
@@ -509,6 +512,48 @@ void or_cross_entropy_bwd(int64_t rows, int64_t V, const double* logits, const i
         for (int64_t j = 0; j < V; ++j) {
             const double q = (j == target[t] ? 1.0 - eps : 0.0) + eps / (double)V;
             dz[j] = g * (exp(z[j] - l) - q);
+        }
+    }
+}
+
+/* ------------------------------------------------------------------------- */
+/* Embedding layer ([LS2] 2.1.2), by the definitions.  Token i = b*seq + l    */
+/* with id w = tokens[i] at position l:                                       */
+/*   y[i, :] = bit(i*H + c) * (s * E[w, c] + P[l, c]) / (1 - p)               */
+/* (keep bits over the flat index of y, as for the other dropouts), and the  */
+/* backward adds  s * bit * dy[i, c] / (1 - p)  into dE[w, c] for every i,    */
+/* in increasing i.  Token ids outside [0, vocab) give a zero row and no      */
+/* gradient.                                                                  */
+/* ------------------------------------------------------------------------- */
+void or_embedding_fwd(int64_t batch, int64_t seq, int64_t H, int64_t vocab,
+                      const int32_t* tokens, const double* E, const double* P, double s,
+                      float p, uint64_t seed, uint64_t offset, double* y, uint32_t* mask_words) {
+    const uint32_t thr = or_dropout_threshold(p);
+    const double scale = 1.0 / (1.0 - (double)p);
+    const int64_t T = batch * seq;
+    memset(mask_words, 0, (size_t)mask_word_count(T * H) * sizeof(uint32_t));
+    for (int64_t i = 0; i < T; ++i) {
+        const int64_t l = i % seq, w = tokens[i];
+        for (int64_t c = 0; c < H; ++c) {
+            const int64_t k = i * H + c;
+            const int bit = keep_bit(seed, offset, (uint64_t)k, thr);
+            if (bit) mask_words[k >> 5] |= 1u << (k & 31);
+            const double v = (w >= 0 && w < vocab) ? s * E[w * H + c] + P[l * H + c] : 0.0;
+            y[k] = bit ? v * scale : 0.0;
+        }
+    }
+}
+
+void or_embedding_bwd(int64_t T, int64_t H, int64_t vocab, const int32_t* tokens,
+                      const double* dy, const uint32_t* mask_words, double s, float p,
+                      double* dE) {
+    const double scale = 1.0 / (1.0 - (double)p);
+    for (int64_t i = 0; i < T; ++i) {
+        const int64_t w = tokens[i];
+        if (w < 0 || w >= vocab) continue;
+        for (int64_t c = 0; c < H; ++c) {
+            const int64_t k = i * H + c;
+            if (get_bit(mask_words, k)) dE[w * H + c] += s * dy[k] * scale;
         }
     }
 }

@@ -84,6 +84,18 @@ void or_softmax_dropout_bwd(int64_t batch, int64_t heads, int64_t q_len, int64_t
                             const double* y, const double* dy_drop, const uint32_t* mask_words,
                             const int32_t* key_len, int causal, float p, double* dx);
 
+/* Embedding layer: y[i] = bit * (s * E[tokens[i]] + P[i % seq]) / (1 - p) for
+ * the batch*seq tokens i (y: [batch*seq, H]; keep bits over the flat index of
+ * y; ids outside [0, vocab) give zero rows).  The backward adds
+ * s * bit * dy / (1 - p) of every token into dE[tokens[i]] (dE: [vocab, H],
+ * accumulated into, token order increasing). */
+void or_embedding_fwd(int64_t batch, int64_t seq, int64_t H, int64_t vocab,
+                      const int32_t* tokens, const double* E, const double* P, double s,
+                      float p, uint64_t seed, uint64_t offset, double* y, uint32_t* mask_words);
+void or_embedding_bwd(int64_t T, int64_t H, int64_t vocab, const int32_t* tokens,
+                      const double* dy, const uint32_t* mask_words, double s, float p,
+                      double* dE);
+
 /* Cross entropy over rows of V logits with integer targets and label
  * smoothing eps: loss[t] = (1-eps)(lse - z[y]) + eps(lse - mean(z)), lse =
  * log sum exp(z) (also returned when lse != NULL); the backward gives

@@ -938,11 +938,24 @@ def run_next_ops(args):
     t["lse"] = torch.empty(T, dtype=torch.float32, device=dev)
     t["dloss"] = torch.ones(T, dtype=torch.float32, device=dev)
     t["dlogits"] = torch.empty(T, V, dtype=dt, device=dev)
+    ev = synth.EMBEDDING_VOCAB[L.name]
+    t["tokens"] = torch.randint(0, ev, (T,), generator=g, device=dev, dtype=torch.int32)
+    t["emb_E"] = rn(ev, H)
+    t["emb_P"] = rn(S, H)
+    t["emb_y"] = torch.empty(T, H, dtype=dt, device=dev)
+    t["emb_mask"] = torch.empty((T * H + 31) // 32, dtype=torch.int32, device=dev)
+    t["emb_dy"] = rn(T, H)
+    t["emb_dE"] = torch.zeros(ev, H, dtype=torch.float32, device=dev)
+    t["emb_ws"] = torch.empty(ls_ops.embedding_workspace_bytes(T), dtype=torch.uint8, device=dev)
+    unique = int(torch.unique(t["tokens"]).numel())
     ws = ls_ops.new_workspace([(T, 3 * H)], device=dev)
     p = L.p
     ls_ops.ls_softmax_dropout_fwd(t["y"], t["y_drop"], t["mask"], t["scores"], t["key_len"],
                                   L.causal, p, 0, 9)
     ls_ops.ls_cross_entropy_fwd(t["loss"], t["lse"], t["logits"], t["target"], 0.1)
+    emb_s = float(H) ** 0.5
+    ls_ops.ls_embedding_fwd(t["emb_y"], t["emb_mask"], t["tokens"], t["emb_E"], t["emb_P"], B, S,
+                            emb_s, p, 0, 10)
     torch.cuda.synchronize()
     sm = dict(batch=B, heads=h, q_len=S, k_len=S, esize=es, key_len=kl_np, causal=L.causal)
     ops = {
@@ -959,6 +972,14 @@ def run_next_ops(args):
             ls_ops.ls_softmax_dropout_bwd(c["dx"], c["y"], c["dy_drop"], c["mask"],
                                           c["key_len"], L.causal, p),
             accounting.softmax_dropout_bwd_bytes(**sm)),
+        "embedding_fwd": (["tokens", "emb_y", "emb_mask"], lambda c: lambda:
+            ls_ops.ls_embedding_fwd(c["emb_y"], c["emb_mask"], c["tokens"], c["emb_E"],
+                                    c["emb_P"], B, S, emb_s, p, 0, 10),
+            accounting.embedding_fwd_bytes(T, S, H, es)),
+        "embedding_bwd": (["emb_dy", "emb_mask", "tokens", "emb_dE"], lambda c: lambda:
+            ls_ops.ls_embedding_bwd(c["emb_dE"], c["emb_dy"], c["emb_mask"], c["tokens"], B, S,
+                                    emb_s, p, workspace=c["emb_ws"]),
+            accounting.embedding_bwd_bytes(T, unique, H, es)),
         "cross_entropy_fwd": (["logits", "loss", "lse"], lambda c: lambda:
             ls_ops.ls_cross_entropy_fwd(c["loss"], c["lse"], c["logits"], c["target"], 0.1),
             accounting.cross_entropy_fwd_bytes(T, V, es)),
@@ -977,7 +998,7 @@ def run_next_ops(args):
     line = {"metric": "next operators: achieved HBM GB/s per operator", "unit": "GB/s",
             "peak": peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
             "config": {"workload": L.name, "tokens": T, "hidden": H, "heads": h, "seq_len": S,
-                       "vocab": V, "dropout_p": p, "storage": L.dtype,
+                       "vocab": V, "embedding_vocab": ev, "dropout_p": p, "storage": L.dtype,
                        "l2": "rotating cloned buffer sets >= 3 x L2"},
             "per_op": rep}
     print(json.dumps(line), flush=True)

@@ -228,6 +228,34 @@ ls_status ls_softmax_dropout_bwd(ls_dtype dtype, void* dx, const void* y, const 
                                  int64_t q_len, int64_t k_len, const int32_t* key_len, int causal,
                                  float p, void* stream);
 
+/* Embedding layer ("LightSeq2", section 2.1.2).  tokens: int32 [batch*seq]
+ * ids (token i = b*seq + l sits at position l); token_table E: [vocab, hidden];
+ * pos_table P: [max_positions >= seq, hidden]; y: [batch*seq, hidden]:
+ *   y[i] = bit(i*hidden + c) * (scale * E[tokens[i]] + P[l]) / (1 - p)
+ * with the keep bits of the other dropouts over the flat index of y, stored
+ * in mask_bits (nullable; the backward needs it).  An id outside [0, vocab)
+ * gives a zero row.  hidden must be a multiple of 8. */
+ls_status ls_embedding_fwd(ls_dtype dtype, void* y, uint32_t* mask_bits, const int32_t* tokens,
+                           const void* token_table, const void* pos_table, int64_t batch,
+                           int64_t seq, int64_t hidden, int64_t vocab, int64_t max_positions,
+                           float scale, float p, uint64_t seed, uint64_t offset, void* stream);
+
+/* Workspace bytes ls_embedding_bwd needs for `tokens` tokens (8 per token). */
+size_t ls_embedding_workspace_bytes(int64_t tokens);
+
+/* Backward of the above into the token table's gradient, FP32 [vocab, hidden],
+ * ACCUMULATED INTO (zero it first for a fresh gradient):
+ *   d_token_table[w] += scale / (1 - p) * sum over tokens i with id w of bit * dy[i]
+ * The sum is deterministic (the pages use atomicAdd): the ids are sorted on
+ * the device, then every id's rows are added in token order by one warp, so
+ * the result is the same bits on every run.  At most 16384 tokens per call
+ * (calls on one stream accumulate in order).  The position table gets no
+ * gradient (the pages' formula has none). */
+ls_status ls_embedding_bwd(ls_dtype dtype, float* d_token_table, const void* dy,
+                           const uint32_t* mask_bits, const int32_t* tokens, int64_t batch,
+                           int64_t seq, int64_t hidden, int64_t vocab, float scale, float p,
+                           void* workspace, size_t workspace_bytes, void* stream);
+
 /* Cross entropy over vocabulary rows ("CMU 11-868 L10 (LightSeq)", technique 1,
  * slide p.12: one of the custom reduce kernels; its normaliser is the online
  * softmax of "CS336 Lecture 5: GPU", section 6.2, so each row is read once).

@@ -43,7 +43,7 @@ def lib():
 
 def test_library_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 21
+    assert len(names) == 24
     assert set(names) == set(ls_ops.EXPORTS)
     out = subprocess.run(["nm", "-D", "--defined-only", lsbuild.LIB], capture_output=True,
                          text=True, check=True).stdout
@@ -262,3 +262,24 @@ def test_cross_entropy_argument_errors(lib):
     assert bwd(lse=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
     assert bwd(dz=B + 16) == ls_ops.LS_ERR_INVALID_ARGUMENT       # dlogits partly over logits
     assert bwd(rows=-1) == ls_ops.LS_ERR_INVALID_ARGUMENT
+
+
+def test_embedding_argument_errors(lib):
+    def fwd(y=A, m=B, tok=C, E=D, P=E, b=2, s=16, h=64, v=100, mp=16, p=0.1):
+        return st("ls_embedding_fwd", F16, y, m, tok, E, P, b, s, h, v, mp, 1.0, p, 0, 0, S)
+
+    def bwd(dE=A, dy=B, m=C, tok=D, b=2, s=16, h=64, v=100, ws=E, wsb=1 << 20):
+        return st("ls_embedding_bwd", F16, dE, dy, m, tok, b, s, h, v, 1.0, 0.1, ws, wsb, S)
+
+    assert ls_ops.embedding_workspace_bytes(32) == 256
+    assert fwd(h=60) == ls_ops.LS_ERR_MISALIGNED
+    assert fwd(mp=8) == ls_ops.LS_ERR_INVALID_ARGUMENT           # positions shorter than seq
+    assert fwd(tok=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(tok=C + 2) == ls_ops.LS_ERR_MISALIGNED
+    assert fwd(p=1.5) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert fwd(y=D) == ls_ops.LS_ERR_INVALID_ARGUMENT            # y over the token table
+    assert fwd(b=0, y=None) == ls_ops.LS_OK
+    assert bwd(wsb=255) == ls_ops.LS_ERR_WORKSPACE_TOO_SMALL
+    assert bwd(m=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert bwd(b=1024, s=17) == ls_ops.LS_ERR_UNSUPPORTED_SHAPE   # > 16384 tokens in one call
+    assert bwd(ws=A + 64) == ls_ops.LS_ERR_INVALID_ARGUMENT       # workspace inside dE

@@ -95,4 +95,7 @@ def test_next_operator_bytes_by_hand():
     # Cross entropy over [3, 64]: the logits once (+ per-row FP32/int32 values).
     assert acc.cross_entropy_fwd_bytes(3, 64, 2) == 3 * 64 * 2 + 12 + 24
     assert acc.cross_entropy_bwd_bytes(3, 64, 2) == 2 * 3 * 64 * 2 + 36
+    # Embedding: 10 tokens of width 16 at seq 5, 4 distinct ids.
+    assert acc.embedding_fwd_bytes(10, 5, 16, 2) == 40 + 320 + 160 + 320 + 20
+    assert acc.embedding_bwd_bytes(10, 4, 16, 2) == 40 + 320 + 20 + 2 * 256
 

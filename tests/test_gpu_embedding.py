@@ -1,0 +1,65 @@
+"""GPU parity: the embedding layer against the FP64 oracle through the C ABI.
+Forward: keep bits bit-exact, values within |err| <= 2e-3 + 2e-3*|ref|.
+Backward (a deterministic scatter-add into an FP32 table gradient): within
+the same bound and within 1e-5 relative, bit-identical from run to run, and
+accumulated into what the table gradient held.  Cases: the layer shapes with
+BERT/GPT-2 vocabularies, a tiny vocabulary (long runs of repeated ids),
+ragged token counts and ids outside the table."""
+import numpy as np
+import pytest
+
+import oracle
+from tests.gpu_util import Guarded, assert_close, dev, f64, require_gpu, tdtype
+from transformer_layer_non_gb300 import ls_ops, synth
+
+torch = pytest.importorskip("torch")
+pytestmark = pytest.mark.gpu
+
+P_DROP, SEED, OFF = 0.1, 99, 4
+
+
+def _case(B, L, H, V, dtype, seed=0, bad_ids=False):
+    rng = np.random.default_rng(seed)
+    tok = rng.integers(0, V, B * L).astype(np.int32)
+    if bad_ids:
+        tok[::13] = -1
+        tok[5::17] = V + 3
+    E = synth.normal(seed, f"emb{V}x{H}/E", (V, H), 0.0, 1.0, dtype)
+    P = synth.normal(seed, f"emb{L}x{H}/P", (L + 2, H), 0.0, 1.0, dtype)
+    dy = synth.normal(seed, f"emb{B}x{L}x{H}/dy", (B * L, H), 0.0, 1.0, dtype)
+    return tok, E, P, dy
+
+
+@pytest.mark.parametrize("B,L,H,V,dtype,bad", [
+    (2, 16, 64, 50, "f32", False),
+    (3, 37, 24, 5, "f16", True),        # 111 tokens, 5 ids: long runs
+    (8, 512, 768, 30522, "f16", False),  # BERT-base
+    (4, 1024, 1280, 50257, "f16", True),  # GPT-2-large, some ids outside the table
+])
+def test_forward_and_backward(B, L, H, V, dtype, bad):
+    require_gpu()
+    tok, E, P, dy = _case(B, L, H, V, dtype, seed=H, bad_ids=bad)
+    s = float(np.sqrt(H))
+    T = B * L
+    y = Guarded((T, H), tdtype(E.dtype))
+    m = Guarded(((T * H + 31) // 32,), torch.int32)
+    ls_ops.ls_embedding_fwd(y.t, m.t, dev(tok), dev(E), dev(P), B, L, s, P_DROP, SEED, OFF)
+    torch.cuda.synchronize()
+    y.check()
+    m.check()
+    ry, rw = oracle.embedding_fwd(tok, E, P, B, L, float(np.float32(s)), P_DROP, SEED, OFF)
+    np.testing.assert_array_equal(m.t.cpu().numpy().view(np.uint32), rw, "keep bits")
+    assert_close(f64(y.t), ry, "y")
+
+    base = synth.normal(1, f"emb{V}x{H}/dE0", (V, H), 0.0, 0.01, "f32")
+    ws = torch.empty(ls_ops.embedding_workspace_bytes(T), dtype=torch.uint8, device="cuda")
+    outs = []
+    for _ in range(2):
+        dE = dev(base)
+        ls_ops.ls_embedding_bwd(dE, dev(dy), m.t, dev(tok), B, L, s, P_DROP, workspace=ws)
+        torch.cuda.synchronize()
+        outs.append(dE.cpu().numpy())
+    np.testing.assert_array_equal(outs[0], outs[1])  # deterministic
+    ref = oracle.embedding_bwd(tok, dy, rw, V, float(np.float32(s)), P_DROP, dE=base)
+    assert_close(outs[0].astype(np.float64), ref, "dE")
+    np.testing.assert_allclose(outs[0], ref, rtol=1e-5, atol=1e-5)

@@ -138,6 +138,20 @@ def cross_entropy_bwd_bytes(rows: int, vocab: int, esize: int) -> float:
     return traffic([rows * vocab * esize, 12 * rows], [rows * vocab * esize])
 
 
+def embedding_fwd_bytes(tokens: int, seq: int, hidden: int, esize: int) -> float:
+    """Ids in; one token-table row per token and the position table once in;
+    y and its mask bits out."""
+    return traffic([4 * tokens, tokens * hidden * esize, seq * hidden * esize],
+                   [tokens * hidden * esize, tokens * hidden * MASK_BYTES_PER_ELEM])
+
+
+def embedding_bwd_bytes(tokens: int, unique: int, hidden: int, esize: int) -> float:
+    """dy, its mask bits and the ids in; each touched FP32 table-gradient row
+    read and written once."""
+    return traffic([4 * tokens, tokens * hidden * esize, tokens * hidden * MASK_BYTES_PER_ELEM,
+                    4 * unique * hidden], [4 * unique * hidden])
+
+
 def adam_bytes(n: int, esize: int) -> float:
     """Trainer update: parameters and gradients in the storage dtype, FP32 moments."""
     return traffic([n * esize, n * esize, 4 * n, 4 * n], [n * esize, 4 * n, 4 * n])

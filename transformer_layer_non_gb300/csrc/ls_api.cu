@@ -697,5 +697,96 @@ ls_status ls_cross_entropy_bwd(ls_dtype dtype, void* dlogits, const void* logits
                      "ls_cross_entropy_bwd launch");
 }
 
+static ls_status emb_common(const char* fn, ls_dtype dtype, int64_t batch, int64_t seq,
+                            int64_t hidden, int64_t vocab, float scale, ls::DType* dt) {
+    LS_TRY(check_dtype(dtype, dt));
+    if (batch < 0 || seq < 0 || vocab < 0)
+        return fail(LS_ERR_INVALID_ARGUMENT, "%s: negative batch/seq/vocab", fn);
+    LS_TRY(check_shape(batch * seq, hidden, kMaxDropoutCols));
+    if (seq > INT32_MAX || vocab > INT32_MAX)
+        return fail(LS_ERR_UNSUPPORTED_SHAPE, "%s: seq or vocab too large", fn);
+    if (!isfinite(scale)) return fail(LS_ERR_INVALID_ARGUMENT, "%s: scale is not finite", fn);
+    return LS_OK;
+}
+
+ls_status ls_embedding_fwd(ls_dtype dtype, void* y, uint32_t* mask_bits, const int32_t* tokens,
+                           const void* token_table, const void* pos_table, int64_t batch,
+                           int64_t seq, int64_t hidden, int64_t vocab, int64_t max_positions,
+                           float scale, float p, uint64_t seed, uint64_t offset, void* stream) {
+    ls::DType dt;
+    LS_TRY(emb_common("ls_embedding_fwd", dtype, batch, seq, hidden, vocab, scale, &dt));
+    ls::DropoutRng rng;
+    LS_TRY(check_p(p, &rng, seed, offset));
+    if (max_positions < seq)
+        return fail(LS_ERR_INVALID_ARGUMENT, "max_positions = %lld < seq = %lld",
+                    (long long)max_positions, (long long)seq);
+    const int64_t T = batch * seq;
+    if (T == 0) return ok();
+    LS_TRY(check_ptr(y, "y", true));
+    LS_TRY(check_ptr(mask_bits, "mask_bits", false));
+    LS_TRY(check_ptr(token_table, "token_table", vocab > 0));
+    LS_TRY(check_ptr(pos_table, "pos_table", true));
+    if (!tokens) return fail(LS_ERR_INVALID_ARGUMENT, "tokens is NULL");
+    if (reinterpret_cast<uintptr_t>(tokens) & 3u)
+        return fail(LS_ERR_MISALIGNED, "tokens is not 4-byte aligned");
+    const size_t es = elem_size(dt);
+    const Span outs[] = {{"y", y, static_cast<size_t>(T * hidden) * es},
+                         {"mask_bits", mask_bits, mask_bytes(T, hidden)}};
+    const Span ins[] = {{"tokens", tokens, static_cast<size_t>(T) * 4},
+                        {"token_table", token_table, static_cast<size_t>(vocab * hidden) * es},
+                        {"pos_table", pos_table, static_cast<size_t>(max_positions * hidden) * es}};
+    LS_TRY(check_overlaps(outs, 2, ins, 3));
+    return from_cuda(ls::launch_embedding_fwd(dt, y, reinterpret_cast<uint8_t*>(mask_bits),
+                                              tokens, token_table, pos_table, batch, seq, hidden,
+                                              vocab, scale, rng,
+                                              static_cast<cudaStream_t>(stream)),
+                     "ls_embedding_fwd launch");
+}
+
+size_t ls_embedding_workspace_bytes(int64_t tokens) {
+    return tokens > 0 ? static_cast<size_t>(tokens) * sizeof(uint64_t) : 0;
+}
+
+ls_status ls_embedding_bwd(ls_dtype dtype, float* d_token_table, const void* dy,
+                           const uint32_t* mask_bits, const int32_t* tokens, int64_t batch,
+                           int64_t seq, int64_t hidden, int64_t vocab, float scale, float p,
+                           void* workspace, size_t workspace_bytes, void* stream) {
+    ls::DType dt;
+    LS_TRY(emb_common("ls_embedding_bwd", dtype, batch, seq, hidden, vocab, scale, &dt));
+    ls::DropoutRng rng;
+    LS_TRY(check_p(p, &rng, 0, 0));
+    const int64_t T = batch * seq;
+    if (T == 0 || vocab == 0) return ok();
+    if (T > ls::kEmbeddingMaxTokens)
+        return fail(LS_ERR_UNSUPPORTED_SHAPE,
+                    "ls_embedding_bwd: %lld tokens in one call; at most %lld (split the batch: "
+                    "calls on one stream accumulate in order)",
+                    (long long)T, (long long)ls::kEmbeddingMaxTokens);
+    LS_TRY(check_ptr(d_token_table, "d_token_table", true));
+    LS_TRY(check_ptr(dy, "dy", true));
+    LS_TRY(check_ptr(mask_bits, "mask_bits", true));
+    LS_TRY(check_ptr(workspace, "workspace", true));
+    if (!tokens) return fail(LS_ERR_INVALID_ARGUMENT, "tokens is NULL");
+    if (reinterpret_cast<uintptr_t>(tokens) & 3u)
+        return fail(LS_ERR_MISALIGNED, "tokens is not 4-byte aligned");
+    if (workspace_bytes < ls_embedding_workspace_bytes(T))
+        return fail(LS_ERR_WORKSPACE_TOO_SMALL, "ls_embedding_bwd: workspace of %zu bytes, need %zu",
+                    workspace_bytes, ls_embedding_workspace_bytes(T));
+    const size_t es = elem_size(dt);
+    const Span outs[] = {{"d_token_table", d_token_table, static_cast<size_t>(vocab * hidden) * 4},
+                         {"workspace", workspace, ls_embedding_workspace_bytes(T)}};
+    const Span ins[] = {{"dy", dy, static_cast<size_t>(T * hidden) * es},
+                        {"mask_bits", mask_bits, mask_bytes(T, hidden)},
+                        {"tokens", tokens, static_cast<size_t>(T) * 4}};
+    LS_TRY(check_overlaps(outs, 2, ins, 3));
+    const float coef = static_cast<float>(static_cast<double>(scale) * rng.scale);
+    return from_cuda(ls::launch_embedding_bwd(dt, d_token_table, dy,
+                                              reinterpret_cast<const uint8_t*>(mask_bits), tokens,
+                                              T, hidden, vocab, coef,
+                                              static_cast<uint64_t*>(workspace),
+                                              static_cast<cudaStream_t>(stream)),
+                     "ls_embedding_bwd launch");
+}
+
 }  // extern "C"
 #pragma GCC visibility pop

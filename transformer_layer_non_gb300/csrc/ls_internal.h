@@ -80,6 +80,18 @@ cudaError_t launch_qkv_fwd(DType dt, void* out, const void* qkv, const void* bia
 cudaError_t launch_qkv_bwd(DType dt, void* dqkv, float* partial, const void* dout, int64_t batch,
                            int64_t seq, int64_t heads, int64_t d, cudaStream_t s);
 
+// Embedding layer: gather + dropout forward; deterministic scatter-add
+// backward into an FP32 dE (one CTA sorts the batch's ids into `sorted`,
+// 8 bytes per token, at most kEmbeddingMaxTokens tokens per call).
+constexpr int64_t kEmbeddingMaxTokens = 16384;
+cudaError_t launch_embedding_fwd(DType dt, void* y, uint8_t* mask, const int32_t* tokens,
+                                 const void* E, const void* P, int64_t batch, int64_t seq,
+                                 int64_t H, int64_t vocab, float s, const DropoutRng& rng,
+                                 cudaStream_t st);
+cudaError_t launch_embedding_bwd(DType dt, float* dE, const void* dy, const uint8_t* mask,
+                                 const int32_t* tokens, int64_t T, int64_t H, int64_t vocab,
+                                 float coef, uint64_t* sorted, cudaStream_t st);
+
 // Cross entropy over rows of `vocab` logits (vocab % 8 == 0), one CTA per row.
 cudaError_t launch_cross_entropy_fwd(DType dt, float* loss, float* lse, const void* logits,
                                      const int32_t* target, int64_t rows, int64_t vocab,

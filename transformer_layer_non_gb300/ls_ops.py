@@ -38,6 +38,7 @@ EXPORTS = (
     "ls_bias_reshape_qkv_fwd", "ls_bias_reshape_qkv_bwd",
     "ls_softmax_dropout_fwd", "ls_softmax_dropout_bwd",
     "ls_cross_entropy_fwd", "ls_cross_entropy_bwd",
+    "ls_embedding_fwd", "ls_embedding_bwd", "ls_embedding_workspace_bytes",
 )
 
 
@@ -70,6 +71,11 @@ _SIGNATURES = {
     "ls_layernorm_bwd_noalloc": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
     "ls_softmax_fwd": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
+    "ls_embedding_fwd": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _F32,
+                                _F32, _U64, _U64, _P]),
+    "ls_embedding_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F32, _F32, _P,
+                                _SZ, _P]),
+    "ls_embedding_workspace_bytes": (_SZ, [_I64]),
     "ls_cross_entropy_fwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _F32, ctypes.c_int32, _P]),
     "ls_cross_entropy_bwd": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _F32, ctypes.c_int32,
                                     _P]),
@@ -321,4 +327,28 @@ def ls_cross_entropy_bwd(dlogits, logits, target, lse, dloss=None, label_smoothi
     _check(load().ls_cross_entropy_bwd(_dtype_code(logits), _ptr(dlogits), _ptr(logits),
                                        _ptr(target), _ptr(lse), _ptr(dloss), rows, vocab,
                                        label_smoothing, ignore_index, _stream(stream)))
+
+
+def ls_embedding_fwd(y, mask_bits, tokens, token_table, pos_table, batch: int, seq: int,
+                     scale: float, p: float, seed: int = 0, offset: int = 0, stream=None):
+    """y [batch*seq, H] = Dropout(scale * E[tokens] + P[positions])."""
+    vocab, hidden = token_table.shape
+    _check(load().ls_embedding_fwd(_dtype_code(token_table), _ptr(y), _ptr(mask_bits),
+                                   _ptr(tokens), _ptr(token_table), _ptr(pos_table), batch, seq,
+                                   hidden, vocab, pos_table.shape[0], scale, p, seed, offset,
+                                   _stream(stream)))
+
+
+def embedding_workspace_bytes(tokens: int) -> int:
+    return int(load().ls_embedding_workspace_bytes(tokens))
+
+
+def ls_embedding_bwd(d_token_table, dy, mask_bits, tokens, batch: int, seq: int, scale: float,
+                     p: float, workspace=None, stream=None):
+    """Adds the token-table gradient (FP32 [vocab, H]) of this batch into d_token_table."""
+    vocab, hidden = d_token_table.shape
+    _check(load().ls_embedding_bwd(_dtype_code(dy), _ptr(d_token_table), _ptr(dy),
+                                   _ptr(mask_bits), _ptr(tokens), batch, seq, hidden, vocab,
+                                   scale, p, _ptr(workspace), _nbytes(workspace),
+                                   _stream(stream)))
 

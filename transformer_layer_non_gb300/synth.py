@@ -162,4 +162,8 @@ def trainer_state(n: int, seed: int = 0, dtype: str = "f16", device="cpu"):
 # padded to a multiple of 8 as the vectorised kernels need (30528, 50264).
 CRITERION_VOCAB = {"bert-base": 30528, "gpt2-large": 50264, "transformer-base": 32000,
                    "tiny": 64}
+# Embedding tables: the unpadded vocabularies (the embedding has no width
+# constraint on the vocabulary).
+EMBEDDING_VOCAB = {"bert-base": 30522, "gpt2-large": 50257, "transformer-base": 32000,
+                   "tiny": 64}
 

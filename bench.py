@@ -980,6 +980,10 @@ def run_next_ops(args):
             ls_ops.ls_embedding_bwd(c["emb_dE"], c["emb_dy"], c["emb_mask"], c["tokens"], B, S,
                                     emb_s, p, workspace=c["emb_ws"]),
             accounting.embedding_bwd_bytes(T, unique, H, es)),
+        "embedding_bwd_atomic": (["emb_dy", "emb_mask", "tokens", "emb_dE"], lambda c: lambda:
+            ls_ops.ls_embedding_bwd(c["emb_dE"], c["emb_dy"], c["emb_mask"], c["tokens"], B, S,
+                                    emb_s, p, deterministic=False),
+            accounting.embedding_bwd_bytes(T, unique, H, es)),
         "cross_entropy_fwd": (["logits", "loss", "lse"], lambda c: lambda:
             ls_ops.ls_cross_entropy_fwd(c["loss"], c["lse"], c["logits"], c["target"], 0.1),
             accounting.cross_entropy_fwd_bytes(T, V, es)),

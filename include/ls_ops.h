@@ -246,15 +246,18 @@ size_t ls_embedding_workspace_bytes(int64_t tokens);
 /* Backward of the above into the token table's gradient, FP32 [vocab, hidden],
  * ACCUMULATED INTO (zero it first for a fresh gradient):
  *   d_token_table[w] += scale / (1 - p) * sum over tokens i with id w of bit * dy[i]
- * The sum is deterministic (the pages use atomicAdd): the ids are sorted on
- * the device, then every id's rows are added in token order by one warp, so
- * the result is the same bits on every run.  At most 16384 tokens per call
- * (calls on one stream accumulate in order).  The position table gets no
- * gradient (the pages' formula has none). */
+ * deterministic == 0: the pages' method, float atomic adds (one pass; the
+ * order of the additions, so the last bits, vary from run to run; no
+ * workspace).  deterministic != 0: the ids are sorted on the device and every
+ * id's rows are added in token order by one warp, the same bits on every run
+ * (workspace of ls_embedding_workspace_bytes(batch*seq) bytes; at most 16384
+ * tokens per call, calls on one stream accumulate in order).  The position
+ * table gets no gradient (the pages' formula has none). */
 ls_status ls_embedding_bwd(ls_dtype dtype, float* d_token_table, const void* dy,
                            const uint32_t* mask_bits, const int32_t* tokens, int64_t batch,
                            int64_t seq, int64_t hidden, int64_t vocab, float scale, float p,
-                           void* workspace, size_t workspace_bytes, void* stream);
+                           int deterministic, void* workspace, size_t workspace_bytes,
+                           void* stream);
 
 /* Cross entropy over vocabulary rows ("CMU 11-868 L10 (LightSeq)", technique 1,
  * slide p.12: one of the custom reduce kernels; its normaliser is the online

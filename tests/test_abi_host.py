@@ -269,7 +269,7 @@ def test_embedding_argument_errors(lib):
         return st("ls_embedding_fwd", F16, y, m, tok, E, P, b, s, h, v, mp, 1.0, p, 0, 0, S)
 
     def bwd(dE=A, dy=B, m=C, tok=D, b=2, s=16, h=64, v=100, ws=E, wsb=1 << 20):
-        return st("ls_embedding_bwd", F16, dE, dy, m, tok, b, s, h, v, 1.0, 0.1, ws, wsb, S)
+        return st("ls_embedding_bwd", F16, dE, dy, m, tok, b, s, h, v, 1.0, 0.1, 1, ws, wsb, S)
 
     assert ls_ops.embedding_workspace_bytes(32) == 256
     assert fwd(h=60) == ls_ops.LS_ERR_MISALIGNED

@@ -63,3 +63,10 @@ def test_forward_and_backward(B, L, H, V, dtype, bad):
     ref = oracle.embedding_bwd(tok, dy, rw, V, float(np.float32(s)), P_DROP, dE=base)
     assert_close(outs[0].astype(np.float64), ref, "dE")
     np.testing.assert_allclose(outs[0], ref, rtol=1e-5, atol=1e-5)
+    # The pages' atomic mode: the same sums up to the order of the additions.
+    dE = dev(base)
+    ls_ops.ls_embedding_bwd(dE, dev(dy), m.t, dev(tok), B, L, s, P_DROP, deterministic=False)
+    torch.cuda.synchronize()
+    got = dE.cpu().numpy()
+    assert_close(got.astype(np.float64), ref, "dE (atomic)")
+    np.testing.assert_allclose(got, ref, rtol=1e-5, atol=1e-5)

@@ -10,8 +10,8 @@
 //
 // Backward: dE[w] += s / (1 - p) * sum over the tokens i with id w of
 // bit * dy[i].  The pages add the rows with atomicAdd, whose order (and so
-// whose rounding) changes from run to run; here the sum is deterministic.  One
-// CTA sorts the (id, index) pairs of the batch in shared memory (a bitonic
+// whose rounding) changes from run to run; that is one mode here (vector
+// float atomics, one pass).  The other mode is deterministic: one CTA sorts the (id, index) pairs of the batch in shared memory (a bitonic
 // sort of unique 64-bit keys, so equal ids stay in index order); then a warp
 // per run of equal ids adds that id's rows in index order and adds the total
 // into dE[w] -- each row of dE has exactly one writer, so no atomics.
@@ -120,6 +120,93 @@ emb_sort_kernel(uint64_t* __restrict__ sorted, const int32_t* __restrict__ token
     for (int k = threadIdx.x; k < T; k += kSortThreads) sorted[k] = keys[k];
 }
 
+// The same sort for n2 <= 4096 with four keys per thread (n2/4 threads):
+// stages whose partners lie in one thread compare in registers, stages whose
+// partners lie in one warp exchange by shuffle, and only the stages with
+// partners 128 or more positions apart go through shared memory -- 15
+// shared-memory stages for 4096 keys instead of 78.
+constexpr int kRegKeys = 4;
+constexpr int kRegSortMax = kSortThreads * kRegKeys;  // 4096
+
+__device__ __forceinline__ void cas(uint64_t& mine, uint64_t other, bool keep_min) {
+    mine = keep_min ? (other < mine ? other : mine) : (other > mine ? other : mine);
+}
+
+__global__ void __launch_bounds__(kSortThreads)
+emb_sort_reg_kernel(uint64_t* __restrict__ sorted, const int32_t* __restrict__ tokens, int T,
+                    int n2, int64_t vocab) {
+    __shared__ uint64_t keys[kRegSortMax];
+    pdl_enter();
+    const int t = threadIdx.x;
+    const int lane = t & 31;
+    uint64_t k[kRegKeys];
+#pragma unroll
+    for (int q = 0; q < kRegKeys; ++q) {
+        const int p = kRegKeys * t + q;
+        uint64_t key = ~uint64_t{0};
+        if (p < T) {
+            const int32_t w = tokens[p];
+            const uint32_t id = (w >= 0 && static_cast<int64_t>(w) < vocab)
+                                    ? static_cast<uint32_t>(w)
+                                    : 0xFFFFFFFFu;
+            key = (static_cast<uint64_t>(id) << 32) | static_cast<uint32_t>(p);
+        }
+        k[q] = key;
+    }
+    for (int size = 2; size <= n2; size <<= 1) {
+        for (int stride = size >> 1; stride > 0; stride >>= 1) {
+            if (stride < kRegKeys) {
+                // partners in this thread: (0,1),(2,3) or (0,2),(1,3); the
+                // direction is that of the pair's lower position
+                auto cx = [&](uint64_t& a, uint64_t& b, int q_lo) {
+                    const bool up = ((kRegKeys * t + q_lo) & size) == 0;
+                    if ((a > b) == up) {
+                        const uint64_t c = a;
+                        a = b;
+                        b = c;
+                    }
+                };
+                if (stride == 1) {
+                    cx(k[0], k[1], 0);
+                    cx(k[2], k[3], 2);
+                } else {
+                    cx(k[0], k[2], 0);
+                    cx(k[1], k[3], 1);
+                }
+            } else if (stride < 32 * kRegKeys) {
+                // partners in this warp: lane ^ (stride / kRegKeys), same slot
+                const int lm = stride / kRegKeys;
+#pragma unroll
+                for (int q = 0; q < kRegKeys; ++q) {
+                    const int p = kRegKeys * t + q;
+                    const uint64_t other = __shfl_xor_sync(0xffffffffu, k[q], lm);
+                    const bool lower = (p & stride) == 0, up = (p & size) == 0;
+                    cas(k[q], other, lower == up);
+                }
+            } else {
+                // partners in other warps: through shared memory
+#pragma unroll
+                for (int q = 0; q < kRegKeys; ++q) keys[kRegKeys * t + q] = k[q];
+                __syncthreads();
+#pragma unroll
+                for (int q = 0; q < kRegKeys; ++q) {
+                    const int p = kRegKeys * t + q;
+                    const uint64_t other = keys[p ^ stride];
+                    const bool lower = (p & stride) == 0, up = (p & size) == 0;
+                    cas(k[q], other, lower == up);
+                }
+                __syncthreads();
+            }
+        }
+    }
+    (void)lane;
+#pragma unroll
+    for (int q = 0; q < kRegKeys; ++q) {
+        const int p = kRegKeys * t + q;
+        if (p < T) sorted[p] = k[q];
+    }
+}
+
 struct EmbBwdArgs {
     int T;
     int nvr;     // H / 8
@@ -166,6 +253,42 @@ emb_accum_kernel(float* __restrict__ dE, const T* __restrict__ dy,
         d1.z = fmaf(a.coef, acc[6], d1.z); d1.w = fmaf(a.coef, acc[7], d1.w);
         *reinterpret_cast<float4*>(dst) = d0;
         *reinterpret_cast<float4*>(dst + 4) = d1;
+    }
+}
+
+// The pages' backward: every masked, scaled gradient vector is added into its
+// table row with vector float atomics (fast, but the order of the additions,
+// and so the rounding, varies from run to run).
+template <typename T, typename I>
+__global__ void __launch_bounds__(kThreads)
+emb_atomic_kernel(float* __restrict__ dE, const T* __restrict__ dy,
+                  const uint8_t* __restrict__ mask, const int32_t* __restrict__ tokens,
+                  uint64_t nv, int64_t vocab, float coef, const __grid_constant__ FastDiv by_nvr) {
+    pdl_enter();
+    const I n = static_cast<I>(nv);
+    const I S = static_cast<I>(gridDim.x) * kThreads;
+    for (I v = static_cast<I>(blockIdx.x) * kThreads + threadIdx.x; v < n; v += S) {
+        uint64_t i;
+        if (sizeof(I) == 4)
+            i = fdiv(static_cast<uint32_t>(v), by_nvr);
+        else
+            i = static_cast<uint64_t>(v) / by_nvr.d;
+        const uint32_t cv = static_cast<uint32_t>(static_cast<uint64_t>(v) - i * by_nvr.d);
+        const int32_t w = tokens[i];
+        if (w < 0 || static_cast<int64_t>(w) >= vocab) continue;
+        const uint32_t bits = mask[v];
+        if (bits == 0) continue;
+        float g[kVec];
+        load8f<T>(dy + static_cast<size_t>(v) * kVec, g);
+#pragma unroll
+        for (int j = 0; j < kVec; ++j) g[j] = ((bits >> j) & 1u) ? coef * g[j] : 0.f;
+        float* dst = dE + (static_cast<size_t>(w) * by_nvr.d + cv) * kVec;
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst), "f"(g[0]),
+                     "f"(g[1]), "f"(g[2]), "f"(g[3])
+                     : "memory");
+        asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(dst + 4), "f"(g[4]),
+                     "f"(g[5]), "f"(g[6]), "f"(g[7])
+                     : "memory");
     }
 }
 
@@ -218,18 +341,46 @@ cudaError_t launch_embedding_fwd(DType dt, void* y, uint8_t* mask, const int32_t
     return fwd_impl<float>(y, mask, tokens, E, P, batch, seq, H, vocab, s, rng, st);
 }
 
+template <typename T>
+cudaError_t atomic_impl(float* dE, const void* dy, const uint8_t* mask, const int32_t* tokens,
+                        int64_t ntok, int64_t H, int64_t vocab, float coef, cudaStream_t st) {
+    const uint64_t nv = static_cast<uint64_t>(ntok) * static_cast<uint64_t>(H / kVec);
+    static const int occ = occupancy(emb_atomic_kernel<T, uint64_t>);
+    const int64_t want = static_cast<int64_t>((nv + kThreads - 1) / kThreads);
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, int64_t{sm_count()} * occ));
+    const bool narrow = nv + static_cast<uint64_t>(grid) * kThreads < (uint64_t{1} << 31);
+    auto kern = narrow ? emb_atomic_kernel<T, uint32_t> : emb_atomic_kernel<T, uint64_t>;
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, st, dE,
+                      static_cast<const T*>(dy), mask, tokens, nv, vocab, coef,
+                      make_fastdiv(static_cast<uint32_t>(H / kVec)));
+}
+
+cudaError_t launch_embedding_bwd_atomic(DType dt, float* dE, const void* dy, const uint8_t* mask,
+                                        const int32_t* tokens, int64_t T, int64_t H,
+                                        int64_t vocab, float coef, cudaStream_t st) {
+    if (dt == DType::F16) return atomic_impl<__half>(dE, dy, mask, tokens, T, H, vocab, coef, st);
+    return atomic_impl<float>(dE, dy, mask, tokens, T, H, vocab, coef, st);
+}
+
 cudaError_t launch_embedding_bwd(DType dt, float* dE, const void* dy, const uint8_t* mask,
                                  const int32_t* tokens, int64_t T, int64_t H, int64_t vocab,
                                  float coef, uint64_t* sorted, cudaStream_t st) {
     int n2 = 1;
     while (n2 < T) n2 <<= 1;
-    const size_t smem = static_cast<size_t>(n2) * sizeof(uint64_t);
-    cudaError_t e = cudaFuncSetAttribute(emb_sort_kernel,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    e = launch_pdl(emb_sort_kernel, dim3(1), dim3(kSortThreads), smem, st, sorted, tokens,
-                   static_cast<int>(T), n2, vocab);
+    cudaError_t e;
+    if (n2 <= kRegSortMax) {
+        // n2/4 threads, at least one warp (padding keys fill the rest)
+        const int n2r = std::max(n2, 32 * kRegKeys);
+        e = launch_pdl(emb_sort_reg_kernel, dim3(1), dim3(n2r / kRegKeys), 0, st, sorted, tokens,
+                       static_cast<int>(T), n2r, vocab);
+    } else {
+        const size_t smem = static_cast<size_t>(n2) * sizeof(uint64_t);
+        e = cudaFuncSetAttribute(emb_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(smem));
+        if (e != cudaSuccess) return e;
+        e = launch_pdl(emb_sort_kernel, dim3(1), dim3(kSortThreads), smem, st, sorted, tokens,
+                       static_cast<int>(T), n2, vocab);
+    }
     if (e != cudaSuccess) return e;
     EmbBwdArgs a;
     a.T = static_cast<int>(T);

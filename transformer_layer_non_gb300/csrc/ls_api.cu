@@ -750,13 +750,33 @@ size_t ls_embedding_workspace_bytes(int64_t tokens) {
 ls_status ls_embedding_bwd(ls_dtype dtype, float* d_token_table, const void* dy,
                            const uint32_t* mask_bits, const int32_t* tokens, int64_t batch,
                            int64_t seq, int64_t hidden, int64_t vocab, float scale, float p,
-                           void* workspace, size_t workspace_bytes, void* stream) {
+                           int deterministic, void* workspace, size_t workspace_bytes,
+                           void* stream) {
     ls::DType dt;
     LS_TRY(emb_common("ls_embedding_bwd", dtype, batch, seq, hidden, vocab, scale, &dt));
     ls::DropoutRng rng;
     LS_TRY(check_p(p, &rng, 0, 0));
     const int64_t T = batch * seq;
     if (T == 0 || vocab == 0) return ok();
+    if (!deterministic) {
+        LS_TRY(check_ptr(d_token_table, "d_token_table", true));
+        LS_TRY(check_ptr(dy, "dy", true));
+        LS_TRY(check_ptr(mask_bits, "mask_bits", true));
+        if (!tokens) return fail(LS_ERR_INVALID_ARGUMENT, "tokens is NULL");
+        if (reinterpret_cast<uintptr_t>(tokens) & 3u)
+            return fail(LS_ERR_MISALIGNED, "tokens is not 4-byte aligned");
+        const Span outs[] = {
+            {"d_token_table", d_token_table, static_cast<size_t>(vocab * hidden) * 4}};
+        const Span ins[] = {{"dy", dy, static_cast<size_t>(T * hidden) * elem_size(dt)},
+                            {"mask_bits", mask_bits, mask_bytes(T, hidden)},
+                            {"tokens", tokens, static_cast<size_t>(T) * 4}};
+        LS_TRY(check_overlaps(outs, 1, ins, 3));
+        const float c = static_cast<float>(static_cast<double>(scale) * rng.scale);
+        return from_cuda(ls::launch_embedding_bwd_atomic(
+                             dt, d_token_table, dy, reinterpret_cast<const uint8_t*>(mask_bits),
+                             tokens, T, hidden, vocab, c, static_cast<cudaStream_t>(stream)),
+                         "ls_embedding_bwd launch");
+    }
     if (T > ls::kEmbeddingMaxTokens)
         return fail(LS_ERR_UNSUPPORTED_SHAPE,
                     "ls_embedding_bwd: %lld tokens in one call; at most %lld (split the batch: "

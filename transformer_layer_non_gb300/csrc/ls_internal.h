@@ -91,6 +91,9 @@ cudaError_t launch_embedding_fwd(DType dt, void* y, uint8_t* mask, const int32_t
 cudaError_t launch_embedding_bwd(DType dt, float* dE, const void* dy, const uint8_t* mask,
                                  const int32_t* tokens, int64_t T, int64_t H, int64_t vocab,
                                  float coef, uint64_t* sorted, cudaStream_t st);
+cudaError_t launch_embedding_bwd_atomic(DType dt, float* dE, const void* dy, const uint8_t* mask,
+                                        const int32_t* tokens, int64_t T, int64_t H,
+                                        int64_t vocab, float coef, cudaStream_t st);
 
 // Cross entropy over rows of `vocab` logits (vocab % 8 == 0), one CTA per row.
 cudaError_t launch_cross_entropy_fwd(DType dt, float* loss, float* lse, const void* logits,

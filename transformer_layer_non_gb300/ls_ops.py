@@ -73,8 +73,8 @@ _SIGNATURES = {
     "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_embedding_fwd": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _F32,
                                 _F32, _U64, _U64, _P]),
-    "ls_embedding_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F32, _F32, _P,
-                                _SZ, _P]),
+    "ls_embedding_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F32, _F32, _INT,
+                                _P, _SZ, _P]),
     "ls_embedding_workspace_bytes": (_SZ, [_I64]),
     "ls_cross_entropy_fwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _F32, ctypes.c_int32, _P]),
     "ls_cross_entropy_bwd": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _F32, ctypes.c_int32,
@@ -344,11 +344,13 @@ def embedding_workspace_bytes(tokens: int) -> int:
 
 
 def ls_embedding_bwd(d_token_table, dy, mask_bits, tokens, batch: int, seq: int, scale: float,
-                     p: float, workspace=None, stream=None):
-    """Adds the token-table gradient (FP32 [vocab, H]) of this batch into d_token_table."""
+                     p: float, deterministic: bool = True, workspace=None, stream=None):
+    """Adds the token-table gradient (FP32 [vocab, H]) of this batch into
+    d_token_table: deterministically (sorted ids; needs a workspace) or with
+    float atomics."""
     vocab, hidden = d_token_table.shape
     _check(load().ls_embedding_bwd(_dtype_code(dy), _ptr(d_token_table), _ptr(dy),
                                    _ptr(mask_bits), _ptr(tokens), batch, seq, hidden, vocab,
-                                   scale, p, _ptr(workspace), _nbytes(workspace),
-                                   _stream(stream)))
+                                   scale, p, int(bool(deterministic)), _ptr(workspace),
+                                   _nbytes(workspace), _stream(stream)))
 

@@ -265,7 +265,12 @@ __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx
                 unpack(buf.a[k], yf);
                 sub8(buf.b[k], dot, o);
 #pragma unroll
-                for (int j = 0; j < kVec; ++j) o[j] *= yf[j];
+                for (int j = 0; j < kVec; j += 2) {
+                    const float2 t = mul2(make_float2(o[j], o[j + 1]),
+                                          make_float2(yf[j], yf[j + 1]));
+                    o[j] = t.x;
+                    o[j + 1] = t.y;
+                }
             } else if (v * kVec < vlen) {
                 float yf[kVec], df[kVec];
                 unpack(buf.a[k], yf);
@@ -426,18 +431,25 @@ softmax_tma_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, Row
         }
         m = group_max<32>(m);
         const float ml = m == -INFINITY ? 0.f : m * kLog2e;  // empty row: all e = 0
-        float sum = 0.f;
+        // Exponentials and their sum two lanes at a time (packed FP32): the
+        // even and odd elements keep separate partial sums, added at the end.
+        float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
         for (int k2 = 0; k2 < VPT; ++k2) {
             if (vlen > k2 * 32 * kVec) {
 #pragma unroll
-                for (int j = 0; j < kVec; ++j) {
-                    f[k2][j] = exp2_approx(fmaf(f[k2][j], kLog2e, -ml));
-                    sum += f[k2][j];
+                for (int j = 0; j < kVec; j += 2) {
+                    float2 t = fma2(make_float2(f[k2][j], f[k2][j + 1]),
+                                    make_float2(kLog2e, kLog2e), make_float2(-ml, -ml));
+                    t.x = exp2_approx(t.x);
+                    t.y = exp2_approx(t.y);
+                    f[k2][j] = t.x;
+                    f[k2][j + 1] = t.y;
+                    acc = add2(acc, t);
                 }
             }
         }
-        sum = group_sum<32>(sum);
+        float sum = group_sum<32>(acc.x + acc.y);
         const float inv = sum > 0.f ? __fdividef(1.f, sum) : 0.f;
 #pragma unroll
         for (int k2 = 0; k2 < VPT; ++k2) {
@@ -447,7 +459,12 @@ softmax_tma_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, Row
             if (vlen > k2 * 32 * kVec) {
                 float o[kVec];
 #pragma unroll
-                for (int j = 0; j < kVec; ++j) o[j] = f[k2][j] * inv;
+                for (int j = 0; j < kVec; j += 2) {
+                    const float2 t = mul2(make_float2(f[k2][j], f[k2][j + 1]),
+                                          make_float2(inv, inv));
+                    o[j] = t.x;
+                    o[j + 1] = t.y;
+                }
                 store8f<T>(dst, o);
             } else {
                 store8<T>(dst, zero8<T>());

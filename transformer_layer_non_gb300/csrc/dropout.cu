@@ -167,6 +167,7 @@ struct BwdArgs {
     int cols;
     int nbands;
     int64_t ntiles;
+    int late_trigger;  // CTAs loop over several tiles: release dependents at exit
     uint32_t thr;
     float scale;
     PhiloxSchedule ks;
@@ -258,7 +259,10 @@ dropout_bwd_kernel(T* dx, float* __restrict__ partial, const T* dout,
                    const uint8_t* __restrict__ mask, const __grid_constant__ BwdArgs a) {
     __shared__ __align__(16) float red[kBwdRps][kBwdColsPerTile];
     const PhiloxSchedule& ks = a.ks;
-    pdl_enter();
+    // With several tiles per CTA the dependent launch is released as CTAs
+    // exit (measured faster); with one tile per CTA at their start.
+    pdl_wait();
+    if (!a.late_trigger) pdl_trigger();
     int64_t t = blockIdx.x;
     Raw8<T> da[kBwdU], db[kBwdU];
     uint32_t ma[kBwdU], mbb[kBwdU];
@@ -373,6 +377,7 @@ cudaError_t bwd_impl(void* dx, float* partial, const void* dout, const uint8_t* 
     static const int occ_regen = occupancy(dropout_bwd_kernel<T, true>, kThreads, 0);
     const int occ = mask ? occ_mask : occ_regen;
     const int64_t grid = std::min<int64_t>(a.ntiles, int64_t{sm_count()} * occ);
+    a.late_trigger = a.ntiles > grid ? 1 : 0;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
                       static_cast<T*>(dx), partial, static_cast<const T*>(dout), mask, a);
 }

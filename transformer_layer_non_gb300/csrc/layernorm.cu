@@ -336,7 +336,10 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
     WarpRing<S> ring;
     ring.init(reinterpret_cast<uint64_t*>(smem) + warp * S,
               data + static_cast<size_t>(warp) * S * stage_bytes, stage_bytes);
-    pdl_enter();
+    // The dependent launch (the column reduction, whose CTAs need whole SMs)
+    // is released as these CTAs finish rather than at their start, so that
+    // its waiting CTAs do not hold SMs that this grid's CTAs still need.
+    pdl_wait();
     const int nvec = cols / kVec;
     for (int v = threadIdx.x; v < nvec; v += kLnTmaWarps * 32)
         store8<T>(gsm + v * kVec, load8<T>(gamma + v * kVec));

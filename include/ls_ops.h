@@ -94,6 +94,14 @@ int ls_version(void);
 #define LS_DEVERR_WAIT_TIMEOUT 1u
 ls_status ls_check_device_errors(uint32_t* flags);
 
+/* Self-test of that failure path (no counterpart on the pages): enqueues one
+ * warp that waits, with the library's bounded wait, on a barrier that nothing
+ * completes; after `polls` polls (1 .. 2^19, each suspending the warp for up
+ * to about 2 us) it records LS_DEVERR_WAIT_TIMEOUT and exits.  Nothing hangs
+ * and the context stays usable; ls_check_device_errors then reports and
+ * clears the flag. */
+ls_status ls_selftest_wait_timeout(uint32_t polls, void* stream);
+
 /* Workspace bytes that the backward calls with a column reduction
  * (ls_bias_dropout_residual_bwd, ls_bias_relu_dropout_bwd, ls_layernorm_bwd)
  * need for an activation of shape [rows, cols]; enough for all three. */

@@ -43,7 +43,7 @@ def lib():
 
 def test_library_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 24
+    assert len(names) == 25
     assert set(names) == set(ls_ops.EXPORTS)
     out = subprocess.run(["nm", "-D", "--defined-only", lsbuild.LIB], capture_output=True,
                          text=True, check=True).stdout
@@ -283,3 +283,8 @@ def test_embedding_argument_errors(lib):
     assert bwd(m=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
     assert bwd(b=1024, s=17) == ls_ops.LS_ERR_UNSUPPORTED_SHAPE   # > 16384 tokens in one call
     assert bwd(ws=A + 64) == ls_ops.LS_ERR_INVALID_ARGUMENT       # workspace inside dE
+
+
+def test_selftest_argument_errors(lib):
+    assert st("ls_selftest_wait_timeout", 0, S) == ls_ops.LS_ERR_INVALID_ARGUMENT
+    assert st("ls_selftest_wait_timeout", (1 << 19) + 1, S) == ls_ops.LS_ERR_INVALID_ARGUMENT

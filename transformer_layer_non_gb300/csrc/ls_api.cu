@@ -188,6 +188,13 @@ ls_status ls_check_device_errors(uint32_t* flags) {
     return ok();
 }
 
+ls_status ls_selftest_wait_timeout(uint32_t polls, void* stream) {
+    if (polls == 0 || polls > (1u << 19))
+        return fail(LS_ERR_INVALID_ARGUMENT, "polls = %u is not in [1, 2^19]", polls);
+    return from_cuda(ls::launch_wait_timeout_selftest(polls, static_cast<cudaStream_t>(stream)),
+                     "ls_selftest_wait_timeout launch");
+}
+
 size_t ls_colreduce_workspace_bytes(int64_t rows, int64_t cols) {
     if (rows <= 0 || cols <= 0 || cols % 8 != 0) return 0;
     const size_t a = ls::dropout_bwd_plan(rows, cols).bytes();

@@ -115,6 +115,9 @@ cudaError_t launch_adam(DType dt, void* param, const void* grad, float* m, float
 // Read and clear the device-side failure flags of one translation unit's
 // kernels (synchronous).
 cudaError_t softmax_take_device_error(unsigned int* flags);
+// One warp waits (polls bounded polls) on a barrier nothing completes and
+// records LS_DEVERR_WAIT_TIMEOUT in the softmax unit's failure word.
+cudaError_t launch_wait_timeout_selftest(uint32_t polls, cudaStream_t s);
 cudaError_t dropout_take_device_error(unsigned int* flags);
 cudaError_t layernorm_take_device_error(unsigned int* flags);
 

@@ -824,7 +824,28 @@ DropArgs make_drop(void* y_drop, uint8_t* mask, const DropoutRng& rng, uint64_t 
     return d;
 }
 
+// Self-test of the bounded-wait failure path: one warp waits on a barrier
+// that expects one arrival nobody makes.  After `polls` bounded polls it
+// records the timeout in this unit's failure word and returns, as the
+// bulk-copy rings do when a copy never lands.
+__global__ void __launch_bounds__(32) wait_timeout_selftest_kernel(uint32_t polls) {
+    __shared__ __align__(8) uint64_t bar;
+    if (threadIdx.x == 0) {
+        mbar_init(&bar, 1);
+        mbar_init_fence();
+    }
+    __syncwarp();
+    bool done = false;
+    for (uint32_t i = 0; i < polls && !done; ++i) done = mbar_try_wait(&bar, 0);
+    if (!done && threadIdx.x == 0) flag_device_error(kDevErrWaitTimeout);
+}
+
 }  // namespace
+
+cudaError_t launch_wait_timeout_selftest(uint32_t polls, cudaStream_t s) {
+    wait_timeout_selftest_kernel<<<1, 32, 0, s>>>(polls);
+    return cudaGetLastError();
+}
 
 cudaError_t softmax_take_device_error(unsigned int* flags) {
     return take_device_error_word(flags);

@@ -39,6 +39,7 @@ EXPORTS = (
     "ls_softmax_dropout_fwd", "ls_softmax_dropout_bwd",
     "ls_cross_entropy_fwd", "ls_cross_entropy_bwd",
     "ls_embedding_fwd", "ls_embedding_bwd", "ls_embedding_workspace_bytes",
+    "ls_selftest_wait_timeout",
 )
 
 
@@ -71,6 +72,7 @@ _SIGNATURES = {
     "ls_layernorm_bwd_noalloc": (_INT, [_INT, _P, _P, _P, _P, _P, _P, _P, _P, _I64, _I64, _P]),
     "ls_softmax_fwd": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
+    "ls_selftest_wait_timeout": (_INT, [ctypes.c_uint32, _P]),
     "ls_embedding_fwd": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _F32,
                                 _F32, _U64, _U64, _P]),
     "ls_embedding_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F32, _F32, _INT,
@@ -146,6 +148,11 @@ def check_device_errors() -> int:
     v = ctypes.c_uint32(0)
     _check(load().ls_check_device_errors(ctypes.byref(v)))
     return int(v.value)
+
+
+def selftest_wait_timeout(polls: int = 1024, stream=None):
+    """Enqueue the bounded-wait failure self-test (see include/ls_ops.h)."""
+    _check(load().ls_selftest_wait_timeout(polls, _stream(stream)))
 
 
 def _check(status: int):

@@ -601,6 +601,27 @@ def e2e_pipelined(step, host_in, nsteps):
     return f0.elapsed_time(f1) / nsteps
 
 
+FUSED_OPS = {
+    "bias_dropout_residual": ("attn_bdr_fwd", "ffn2_bdr_fwd", "ffn2_bdr_bwd", "attn_bdr_bwd"),
+    "bias_relu_dropout": ("ffn1_brd_fwd", "ffn1_brd_bwd"),
+    "layernorm": ("ln1_fwd", "ln2_fwd", "ln2_bwd", "ln1_bwd"),
+    "softmax": ("softmax_fwd", "softmax_bwd"),
+}
+
+
+def fused_op_summary(ops_report, peak):
+    """Per fused operator, forward and backward together: the sum of its
+    launches' algorithmic bytes over the sum of their times."""
+    out = {}
+    for name, members in FUSED_OPS.items():
+        b = sum(ops_report[m]["bytes"] for m in members)
+        us = sum(ops_report[m]["us"] for m in members)
+        gbs = b / (us * 1e-6) / 1e9
+        out[name] = {"us": round(us, 2), "bytes": int(b), "GB/s": round(gbs, 1),
+                     "frac": round(gbs / peak, 4)}
+    return out
+
+
 def run_ours(args):
     import torch
 
@@ -715,6 +736,7 @@ def run_ours(args):
         "pct_of_peak": round(value / world / peak * 100, 2),
         "tokens_per_s": round(layer.tokens * world / (ms_step * 1e-3), 1),
         "per_op": ops_report,
+        "per_fused_op": fused_op_summary(ops_report, peak),
         "per_op_note": "us: the operator alone, back to back over rotating L2-cold buffer "
                        "sets (CUDA events); in_step_events_us: between CUDA events recorded "
                        "around it inside the running step, which also stop the overlap of "

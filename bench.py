@@ -37,6 +37,10 @@ DEFAULT_WORKLOAD = "bert-base"
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 SWEEP_K_LENS = (16, 32, 64, 128, 256, 512, 1024, 2048, 4096)
+# Rows past the on-chip limit (two-pass online softmax), on 2^26 elements so
+# that even the longest rows give one CTA per row for every SM several times.
+SWEEP_LONG_K_LENS = (16384, 32768, 65536, 262144)
+SWEEP_LONG_ELEMENTS = 1 << 26
 
 
 def parse_args():
@@ -64,8 +68,9 @@ def parse_args():
                     help="time the fused trainer update (Adam) over the BERT-base parameter "
                          "workspace; one JSON line")
     ap.add_argument("--sweep", action="store_true",
-                    help="time the softmax row-length sweep (k_len 16..4096, 2^22 elements "
-                         "each, random valid lengths) forward and backward; one JSON line")
+                    help="time the softmax row-length sweep (k_len 16..4096 on 2^22 elements, "
+                         "16384..262144 on 2^26, random valid lengths) forward and backward; "
+                         "one JSON line")
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -817,8 +822,10 @@ def run_sweep(args):
     dev = torch.device("cuda", 0)
     peak, peak_kind = load_peaks()
     rows_out = {}
-    for k_len in SWEEP_K_LENS:
-        x, dy, kl = synth.sweep_inputs(k_len, args.seed)
+    cases = [(k, synth.SWEEP_ELEMENTS) for k in SWEEP_K_LENS]
+    cases += [(k, SWEEP_LONG_ELEMENTS) for k in SWEEP_LONG_K_LENS]
+    for k_len, elements in cases:
+        x, dy, kl = synth.sweep_inputs(k_len, args.seed, elements)
         b, h, q, k = x.shape
         t = {"x": torch.from_numpy(x).to(dev), "dy": torch.from_numpy(dy).to(dev),
              "kl": torch.from_numpy(kl).to(dev), "y": torch.empty(x.shape, dtype=torch.float16,
@@ -843,10 +850,13 @@ def run_sweep(args):
             res[d] = {"us": round(ms * 1e3, 2), "bytes": int(nbytes[d]), "GB/s": round(gbs, 1),
                       "frac": round(gbs / peak, 4), "buffer_sets": nsets}
             del sets, thunks
+        res["elements"] = int(x.size)
         rows_out[str(k_len)] = res
     line = {"metric": "softmax sweep: achieved HBM GB/s per row length", "unit": "GB/s",
             "peak": peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
-            "config": {"workload": "softmax-sweep", "elements": synth.SWEEP_ELEMENTS,
+            "config": {"workload": "softmax-sweep",
+                       "elements": {"k_len <= 4096": synth.SWEEP_ELEMENTS,
+                                    "k_len >= 16384": SWEEP_LONG_ELEMENTS},
                        "valid_len": "U[1, k_len] per row", "storage": "f16",
                        "l2": "rotating cloned buffer sets >= 3 x L2"},
             "k_len": rows_out}

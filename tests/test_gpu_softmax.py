@@ -4,7 +4,9 @@ oracle, |err| <= 2e-3 + 2e-3*|ref|; masked entries must be exactly zero.
 Full layer sizes run on the GPU in one call (the launch the benchmark times);
 the oracle checks every (batch, head) slice of the smaller layers and a sample
 of slices of the larger ones.  The shape sweep (k_len 16..4096, 2^22 elements,
-random valid length per row) is checked on every element."""
+random valid length per row) is checked on every element; rows longer than
+16384 keys (the two-pass online path) up to 2^18 on every element of a few
+rows."""
 import numpy as np
 import pytest
 
@@ -118,7 +120,8 @@ def test_sweep_every_element(k_len):
 @pytest.mark.parametrize("shape,causal", [
     ((2, 2, 8, 8192), False), ((1, 2, 3, 16384), True), ((3, 2, 5, 24), True),
     ((2, 3, 7, 40), False), ((2, 1, 9, 264), True), ((1, 1, 300, 1032), True),
-    ((2, 2, 16, 8), True)])
+    ((2, 2, 16, 8), True), ((1, 2, 3, 16392), True), ((2, 1, 2, 65536), False),
+    ((1, 1, 2, 262144), True)])
 def test_odd_lengths_and_masks(dtype, shape, causal):
     # k_len classes between the sweep points, q_len != k_len with the causal
     # diagonal, and key lengths that are 0, negative, 1, or past k_len.
@@ -147,6 +150,24 @@ def test_no_mask_and_in_place():
     ls_ops.ls_softmax_bwd(dyt, dev(y16), dyt)  # dx over dy
     torch.cuda.synchronize()
     assert_close(f64(dyt), oracle.softmax_bwd(y16, dy), "in-place dx")
+
+
+def test_long_rows_in_place():
+    # Rows past the on-chip limit are read twice; in place, the second pass
+    # must still see the inputs (each thread rewrites only what it reads).
+    require_gpu()
+    shape = (1, 2, 2, 32768)
+    x = synth.normal(11, "sml/x", shape, 0.0, 3.0, "f16")
+    dy = synth.normal(11, "sml/dy", shape, 0.0, 1.0, "f16")
+    kl = np.array([20001], dtype=np.int32)
+    ry = oracle.softmax_fwd(x, kl, True)
+    y = run_fwd(x, kl, True, in_place=True)
+    assert_close(f64(y), ry, "long in-place y")
+    y16 = ry.astype(np.float16)
+    dyt = dev(dy)
+    ls_ops.ls_softmax_bwd(dyt, dev(y16), dyt, dev(kl), True)
+    torch.cuda.synchronize()
+    assert_close(f64(dyt), oracle.softmax_bwd(y16, dy, kl, True), "long in-place dx")
 
 
 def test_no_device_side_failures_after_streamed_rows():

@@ -2,7 +2,8 @@
 against the FP64 oracle, every element, through the C ABI.  The dropout bits
 must match bit for bit (keep on valid entries, 0 on masked ones); y, y_drop
 and the backward within |err| <= 2e-3 + 2e-3*|ref|.  Cases cover every
-row-length class of the dispatch (sub-warp, warp and CTA per row), padding
+row-length class of the dispatch (sub-warp, warp and CTA per row, and the
+two-pass rows longer than 16384 keys), padding
 and causal masks, FP16 and FP32, and the BERT-base layer at full size."""
 import numpy as np
 import pytest
@@ -60,7 +61,8 @@ def test_sweep_row_lengths(k_len):
 
 @pytest.mark.parametrize("dtype", ["f16", "f32"])
 @pytest.mark.parametrize("shape,causal", [((2, 3, 5, 24), False), ((1, 2, 7, 136), True),
-                                          ((2, 2, 33, 40), True), ((1, 1, 3, 2056), False)])
+                                          ((2, 2, 33, 40), True), ((1, 1, 3, 2056), False),
+                                          ((1, 1, 3, 65544), True), ((2, 1, 2, 16400), False)])
 def test_odd_shapes_and_masks(dtype, shape, causal):
     require_gpu()
     b = shape[0]

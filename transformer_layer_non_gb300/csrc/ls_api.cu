@@ -407,9 +407,9 @@ static ls_status softmax_common(const char* fn, ls_dtype dtype, int64_t batch, i
     if (k_len <= 0) return fail(LS_ERR_INVALID_ARGUMENT, "%s: k_len = %lld <= 0", fn, (long long)k_len);
     if (k_len % 8 != 0)
         return fail(LS_ERR_MISALIGNED, "%s: k_len = %lld is not a multiple of 8", fn, (long long)k_len);
-    if (k_len > ls::kMaxRowLen)
+    if (k_len > ls::kMaxSoftmaxRowLen)
         return fail(LS_ERR_UNSUPPORTED_SHAPE, "%s: k_len = %lld exceeds %lld", fn,
-                    (long long)k_len, (long long)ls::kMaxRowLen);
+                    (long long)k_len, (long long)ls::kMaxSoftmaxRowLen);
     if (q_len > (int64_t{1} << 30) || batch > (int64_t{1} << 30) || heads > (int64_t{1} << 30))
         return fail(LS_ERR_UNSUPPORTED_SHAPE, "%s: dimension too large", fn);
     const double n = static_cast<double>(batch) * heads * q_len;

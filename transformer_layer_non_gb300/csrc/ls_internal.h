@@ -69,7 +69,8 @@ cudaError_t launch_softmax_dropout_bwd(DType dt, void* dx, const void* y, const 
                                        const uint8_t* mask, const SoftmaxShape& sh, float scale,
                                        cudaStream_t s);
 
-constexpr int64_t kMaxRowLen = 16384;
+constexpr int64_t kMaxRowLen = 16384;          // LayerNorm rows
+constexpr int64_t kMaxSoftmaxRowLen = 1 << 20;  // softmax rows (longer than 16384 stream)
 
 // Bias + reshape of Q, K, V: [batch*seq, 3*heads*d] (+ bias) <-> [3, batch,
 // heads, seq, d].  The backward writes one FP32 partial row of the bias

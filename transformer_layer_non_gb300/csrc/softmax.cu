@@ -13,6 +13,8 @@
 //   32 < nvec <= 128  a warp per row, VPT = 2..4 vectors per lane.
 //   nvec > 128        a CTA per row (4 or 8 warps), partial results of the two
 //                     reductions through shared memory.
+//   nvec > 2048       a CTA per row that reads the row twice: an online
+//                     (maximum, sum) pass, then the output pass.
 // Masked keys are never loaded: a lane loads a vector only if it holds at
 // least one valid key; masked outputs are written as exact zeros.
 #include <math.h>
@@ -625,13 +627,196 @@ softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
 }
 
 // ----------------------------------------------------------------------------
+// Rows longer than registers hold (k_len > 16384): a CTA per row streams the
+// valid prefix twice.  Forward: the first pass keeps each thread's running
+// maximum and its rescaled running sum of exponentials -- the online softmax
+// normaliser of "CS336 Lecture 5: GPU", section 6.2 -- and the CTA merges the
+// pairs by the same rule; the second pass writes y (and the dropout
+// epilogue).  Backward: the first pass sums y*g, the second writes dx.  The
+// row's second read comes from L2 (a row is at most 2 MB).
+// ----------------------------------------------------------------------------
+constexpr int kStreamThreads = 512;
+constexpr int kStreamWarps = kStreamThreads / 32;
+// Vectors per thread in flight: 64 bytes of either storage type.
+template <typename T>
+constexpr int stream_unroll() { return sizeof(T) == 2 ? 4 : 2; }
+
+__device__ __forceinline__ void online_merge(float& m, float& l, float m2, float l2) {
+    const float mm = fmaxf(m, m2);
+    if (mm == -INFINITY) return;  // both empty
+    l = l * exp2_approx((m - mm) * kLog2e) + l2 * exp2_approx((m2 - mm) * kLog2e);
+    m = mm;
+}
+
+// Loads the vectors v0 + u * kStreamThreads (u < U) of a row that
+// hold at least one of its vlen valid elements.
+template <typename T, int U>
+__device__ __forceinline__ void stream_load(Raw8<T> (&r)[U], const T* row_ptr, int v0,
+                                            int vlen) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const int v = v0 + u * kStreamThreads;
+        if (v * kVec < vlen) r[u] = load8<T>(row_ptr + v * kVec);
+    }
+}
+
+template <typename T, bool DROP>
+__global__ void __launch_bounds__(kStreamThreads, 2)
+softmax_fwd_stream_kernel(T* y, const T* x, int k_len, RowMask mk,
+                          const __grid_constant__ DropArgs d) {
+    constexpr int U = stream_unroll<T>();
+    __shared__ float sm_m[kStreamWarps], sm_l[kStreamWarps];
+    pdl_enter();
+    if (DROP) drop_tail(d);
+    const int64_t row = blockIdx.x;
+    const int vlen = valid_len(row, k_len, mk);
+    const int nvec = k_len / kVec;
+    const int64_t base = row * k_len;
+    float m = -INFINITY, l = 0.f;
+    for (int v0 = threadIdx.x; v0 * kVec < vlen; v0 += kStreamThreads * U) {
+        Raw8<T> r[U];
+        stream_load<T, U>(r, x + base, v0, vlen);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * kStreamThreads;
+            const int cnt = min(vlen - v * kVec, kVec);
+            if (cnt <= 0) break;
+            float f[kVec];
+            unpack(r[u], f);
+            float vm = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) vm = fmaxf(vm, j < cnt ? f[j] : -INFINITY);
+            if (vm > m) {  // rescale the running sum to the new maximum
+                l *= exp2_approx((m - vm) * kLog2e);
+                m = vm;
+            }
+            const float ml = m == -INFINITY ? 0.f : m * kLog2e;  // all -inf so far: e = 0
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                l += j < cnt ? exp2_approx(fmaf(f[j], kLog2e, -ml)) : 0.f;
+        }
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        online_merge(m, l, __shfl_xor_sync(0xffffffffu, m, o), __shfl_xor_sync(0xffffffffu, l, o));
+    if ((threadIdx.x & 31) == 0) {
+        sm_m[threadIdx.x >> 5] = m;
+        sm_l[threadIdx.x >> 5] = l;
+    }
+    __syncthreads();
+    float M = sm_m[0], L = sm_l[0];
+    for (int w = 1; w < kStreamWarps; ++w) online_merge(M, L, sm_m[w], sm_l[w]);
+    const float ml = M == -INFINITY ? 0.f : M * kLog2e;
+    const float inv = L > 0.f ? __fdividef(1.f, L) : 0.f;
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += kStreamThreads * U) {
+        Raw8<T> r[U];
+        stream_load<T, U>(r, x + base, v0, vlen);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * kStreamThreads;
+            if (v >= nvec) break;
+            const int cnt = min(max(vlen - v * kVec, 0), kVec);
+            float o[kVec];
+            if (cnt > 0) {
+                float f[kVec];
+                unpack(r[u], f);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j)
+                    o[j] = j < cnt ? exp2_approx(fmaf(f[j], kLog2e, -ml)) * inv : 0.f;
+            } else {
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) o[j] = 0.f;
+            }
+            store8f<T>(y + base + v * kVec, o);
+            if (DROP) drop_store<T>(o, base, v, vlen, d);
+        }
+    }
+}
+
+template <typename T, bool DROP>
+__global__ void __launch_bounds__(kStreamThreads, 2)
+softmax_bwd_stream_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
+                          const __grid_constant__ DropArgs d) {
+    constexpr int U = stream_unroll<T>();
+    __shared__ float red[kStreamWarps];
+    pdl_enter();
+    const int64_t row = blockIdx.x;
+    const int vlen = valid_len(row, k_len, mk);
+    const int nvec = k_len / kVec;
+    const int64_t base = row * k_len;
+    // g = dy, or bit * dy_drop * scale with the fused dropout
+    auto grads = [&](const Raw8<T>& r, uint32_t bits, float (&g)[kVec]) {
+        unpack(r, g);
+        if (DROP) {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) g[j] = ((bits >> j) & 1u) ? g[j] * d.scale : 0.f;
+        }
+    };
+    auto load_bits = [&](uint32_t (&mb)[U], int v0) {
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * kStreamThreads;
+            mb[u] = (DROP && v * kVec < vlen) ? d.mask[(base >> 3) + v] : 0u;
+        }
+    };
+    float dot = 0.f;
+    for (int v0 = threadIdx.x; v0 * kVec < vlen; v0 += kStreamThreads * U) {
+        Raw8<T> ry[U], rg[U];
+        uint32_t mb[U];
+        stream_load<T, U>(ry, y + base, v0, vlen);
+        stream_load<T, U>(rg, dy + base, v0, vlen);
+        load_bits(mb, v0);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * kStreamThreads;
+            const int cnt = min(vlen - v * kVec, kVec);
+            if (cnt <= 0) break;
+            float yf[kVec], g[kVec];
+            unpack(ry[u], yf);
+            grads(rg[u], mb[u], g);
+#pragma unroll
+            for (int j = 0; j < kVec; ++j)
+                if (j < cnt) dot = fmaf(yf[j], g[j], dot);
+        }
+    }
+    dot = cta_sum<kStreamWarps>(dot, red);
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += kStreamThreads * U) {
+        Raw8<T> ry[U], rg[U];
+        uint32_t mb[U];
+        stream_load<T, U>(ry, y + base, v0, vlen);
+        stream_load<T, U>(rg, dy + base, v0, vlen);
+        load_bits(mb, v0);
+#pragma unroll
+        for (int u = 0; u < U; ++u) {
+            const int v = v0 + u * kStreamThreads;
+            if (v >= nvec) break;
+            const int cnt = min(max(vlen - v * kVec, 0), kVec);
+            float o[kVec];
+            if (cnt > 0) {
+                float yf[kVec], g[kVec];
+                unpack(ry[u], yf);
+                grads(rg[u], mb[u], g);
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) o[j] = j < cnt ? yf[j] * (g[j] - dot) : 0.f;
+            } else {
+#pragma unroll
+                for (int j = 0; j < kVec; ++j) o[j] = 0.f;
+            }
+            store8f<T>(dx + base + v * kVec, o);
+        }
+    }
+}
+
+// ----------------------------------------------------------------------------
 // Dispatch by row length.
 // ----------------------------------------------------------------------------
 struct SmPlan {
-    bool cta;
+    bool cta, stream;
     int lpr, vpt, warps;
     int64_t grid;
 };
+
+constexpr int64_t kMaxRegisterRowLen = 16384;  // 8 warps x 8 vectors x 8 elements
 
 SmPlan plan_for(int64_t nrows, int64_t k_len) {
     const int nvec = static_cast<int>(k_len / kVec);
@@ -648,10 +833,13 @@ SmPlan plan_for(int64_t nrows, int64_t k_len) {
         }
         const int64_t rpc = kThreads / p.lpr;
         p.grid = (nrows + rpc - 1) / rpc;
-    } else {
+    } else if (k_len <= kMaxRegisterRowLen) {
         p.cta = true;
         p.warps = nvec <= 512 ? 4 : 8;
         p.vpt = (nvec + p.warps * 32 - 1) / (p.warps * 32);
+        p.grid = nrows;
+    } else {
+        p.stream = true;
         p.grid = nrows;
     }
     return p;
@@ -783,6 +971,10 @@ cudaError_t fwd_dispatch(void* y, const void* x, const SoftmaxShape& sh, const D
     const int k_len = static_cast<int>(sh.k_len);
     const SmPlan p = plan_for(nrows, sh.k_len);
     const RowMask m = make_mask(sh);
+    if (p.stream)
+        return launch_pdl(softmax_fwd_stream_kernel<T, DROP>, dim3(static_cast<unsigned>(p.grid)),
+                          dim3(kStreamThreads), 0, s, static_cast<T*>(y),
+                          static_cast<const T*>(x), k_len, m, d);
     if (!p.cta) {
         LS_SM_GROUP_CASES(fwd_group, LS_SM_T_DROP, y, x, nrows, k_len, m, d, p, s)
     } else {
@@ -797,6 +989,10 @@ cudaError_t bwd_dispatch(void* dx, const void* y, const void* dy, const SoftmaxS
     const int k_len = static_cast<int>(sh.k_len);
     const SmPlan p = plan_for(nrows, sh.k_len);
     const RowMask m = make_mask(sh);
+    if (p.stream)
+        return launch_pdl(softmax_bwd_stream_kernel<T, DROP>, dim3(static_cast<unsigned>(p.grid)),
+                          dim3(kStreamThreads), 0, s, static_cast<T*>(dx),
+                          static_cast<const T*>(y), static_cast<const T*>(dy), k_len, m, d);
     if (!p.cta) {
         LS_SM_GROUP_CASES(bwd_group, LS_SM_T_DROP, dx, y, dy, nrows, k_len, m, d, p, s)
     } else {

@@ -39,7 +39,7 @@ FALLBACK_HBM_GBS = 6800.0
 SWEEP_K_LENS = (16, 32, 64, 128, 256, 512, 1024, 2048, 4096)
 # Rows past the on-chip limit (two-pass online softmax), on 2^26 elements so
 # that even the longest rows give one CTA per row for every SM several times.
-SWEEP_LONG_K_LENS = (16384, 32768, 65536, 262144)
+SWEEP_LONG_K_LENS = (8192, 16384, 32768, 65536, 262144)
 SWEEP_LONG_ELEMENTS = 1 << 26
 
 
@@ -61,6 +61,9 @@ def parse_args():
                          "in layer order) inside the NVTX range 'profile' (for ncu --nvtx "
                          "--nvtx-include profile/); no timing")
     ap.add_argument("--profile-launches", type=int, default=2)
+    ap.add_argument("--reductions", default="side", choices=["side", "inline"],
+                    help="layer step: fork the backward column reductions onto a second "
+                         "stream (side) or keep them on the step's stream (inline)")
     ap.add_argument("--next-ops", action="store_true",
                     help="time the operators beyond the layer step (bias + reshape of Q/K/V, "
                          "softmax with fused dropout) at the workload's shapes; one JSON line")
@@ -69,7 +72,7 @@ def parse_args():
                          "workspace; one JSON line")
     ap.add_argument("--sweep", action="store_true",
                     help="time the softmax row-length sweep (k_len 16..4096 on 2^22 elements, "
-                         "16384..262144 on 2^26, random valid lengths) forward and backward; "
+                         "8192..262144 on 2^26, random valid lengths) forward and backward; "
                          "one JSON line")
     a = ap.parse_args()
     if a.warmup < 3:
@@ -196,7 +199,9 @@ class LayerStep:
         "softmax_bwd": ("probs", "scores_dy", "key_len", "scores_dx"),
     }
 
-    def __init__(self, layer, seed, device):
+    BWD_WITH_REDUCTION = ("ln2_bwd", "ffn2_bdr_bwd", "ffn1_brd_bwd", "ln1_bwd", "attn_bdr_bwd")
+
+    def __init__(self, layer, seed, device, reductions="side"):
         import numpy as np
         import torch
 
@@ -232,17 +237,22 @@ class LayerStep:
         self.outputs = sorted(out)
         self.t = {k: dev(v) for k, v in host.items()}
         self.t.update(out)
-        self.workspace = ls_ops.new_workspace([(T, F), (T, H)], device=device)
+        # Column reductions forked onto a second stream need a workspace per
+        # backward call to overlap the next operator (a shared one is ordered).
+        self.side = torch.cuda.Stream(device=device) if reductions == "side" else None
+        shared = ls_ops.new_workspace([(T, F), (T, H)], device=device)
+        self.ws = {n: (ls_ops.new_workspace([(T, F), (T, H)], device=device) if self.side
+                       else shared) for n in self.BWD_WITH_REDUCTION}
         self.bytes = accounting.layer_step_bytes(T, H, F, L.batch, L.heads, L.seq, self.esize,
                                                  self.key_len_np, L.causal)
         self.launches = {k: 1 for k in self.bytes}
-        for k in ("ln2_bwd", "ffn2_bdr_bwd", "ffn1_brd_bwd", "ln1_bwd", "attn_bdr_bwd"):
+        for k in self.BWD_WITH_REDUCTION:
             self.launches[k] = 2  # main kernel + deterministic column reduction
 
     def ops(self, t=None):
         """(name, thunk) in layer order: forward, then backward in reverse."""
         t = self.t if t is None else t
-        ls, L, ws = self.ls, self.layer, self.workspace
+        ls, L, ws = self.ls, self.layer, self.ws
         kl = t.get("key_len")
         p = L.p
         return [
@@ -259,19 +269,37 @@ class LayerStep:
                                                     t["ln2_x"], t["ln2_gamma"], t["ln2_beta"], 1e-5)),
             ("ln2_bwd", lambda: ls.ls_layernorm_bwd(
                 t["ln2_dx"], t["ln2_dgamma"], t["ln2_dbeta"], t["ln2_dy"], t["ln2_x"],
-                t["ln2_gamma"], t["ln2_mean"], t["ln2_rstd"], workspace=ws)),
+                t["ln2_gamma"], t["ln2_mean"], t["ln2_rstd"], workspace=ws["ln2_bwd"])),
             ("ffn2_bdr_bwd", lambda: ls.ls_bias_dropout_residual_bwd(
-                t["ffn2_dx"], t["ffn2_dbias"], t["ffn2_dout"], t["ffn2_mask"], p, workspace=ws)),
+                t["ffn2_dx"], t["ffn2_dbias"], t["ffn2_dout"], t["ffn2_mask"], p,
+                workspace=ws["ffn2_bdr_bwd"])),
             ("ffn1_brd_bwd", lambda: ls.ls_bias_relu_dropout_bwd(
-                t["ffn1_dx"], t["ffn1_dbias"], t["ffn1_dout"], t["ffn1_mask"], p, workspace=ws)),
+                t["ffn1_dx"], t["ffn1_dbias"], t["ffn1_dout"], t["ffn1_mask"], p,
+                workspace=ws["ffn1_brd_bwd"])),
             ("ln1_bwd", lambda: ls.ls_layernorm_bwd(
                 t["ln1_dx"], t["ln1_dgamma"], t["ln1_dbeta"], t["ln1_dy"], t["ln1_x"],
-                t["ln1_gamma"], t["ln1_mean"], t["ln1_rstd"], workspace=ws)),
+                t["ln1_gamma"], t["ln1_mean"], t["ln1_rstd"], workspace=ws["ln1_bwd"])),
             ("attn_bdr_bwd", lambda: ls.ls_bias_dropout_residual_bwd(
-                t["attn_dx"], t["attn_dbias"], t["attn_dout"], t["attn_mask"], p, workspace=ws)),
+                t["attn_dx"], t["attn_dbias"], t["attn_dout"], t["attn_mask"], p,
+                workspace=ws["attn_bdr_bwd"])),
             ("softmax_bwd", lambda: ls.ls_softmax_bwd(t["scores_dx"], t["probs"], t["scores_dy"],
                                                       kl, L.causal)),
         ]
+
+    def begin(self):
+        """Start of a step: fork the column reductions onto the side stream."""
+        if self.side is not None:
+            self.ls.set_reduction_stream(self.side)
+
+    def end(self):
+        """End of a step: the current stream waits for the forked reductions."""
+        if self.side is not None:
+            self.ls.join_reductions()
+            self.ls.set_reduction_stream(None)
+
+    def step_thunks(self, t=None):
+        """One whole step: begin, the operators in layer order, end."""
+        return [self.begin] + [fn for _, fn in self.ops(t)] + [self.end]
 
     def nbytes(self, keys):
         return sum(self.t[k].numel() * self.t[k].element_size() for k in keys if k in self.t)
@@ -324,7 +352,7 @@ def in_step_times(step, reps=10):
     import torch
 
     ops = step.ops()
-    for _, fn in ops:
+    for fn in step.step_thunks():
         fn()
     torch.cuda.synchronize()
     evs = [torch.cuda.Event(enable_timing=True) for _ in range(reps * len(ops) + 1)]
@@ -332,8 +360,11 @@ def in_step_times(step, reps=10):
     evs[0].record()
     k = 1
     for _ in range(reps):
-        for _, fn in ops:
+        step.begin()
+        for i, (_, fn) in enumerate(ops):
             fn()
+            if i == len(ops) - 1:
+                step.end()
             evs[k].record()
             k += 1
     torch.cuda.synchronize()
@@ -562,7 +593,7 @@ def e2e_pipelined(step, host_in, nsteps):
     import torch
 
     sets = [step.t, {k: v.clone() for k, v in step.t.items()}]
-    graphs = [capture([fn for _, fn in step.ops(t)]) for t in sets]
+    graphs = [capture(step.step_thunks(t)) for t in sets]
     host_out = [{k: torch.empty(step.t[k].shape, dtype=step.t[k].dtype).pin_memory()
                  for k in step.outputs} for _ in sets]
     cs = torch.cuda.current_stream()
@@ -646,10 +677,10 @@ def run_ours(args):
         pg = dist
     ls_ops.load()
     layer = synth.LAYERS[args.workload]
-    step = LayerStep(layer, args.seed, device)
+    step = LayerStep(layer, args.seed, device, args.reductions)
     step_bytes = sum(step.bytes.values())
     names = [n for n, _ in step.ops()]
-    graph = capture([fn for _, fn in step.ops()])
+    graph = capture(step.step_thunks())
 
     sampler = ClockSampler(local)
     sampler.start()
@@ -737,7 +768,10 @@ def run_ours(args):
                    "l2": f"inputs larger than L2: one step touches "
                          f"{step.footprint_bytes() / 1e6:.0f} MB of distinct buffers "
                          f"(L2 {L2_BYTES / 1e6:.0f} MB); no flush",
-                   "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}"},
+                   "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}",
+                   "column_reductions": (
+                       "forked onto a second stream, joined at the end of the step"
+                       if step.side is not None else "inline on the step's stream")},
         "pct_of_peak": round(value / world / peak * 100, 2),
         "tokens_per_s": round(layer.tokens * world / (ms_step * 1e-3), 1),
         "per_op": ops_report,
@@ -856,7 +890,7 @@ def run_sweep(args):
             "peak": peak, "peak_source": f"{peak_kind} hbm_gbs (copy)",
             "config": {"workload": "softmax-sweep",
                        "elements": {"k_len <= 4096": synth.SWEEP_ELEMENTS,
-                                    "k_len >= 16384": SWEEP_LONG_ELEMENTS},
+                                    "k_len >= 8192": SWEEP_LONG_ELEMENTS},
                        "valid_len": "U[1, k_len] per row", "storage": "f16",
                        "l2": "rotating cloned buffer sets >= 3 x L2"},
             "k_len": rows_out}

@@ -107,6 +107,35 @@ ls_status ls_selftest_wait_timeout(uint32_t polls, void* stream);
  * need for an activation of shape [rows, cols]; enough for all three. */
 size_t ls_colreduce_workspace_bytes(int64_t rows, int64_t cols);
 
+/* Column reductions on a second stream (a scheduling facility; results are
+ * bit-identical to the default).  The backward entries with a bias, gamma or
+ * beta gradient (ls_bias_dropout_residual_bwd, ls_bias_relu_dropout_bwd,
+ * ls_layernorm_bwd, ls_bias_reshape_qkv_bwd) run a main kernel that writes dx
+ * and per-tile partial sums into the workspace, then the fixed-order sum of
+ * the partials -- the sums over rows that give dbias ("LightSeq2", section
+ * 2.1.2) and dgamma, dbeta ("CMU 11-868 L10 (LightSeq)", technique 2, slide
+ * p.22).  After
+ * ls_set_reduction_stream(rs), calls made from the calling thread launch that
+ * reduction on rs, ordered after the main kernel by an event, so that the
+ * caller's next kernel on the main stream does not wait for it.  Until
+ * ls_join_reductions(stream) has been called and stream reached that point,
+ * the gradients (dbias, dgamma, dbeta) are not ready and the workspaces the
+ * pending reductions read must not be written by anything but these entries:
+ * a later backward call whose workspace overlaps a pending reduction's makes
+ * its own stream wait for that reduction first (correct, but no overlap -- give
+ * each backward call of a step its own workspace to overlap).  Join before a
+ * stream capture ends (the reduction stream joins the capture at the first
+ * fork) and before starting one.  rs = NULL restores the default.  The state
+ * (rs, 18 CUDA events of the current device, up to 16 pending reductions) is
+ * per host thread.  Errors: LS_ERR_INVALID_ARGUMENT if reductions are pending
+ * (join first); LS_ERR_CUDA if the events cannot be created.
+ * ls_layernorm_bwd_noalloc never forks. */
+ls_status ls_set_reduction_stream(void* reduce_stream);
+
+/* Makes stream wait for every reduction forked since the last join (no-op if
+ * none), then forgets them.  Errors: LS_ERR_CUDA. */
+ls_status ls_join_reductions(void* stream);
+
 /* Fused bias + dropout + residual, forward ("CMU 11-868 L10 (LightSeq)",
  * technique 1; "LightSeq2", section 2.1.1):
  *   out[r,c] = residual[r,c] + keep(i) * (x[r,c] + bias[c]) / (1 - p),  i = r*cols + c.

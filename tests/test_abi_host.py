@@ -43,7 +43,7 @@ def lib():
 
 def test_library_exports_every_declared_symbol(lib):
     names = declared_functions()
-    assert len(names) == 25
+    assert len(names) == 27
     assert set(names) == set(ls_ops.EXPORTS)
     out = subprocess.run(["nm", "-D", "--defined-only", lsbuild.LIB], capture_output=True,
                          text=True, check=True).stdout
@@ -288,3 +288,10 @@ def test_embedding_argument_errors(lib):
 def test_selftest_argument_errors(lib):
     assert st("ls_selftest_wait_timeout", 0, S) == ls_ops.LS_ERR_INVALID_ARGUMENT
     assert st("ls_selftest_wait_timeout", (1 << 19) + 1, S) == ls_ops.LS_ERR_INVALID_ARGUMENT
+
+
+def test_reduction_stream_default_and_empty_join(lib):
+    # Restoring the default and joining with nothing forked make no CUDA call.
+    assert lib.ls_set_reduction_stream(None) == ls_ops.LS_OK
+    assert lib.ls_join_reductions(None) == ls_ops.LS_OK
+    assert lib.ls_join_reductions(A) == ls_ops.LS_OK

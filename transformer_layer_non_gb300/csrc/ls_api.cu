@@ -1,8 +1,9 @@
 // ls_api.cu -- the C ABI declared in include/ls_ops.h.  Every entry point
 // validates its arguments on the host (returning before anything is enqueued
 // on an error), then hands the call to a launcher in ls_internal.h.  Nothing
-// here allocates, synchronises, or keeps state beyond the per-thread message
-// of the last error.
+// here allocates device memory or synchronises; per-thread state is the
+// message of the last error and, once a reduction stream is set, that
+// stream's events and the workspaces its pending reductions read.
 #include <math.h>
 #include <stdarg.h>
 #include <stdio.h>
@@ -37,6 +38,103 @@ ls_status from_cuda(cudaError_t e, const char* what) {
 }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// ----------------------------------------------------------------------------
+// Column reductions on a second stream.  The backward entries with a bias,
+// gamma or beta gradient run a main kernel (dx and per-tile partial sums in
+// the workspace) and then the fixed-order reduction of the partial sums.
+// Only the gradient depends on the reduction, so with a reduction stream set
+// the reduction is forked onto it (an event recorded after the main kernel)
+// and the caller's next kernel follows the main kernel directly.  Each fork
+// remembers the workspace it reads and an event recorded after it; a later
+// backward call whose workspace overlaps a pending one first makes its own
+// stream wait for that event, so sharing one workspace stays correct (and
+// merely does not overlap).  ls_join_reductions ends all of it.
+// ----------------------------------------------------------------------------
+constexpr int kMaxPendingReductions = 16;
+
+struct PendingReduction {
+    uintptr_t lo, hi;  // workspace bytes [lo, hi) the reduction reads
+    int ev;            // index into ReductionState::done
+};
+
+struct ReductionState {
+    cudaStream_t side = nullptr;
+    bool active = false;  // a reduction stream is set
+    int device = -1;      // the device the events belong to
+    cudaEvent_t fork = nullptr, join = nullptr;
+    cudaEvent_t done[kMaxPendingReductions] = {};
+    bool used[kMaxPendingReductions] = {};
+    PendingReduction pend[kMaxPendingReductions];
+    int npend = 0;
+    bool forked = false;  // a fork since the last join
+};
+
+thread_local ReductionState t_red;
+
+cudaError_t make_event(cudaEvent_t* ev) {
+    if (*ev) return cudaSuccess;
+    return cudaEventCreateWithFlags(ev, cudaEventDisableTiming);
+}
+
+// Drops pending entry i (its event slot becomes free).
+void drop_pending(int i) {
+    ReductionState& r = t_red;
+    r.used[r.pend[i].ev] = false;
+    r.pend[i] = r.pend[r.npend - 1];
+    --r.npend;
+}
+
+// Before a backward call writes partial sums into [ws, ws + bytes) on s:
+// order s after every pending reduction that reads an overlapping range.
+cudaError_t guard_workspace(cudaStream_t s, const void* ws, size_t bytes) {
+    ReductionState& r = t_red;
+    if (r.npend == 0 || !ws || bytes == 0) return cudaSuccess;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ws), hi = lo + bytes;
+    for (int i = 0; i < r.npend; ++i)
+        if (lo < r.pend[i].hi && r.pend[i].lo < hi) {
+            const cudaError_t e = cudaStreamWaitEvent(s, r.done[r.pend[i].ev], 0);
+            if (e != cudaSuccess) return e;
+        }
+    return cudaSuccess;
+}
+
+// Launches a column reduction fn(stream) that reads [ws, ws + bytes): on s,
+// or forked onto the reduction stream after s's work so far.
+template <typename F>
+cudaError_t launch_reduction(cudaStream_t s, const void* ws, size_t bytes, F fn) {
+    ReductionState& r = t_red;
+    if (!r.active) return fn(s);
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev != r.device) return cudaErrorInvalidResourceHandle;  // events of another device
+    if (r.npend == kMaxPendingReductions) {
+        // Full: order s after the oldest pending reduction and forget it.
+        e = cudaStreamWaitEvent(s, r.done[r.pend[0].ev], 0);
+        if (e != cudaSuccess) return e;
+        drop_pending(0);
+    }
+    int slot = 0;
+    while (r.used[slot]) ++slot;
+    e = cudaEventRecord(r.fork, s);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(r.side, r.fork, 0);
+    if (e == cudaSuccess) e = fn(r.side);
+    if (e == cudaSuccess) e = cudaEventRecord(r.done[slot], r.side);
+    if (e != cudaSuccess) return e;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ws), hi = lo + bytes;
+    // Pending reductions inside this range are implied by the new one (the
+    // reduction stream runs in order).
+    for (int i = 0; i < r.npend;)
+        if (lo <= r.pend[i].lo && r.pend[i].hi <= hi)
+            drop_pending(i);
+        else
+            ++i;
+    r.used[slot] = true;
+    r.pend[r.npend++] = PendingReduction{lo, hi, slot};
+    r.forked = true;
+    return cudaSuccess;
+}
 
 // A byte range [p, p+n) of one argument.
 struct Span {
@@ -195,6 +293,50 @@ ls_status ls_selftest_wait_timeout(uint32_t polls, void* stream) {
                      "ls_selftest_wait_timeout launch");
 }
 
+ls_status ls_set_reduction_stream(void* reduce_stream) {
+    ReductionState& r = t_red;
+    if (r.forked)
+        return fail(LS_ERR_INVALID_ARGUMENT,
+                    "ls_set_reduction_stream: reductions are pending on the previous reduction "
+                    "stream; call ls_join_reductions first");
+    if (!reduce_stream) {
+        r.active = false;
+        r.side = nullptr;
+        return ok();
+    }
+    int dev = -1;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e == cudaSuccess && r.device >= 0 && dev != r.device) {
+        // Events of another device: release them and start over.
+        cudaEventDestroy(r.fork);
+        cudaEventDestroy(r.join);
+        for (cudaEvent_t& ev : r.done) {
+            if (ev) cudaEventDestroy(ev);
+            ev = nullptr;
+        }
+        r.fork = r.join = nullptr;
+    }
+    if (e == cudaSuccess) e = make_event(&r.fork);
+    if (e == cudaSuccess) e = make_event(&r.join);
+    for (int i = 0; e == cudaSuccess && i < kMaxPendingReductions; ++i) e = make_event(&r.done[i]);
+    if (e != cudaSuccess) return from_cuda(e, "ls_set_reduction_stream");
+    r.device = dev;
+    r.side = static_cast<cudaStream_t>(reduce_stream);
+    r.active = true;
+    return ok();
+}
+
+ls_status ls_join_reductions(void* stream) {
+    ReductionState& r = t_red;
+    if (!r.forked) return ok();
+    cudaError_t e = cudaEventRecord(r.join, r.side);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(static_cast<cudaStream_t>(stream), r.join, 0);
+    if (e != cudaSuccess) return from_cuda(e, "ls_join_reductions");
+    while (r.npend > 0) drop_pending(r.npend - 1);
+    r.forked = false;
+    return ok();
+}
+
 size_t ls_colreduce_workspace_bytes(int64_t rows, int64_t cols) {
     if (rows <= 0 || cols <= 0 || cols % 8 != 0) return 0;
     const size_t a = ls::dropout_bwd_plan(rows, cols).bytes();
@@ -270,11 +412,15 @@ static ls_status dropout_bwd_common(const char* fn, ls_dtype dtype, void* dx, vo
     LS_TRY(check_overlaps(outs, 3, ins, 2));
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     float* partial = dbias ? static_cast<float*>(workspace) : nullptr;
-    cudaError_t e = ls::launch_dropout_bwd(dt, dx, partial, dout,
-                                           reinterpret_cast<const uint8_t*>(mask_bits), rows,
-                                           cols, rng, s);
+    cudaError_t e = guard_workspace(s, partial, plan.bytes());
+    if (e == cudaSuccess)
+        e = ls::launch_dropout_bwd(dt, dx, partial, dout,
+                                   reinterpret_cast<const uint8_t*>(mask_bits), rows, cols, rng,
+                                   s);
     if (e == cudaSuccess && dbias)
-        e = ls::launch_colreduce(dt, dbias, nullptr, cols, partial, plan.parts, cols, s);
+        e = launch_reduction(s, partial, plan.bytes(), [&](cudaStream_t rs) {
+            return ls::launch_colreduce(dt, dbias, nullptr, cols, partial, plan.parts, cols, rs);
+        });
     return from_cuda(e, fn);
 }
 
@@ -388,12 +534,16 @@ ls_status ls_layernorm_bwd(ls_dtype dtype, void* dx, void* dgamma, void* dbeta, 
                         {"mean", mean, sb},   {"rstd", rstd, sb}};
     LS_TRY(check_overlaps(outs, 4, ins, 5));
     float* partial = dgamma ? static_cast<float*>(workspace) : nullptr;
-    cudaError_t e =
-        ls::launch_layernorm_bwd(dt, dx, partial, dy, x, gamma, mean, rstd, rows, cols, s);
+    cudaError_t e = guard_workspace(s, partial, plan.bytes());
+    if (e == cudaSuccess)
+        e = ls::launch_layernorm_bwd(dt, dx, partial, dy, x, gamma, mean, rstd, rows, cols, s);
     if (e == cudaSuccess && dgamma) {
         // Each partial row is [dgamma part | dbeta part]: one reduction of
         // 2*cols columns, the first half to dgamma and the second to dbeta.
-        e = ls::launch_colreduce(dt, dgamma, dbeta, cols, partial, plan.parts, plan.width, s);
+        e = launch_reduction(s, partial, plan.bytes(), [&](cudaStream_t rs) {
+            return ls::launch_colreduce(dt, dgamma, dbeta, cols, partial, plan.parts, plan.width,
+                                        rs);
+        });
     }
     return from_cuda(e, "ls_layernorm_bwd launch");
 }
@@ -575,9 +725,13 @@ ls_status ls_bias_reshape_qkv_bwd(ls_dtype dtype, void* dqkv, void* dbias, const
                         o.name);
     LS_TRY(check_overlaps(outs, 3, nullptr, 0));
     float* partial = dbias ? static_cast<float*>(workspace) : nullptr;
-    cudaError_t e = ls::launch_qkv_bwd(dt, dqkv, partial, dq_k_v, batch, seq, heads, head_dim, s);
+    cudaError_t e = guard_workspace(s, partial, plan.bytes());
+    if (e == cudaSuccess)
+        e = ls::launch_qkv_bwd(dt, dqkv, partial, dq_k_v, batch, seq, heads, head_dim, s);
     if (e == cudaSuccess && dbias)
-        e = ls::launch_colreduce(dt, dbias, nullptr, cols, partial, plan.parts, cols, s);
+        e = launch_reduction(s, partial, plan.bytes(), [&](cudaStream_t rs) {
+            return ls::launch_colreduce(dt, dbias, nullptr, cols, partial, plan.parts, cols, rs);
+        });
     return from_cuda(e, "ls_bias_reshape_qkv_bwd launch");
 }
 

@@ -14,7 +14,7 @@
 //   nvec > 128        a CTA per row (4 or 8 warps), partial results of the two
 //                     reductions through shared memory.
 //   nvec > 2048       a CTA per row that reads the row twice: an online
-//                     (maximum, sum) pass, then the output pass.
+//   (fwd: > 1792)     (maximum, sum) pass, then the output pass.
 // Masked keys are never loaded: a lane loads a vector only if it holds at
 // least one valid key; masked outputs are written as exact zeros.
 #include <math.h>
@@ -816,9 +816,15 @@ struct SmPlan {
     int64_t grid;
 };
 
-constexpr int64_t kMaxRegisterRowLen = 16384;  // 8 warps x 8 vectors x 8 elements
+// Longest rows held in registers: 8 warps x 8 vectors x 8 elements.  The
+// forward at 8 vectors per lane needs so many registers that only two CTAs
+// fit on an SM, and measured slower than the two-pass kernel at 16384 keys
+// (the backward is even there), so forward rows past 7 vectors per lane
+// stream.
+constexpr int64_t kMaxRegisterRowLen = 16384;
+constexpr int64_t kMaxRegisterRowLenFwd = 8 * 32 * 7 * kVec;  // 14336
 
-SmPlan plan_for(int64_t nrows, int64_t k_len) {
+SmPlan plan_for(int64_t nrows, int64_t k_len, bool fwd) {
     const int nvec = static_cast<int>(k_len / kVec);
     SmPlan p{};
     if (nvec <= 128) {
@@ -833,7 +839,7 @@ SmPlan plan_for(int64_t nrows, int64_t k_len) {
         }
         const int64_t rpc = kThreads / p.lpr;
         p.grid = (nrows + rpc - 1) / rpc;
-    } else if (k_len <= kMaxRegisterRowLen) {
+    } else if (k_len <= (fwd ? kMaxRegisterRowLenFwd : kMaxRegisterRowLen)) {
         p.cta = true;
         p.warps = nvec <= 512 ? 4 : 8;
         p.vpt = (nvec + p.warps * 32 - 1) / (p.warps * 32);
@@ -969,7 +975,7 @@ cudaError_t fwd_dispatch(void* y, const void* x, const SoftmaxShape& sh, const D
                          cudaStream_t s) {
     const int64_t nrows = sh.batch * sh.heads * sh.q_len;
     const int k_len = static_cast<int>(sh.k_len);
-    const SmPlan p = plan_for(nrows, sh.k_len);
+    const SmPlan p = plan_for(nrows, sh.k_len, true);
     const RowMask m = make_mask(sh);
     if (p.stream)
         return launch_pdl(softmax_fwd_stream_kernel<T, DROP>, dim3(static_cast<unsigned>(p.grid)),
@@ -987,7 +993,7 @@ cudaError_t bwd_dispatch(void* dx, const void* y, const void* dy, const SoftmaxS
                          const DropArgs& d, cudaStream_t s) {
     const int64_t nrows = sh.batch * sh.heads * sh.q_len;
     const int k_len = static_cast<int>(sh.k_len);
-    const SmPlan p = plan_for(nrows, sh.k_len);
+    const SmPlan p = plan_for(nrows, sh.k_len, false);
     const RowMask m = make_mask(sh);
     if (p.stream)
         return launch_pdl(softmax_bwd_stream_kernel<T, DROP>, dim3(static_cast<unsigned>(p.grid)),

@@ -39,7 +39,7 @@ EXPORTS = (
     "ls_softmax_dropout_fwd", "ls_softmax_dropout_bwd",
     "ls_cross_entropy_fwd", "ls_cross_entropy_bwd",
     "ls_embedding_fwd", "ls_embedding_bwd", "ls_embedding_workspace_bytes",
-    "ls_selftest_wait_timeout",
+    "ls_selftest_wait_timeout", "ls_set_reduction_stream", "ls_join_reductions",
 )
 
 
@@ -73,6 +73,8 @@ _SIGNATURES = {
     "ls_softmax_fwd": (_INT, [_INT, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_softmax_bwd": (_INT, [_INT, _P, _P, _P, _I64, _I64, _I64, _I64, _P, _INT, _P]),
     "ls_selftest_wait_timeout": (_INT, [ctypes.c_uint32, _P]),
+    "ls_set_reduction_stream": (_INT, [_P]),
+    "ls_join_reductions": (_INT, [_P]),
     "ls_embedding_fwd": (_INT, [_INT, _P, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _I64, _F32,
                                 _F32, _U64, _U64, _P]),
     "ls_embedding_bwd": (_INT, [_INT, _P, _P, _P, _P, _I64, _I64, _I64, _I64, _F32, _F32, _INT,
@@ -153,6 +155,20 @@ def check_device_errors() -> int:
 def selftest_wait_timeout(polls: int = 1024, stream=None):
     """Enqueue the bounded-wait failure self-test (see include/ls_ops.h)."""
     _check(load().ls_selftest_wait_timeout(polls, _stream(stream)))
+
+
+def set_reduction_stream(stream):
+    """Fork the column reductions of the backward calls made from this thread
+    onto `stream` (a torch.cuda.Stream or a raw handle); None restores the
+    default.  See ls_set_reduction_stream in include/ls_ops.h."""
+    h = None if stream is None else (stream if isinstance(stream, int) else stream.cuda_stream)
+    _check(load().ls_set_reduction_stream(h))
+
+
+def join_reductions(stream=None):
+    """Order `stream` (default: the current stream) after every forked
+    reduction; the gradients are ready from there on."""
+    _check(load().ls_join_reductions(_stream(stream)))
 
 
 def _check(status: int):

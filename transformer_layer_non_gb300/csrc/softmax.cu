@@ -186,10 +186,13 @@ __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y,
     }
 }
 
-// The backward keeps per-lane branches: it moves twice the bytes per row and
-// measured faster this way than branch-free (which needs more registers).  A
-// vector wholly inside the valid prefix takes the unpredicated path, with the
-// FP16 conversions folded into mixed-precision instructions.
+// The backward branches (branch-free needs more registers and measured
+// slower).  A vector wholly inside the valid prefix takes the unpredicated
+// path, with the FP16 conversions folded into mixed-precision instructions.
+// With a warp per row the branch is taken per slot of 32 vectors (the warp's
+// k-th vectors) rather than per lane, so it is warp-uniform: a slot that
+// straddles the end of the valid prefix runs only the predicated path instead
+// of the full, predicated and empty paths one after another.
 template <typename T, int LPR, int VPT, bool DROP>
 __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx, int64_t row,
                                            int64_t nrows, int k_len, int gl, const DropArgs& d) {
@@ -239,19 +242,26 @@ __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx
         }
         return;
     }
+    // full(k): vector gl + k*LPR lies wholly in the valid prefix; any(k): it
+    // holds a valid element.  Warp-uniform (whole slot) for a warp per row.
+    constexpr bool kSlot = LPR == 32;
+    auto full = [&](int k) {
+        return ((kSlot ? k * LPR + LPR : gl + k * LPR + 1) * kVec) <= vlen;
+    };
+    auto any = [&](int k) { return ((kSlot ? k * LPR : gl + k * LPR) * kVec) < vlen; };
     float dot = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = gl + k * LPR;
-        if ((v + 1) * kVec <= vlen) {
+        if (full(k)) {
             dot = dot8_acc(buf.a[k], buf.b[k], dot);
-        } else if (v * kVec < vlen) {
+        } else if (any(k)) {
             float yf[kVec], df[kVec];
             unpack(buf.a[k], yf);
             unpack(buf.b[k], df);
 #pragma unroll
             for (int j = 0; j < kVec; ++j)
-                if (v * kVec + j < vlen) dot = fmaf(yf[j], df[j], dot);
+                dot = v * kVec + j < vlen ? fmaf(yf[j], df[j], dot) : dot;  // unloaded: discarded
         }
     }
     dot = group_sum<LPR>(dot);
@@ -262,7 +272,7 @@ __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx
         const int v = gl + k * LPR;
         if (v < nvec) {
             float o[kVec];
-            if ((v + 1) * kVec <= vlen) {
+            if (full(k)) {
                 float yf[kVec];
                 unpack(buf.a[k], yf);
                 sub8(buf.b[k], dot, o);
@@ -273,7 +283,7 @@ __device__ __forceinline__ void sm_bwd_row(const RowBuf<T, LPR, VPT>& buf, T* dx
                     o[j] = t.x;
                     o[j + 1] = t.y;
                 }
-            } else if (v * kVec < vlen) {
+            } else if (any(k)) {
                 float yf[kVec], df[kVec];
                 unpack(buf.a[k], yf);
                 unpack(buf.b[k], df);

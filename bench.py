@@ -36,6 +36,9 @@ UNIT = "GB/s"
 DEFAULT_WORKLOAD = "bert-base"
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
+# GB300's nominal HBM3e bandwidth (vendor figure; context beside the measured
+# copy bandwidth, which is the roofline denominator).
+NOMINAL_HBM_GBS = 7900.0
 SWEEP_K_LENS = (16, 32, 64, 128, 256, 512, 1024, 2048, 4096)
 # Rows past the on-chip limit (two-pass online softmax), on 2^26 elements so
 # that even the longest rows give one CTA per row for every SM several times.
@@ -773,6 +776,8 @@ def run_ours(args):
                        "forked onto a second stream, joined at the end of the step"
                        if step.side is not None else "inline on the step's stream")},
         "pct_of_peak": round(value / world / peak * 100, 2),
+        "pct_of_nominal_hbm": round(value / world / NOMINAL_HBM_GBS * 100, 2),
+        "nominal_hbm_gbs": NOMINAL_HBM_GBS,
         "tokens_per_s": round(layer.tokens * world / (ms_step * 1e-3), 1),
         "per_op": ops_report,
         "per_fused_op": fused_op_summary(ops_report, peak),

@@ -279,7 +279,9 @@ ls_status ls_embedding_fwd(ls_dtype dtype, void* y, uint32_t* mask_bits, const i
                            int64_t seq, int64_t hidden, int64_t vocab, int64_t max_positions,
                            float scale, float p, uint64_t seed, uint64_t offset, void* stream);
 
-/* Workspace bytes ls_embedding_bwd needs for `tokens` tokens (8 per token). */
+/* Workspace bytes ls_embedding_bwd needs for `tokens` tokens: 0 (the
+ * deterministic backward keeps no scratch; the workspace arguments may be
+ * NULL and 0). */
 size_t ls_embedding_workspace_bytes(int64_t tokens);
 
 /* Backward of the above into the token table's gradient, FP32 [vocab, hidden],
@@ -287,11 +289,11 @@ size_t ls_embedding_workspace_bytes(int64_t tokens);
  *   d_token_table[w] += scale / (1 - p) * sum over tokens i with id w of bit * dy[i]
  * deterministic == 0: the pages' method, float atomic adds (one pass; the
  * order of the additions, so the last bits, vary from run to run; no
- * workspace).  deterministic != 0: the ids are sorted on the device and every
- * id's rows are added in token order by one warp, the same bits on every run
- * (workspace of ls_embedding_workspace_bytes(batch*seq) bytes; at most 16384
- * tokens per call, calls on one stream accumulate in order).  The position
- * table gets no gradient (the pages' formula has none). */
+ * workspace).  deterministic != 0: the warp of each id's first token adds
+ * that id's rows in token order, the same bits on every run (no workspace; at
+ * most 16384 tokens per call, calls on one stream accumulate in order; an id
+ * that occurs n times costs its warp n row reads one after another).  The
+ * position table gets no gradient (the pages' formula has none). */
 ls_status ls_embedding_bwd(ls_dtype dtype, float* d_token_table, const void* dy,
                            const uint32_t* mask_bits, const int32_t* tokens, int64_t batch,
                            int64_t seq, int64_t hidden, int64_t vocab, float scale, float p,

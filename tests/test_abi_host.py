@@ -271,7 +271,7 @@ def test_embedding_argument_errors(lib):
     def bwd(dE=A, dy=B, m=C, tok=D, b=2, s=16, h=64, v=100, ws=E, wsb=1 << 20):
         return st("ls_embedding_bwd", F16, dE, dy, m, tok, b, s, h, v, 1.0, 0.1, 1, ws, wsb, S)
 
-    assert ls_ops.embedding_workspace_bytes(32) == 256
+    assert ls_ops.embedding_workspace_bytes(32) == 0
     assert fwd(h=60) == ls_ops.LS_ERR_MISALIGNED
     assert fwd(mp=8) == ls_ops.LS_ERR_INVALID_ARGUMENT           # positions shorter than seq
     assert fwd(tok=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
@@ -279,10 +279,11 @@ def test_embedding_argument_errors(lib):
     assert fwd(p=1.5) == ls_ops.LS_ERR_INVALID_ARGUMENT
     assert fwd(y=D) == ls_ops.LS_ERR_INVALID_ARGUMENT            # y over the token table
     assert fwd(b=0, y=None) == ls_ops.LS_OK
-    assert bwd(wsb=255) == ls_ops.LS_ERR_WORKSPACE_TOO_SMALL
+    # no workspace is needed: a NULL one gets past to the later checks
+    assert bwd(ws=None, wsb=0, tok=D + 2) == ls_ops.LS_ERR_MISALIGNED
     assert bwd(m=None) == ls_ops.LS_ERR_INVALID_ARGUMENT
     assert bwd(b=1024, s=17) == ls_ops.LS_ERR_UNSUPPORTED_SHAPE   # > 16384 tokens in one call
-    assert bwd(ws=A + 64) == ls_ops.LS_ERR_INVALID_ARGUMENT       # workspace inside dE
+    assert bwd(tok=A + 64) == ls_ops.LS_ERR_INVALID_ARGUMENT      # tokens inside dE
 
 
 def test_selftest_argument_errors(lib):

@@ -11,10 +11,9 @@
 // Backward: dE[w] += s / (1 - p) * sum over the tokens i with id w of
 // bit * dy[i].  The pages add the rows with atomicAdd, whose order (and so
 // whose rounding) changes from run to run; that is one mode here (vector
-// float atomics, one pass).  The other mode is deterministic: one CTA sorts the (id, index) pairs of the batch in shared memory (a bitonic
-// sort of unique 64-bit keys, so equal ids stay in index order); then a warp
-// per run of equal ids adds that id's rows in index order and adds the total
-// into dE[w] -- each row of dE has exactly one writer, so no atomics.
+// float atomics, one pass).  The other mode is deterministic: the warp of the
+// first token with each id adds that id's rows in index order and adds the
+// total into dE[w] -- each row of dE has exactly one writer, so no atomics.
 #include "ls_device.cuh"
 #include "ls_internal.h"
 
@@ -80,179 +79,119 @@ emb_fwd_kernel(T* __restrict__ y, uint8_t* __restrict__ mask, const int32_t* __r
 }
 
 // --- backward ------------------------------------------------------------
-// Sort: keys (id << 32 | index), ids outside [0, vocab) replaced by 2^32 - 1
-// so that they sort last and are skipped.  n2 = the power of two >= T.
-constexpr int kSortThreads = 1024;
-
-__global__ void __launch_bounds__(kSortThreads)
-emb_sort_kernel(uint64_t* __restrict__ sorted, const int32_t* __restrict__ tokens, int T, int n2,
-                int64_t vocab) {
-    extern __shared__ uint64_t keys[];
-    pdl_enter();
-    for (int k = threadIdx.x; k < n2; k += kSortThreads) {
-        uint64_t key = ~uint64_t{0};  // padding: after every real key
-        if (k < T) {
-            const int32_t w = tokens[k];
-            const uint32_t id = (w >= 0 && static_cast<int64_t>(w) < vocab)
-                                    ? static_cast<uint32_t>(w)
-                                    : 0xFFFFFFFFu;
-            key = (static_cast<uint64_t>(id) << 32) | static_cast<uint32_t>(k);
-        }
-        keys[k] = key;
-    }
-    __syncthreads();
-    // Bitonic sort, ascending.
-    for (int size = 2; size <= n2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            for (int t = threadIdx.x; t < n2 / 2; t += kSortThreads) {
-                const int lo = 2 * t - (t & (stride - 1));
-                const int hi = lo + stride;
-                const bool up = (lo & size) == 0;
-                const uint64_t a = keys[lo], b = keys[hi];
-                if ((a > b) == up) {
-                    keys[lo] = b;
-                    keys[hi] = a;
-                }
-            }
-            __syncthreads();
-        }
-    }
-    for (int k = threadIdx.x; k < T; k += kSortThreads) sorted[k] = keys[k];
-}
-
-// The same sort for n2 <= 4096 with four keys per thread (n2/4 threads):
-// stages whose partners lie in one thread compare in registers, stages whose
-// partners lie in one warp exchange by shuffle, and only the stages with
-// partners 128 or more positions apart go through shared memory -- 15
-// shared-memory stages for 4096 keys instead of 78.
-constexpr int kRegKeys = 4;
-constexpr int kRegSortMax = kSortThreads * kRegKeys;  // 4096
-
-__device__ __forceinline__ void cas(uint64_t& mine, uint64_t other, bool keep_min) {
-    mine = keep_min ? (other < mine ? other : mine) : (other > mine ? other : mine);
-}
-
-__global__ void __launch_bounds__(kSortThreads)
-emb_sort_reg_kernel(uint64_t* __restrict__ sorted, const int32_t* __restrict__ tokens, int T,
-                    int n2, int64_t vocab) {
-    __shared__ uint64_t keys[kRegSortMax];
-    pdl_enter();
-    const int t = threadIdx.x;
-    const int lane = t & 31;
-    uint64_t k[kRegKeys];
-#pragma unroll
-    for (int q = 0; q < kRegKeys; ++q) {
-        const int p = kRegKeys * t + q;
-        uint64_t key = ~uint64_t{0};
-        if (p < T) {
-            const int32_t w = tokens[p];
-            const uint32_t id = (w >= 0 && static_cast<int64_t>(w) < vocab)
-                                    ? static_cast<uint32_t>(w)
-                                    : 0xFFFFFFFFu;
-            key = (static_cast<uint64_t>(id) << 32) | static_cast<uint32_t>(p);
-        }
-        k[q] = key;
-    }
-    for (int size = 2; size <= n2; size <<= 1) {
-        for (int stride = size >> 1; stride > 0; stride >>= 1) {
-            if (stride < kRegKeys) {
-                // partners in this thread: (0,1),(2,3) or (0,2),(1,3); the
-                // direction is that of the pair's lower position
-                auto cx = [&](uint64_t& a, uint64_t& b, int q_lo) {
-                    const bool up = ((kRegKeys * t + q_lo) & size) == 0;
-                    if ((a > b) == up) {
-                        const uint64_t c = a;
-                        a = b;
-                        b = c;
-                    }
-                };
-                if (stride == 1) {
-                    cx(k[0], k[1], 0);
-                    cx(k[2], k[3], 2);
-                } else {
-                    cx(k[0], k[2], 0);
-                    cx(k[1], k[3], 1);
-                }
-            } else if (stride < 32 * kRegKeys) {
-                // partners in this warp: lane ^ (stride / kRegKeys), same slot
-                const int lm = stride / kRegKeys;
-#pragma unroll
-                for (int q = 0; q < kRegKeys; ++q) {
-                    const int p = kRegKeys * t + q;
-                    const uint64_t other = __shfl_xor_sync(0xffffffffu, k[q], lm);
-                    const bool lower = (p & stride) == 0, up = (p & size) == 0;
-                    cas(k[q], other, lower == up);
-                }
-            } else {
-                // partners in other warps: through shared memory
-#pragma unroll
-                for (int q = 0; q < kRegKeys; ++q) keys[kRegKeys * t + q] = k[q];
-                __syncthreads();
-#pragma unroll
-                for (int q = 0; q < kRegKeys; ++q) {
-                    const int p = kRegKeys * t + q;
-                    const uint64_t other = keys[p ^ stride];
-                    const bool lower = (p & stride) == 0, up = (p & size) == 0;
-                    cas(k[q], other, lower == up);
-                }
-                __syncthreads();
-            }
-        }
-    }
-    (void)lane;
-#pragma unroll
-    for (int q = 0; q < kRegKeys; ++q) {
-        const int p = kRegKeys * t + q;
-        if (p < T) sorted[p] = k[q];
-    }
-}
-
 struct EmbBwdArgs {
     int T;
     int nvr;     // H / 8
     int64_t H;
+    int64_t vocab;
     float coef;  // s / (1 - p)
 };
 
-// One warp per sorted position; the warp at the head of a run of equal ids
-// adds the run's rows in index order and adds the total into dE[id].
+constexpr int kOwnerBlk = 3;  // column vectors per lane per pass over the matches
+constexpr int kIdsPerLane = 8;
+constexpr int kIdStep = 32 * kIdsPerLane;  // ids a warp compares per ballot
+
+// Deterministic backward without a sort: one warp per token j.  The warp
+// returns unless j is the first token with its id w; the owner then walks the
+// tokens from j on, and for every token i with id w, in increasing i, adds
+// bit * dy[i] into FP32 registers, and finally adds coef times the sum into
+// dE[w].  Each row of dE has one writer and a fixed order of additions, so the
+// bits are the same on every run.  The ids (which stay in L1) are compared
+// 256 per step, load q of lane l reading id base + 32q + l (each load a
+// coalesced 128 bytes), so a scan over the batch is a short chain of
+// independent loads; the matches are taken load by load and lane by lane,
+// i.e. in increasing index.  Column vectors go kOwnerBlk per lane per pass
+// (one pass for H <= 768); four CTAs per SM keep a whole 4096-token batch
+// resident in one wave.  The owner asks L2 for its dE row and its own dy row
+// before it scans, so those reads overlap the scan.
 template <typename T>
-__global__ void __launch_bounds__(kThreads)
-emb_accum_kernel(float* __restrict__ dE, const T* __restrict__ dy,
-                 const uint8_t* __restrict__ mask, const uint64_t* __restrict__ sorted,
+__global__ void __launch_bounds__(kThreads, min_ctas<T>(4))
+emb_owner_kernel(float* __restrict__ dE, const T* __restrict__ dy,
+                 const uint8_t* __restrict__ mask, const int32_t* __restrict__ tokens,
                  const __grid_constant__ EmbBwdArgs a) {
     pdl_enter();
     const int j = static_cast<int>((static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5);
     const int lane = threadIdx.x & 31;
-    if (j >= a.T) return;
-    const uint64_t key = sorted[j];
-    const uint32_t id = static_cast<uint32_t>(key >> 32);
-    if (id == 0xFFFFFFFFu) return;                                  // invalid ids sort last
-    if (j > 0 && static_cast<uint32_t>(sorted[j - 1] >> 32) == id) return;  // not a run head
-    int end = j + 1;
-    while (end < a.T && static_cast<uint32_t>(sorted[end] >> 32) == id) ++end;
-    for (int cv = lane; cv < a.nvr; cv += 32) {
-        float acc[kVec];
+    if (j >= a.T) return;  // whole warps
+    const int32_t w = tokens[j];
+    if (w < 0 || static_cast<int64_t>(w) >= a.vocab) return;  // no table row: no gradient
+    // This lane's ids of the step at `base`, restricted to [lo, hi), as a bit
+    // mask of matches with w (ids outside the range are never loaded).
+    auto matches = [&](int base, int lo, int hi) {
+        int32_t t[kIdsPerLane];
 #pragma unroll
-        for (int q = 0; q < kVec; ++q) acc[q] = 0.f;
-        for (int r = j; r < end; ++r) {
-            const int64_t i = static_cast<int64_t>(static_cast<uint32_t>(sorted[r]));
-            const int64_t e = i * a.H + static_cast<int64_t>(cv) * kVec;
-            const uint32_t bits = mask[e >> 3];
-            float g[kVec];
-            load8f<T>(dy + e, g);
-#pragma unroll
-            for (int q = 0; q < kVec; ++q)
-                if ((bits >> q) & 1u) acc[q] += g[q];
+        for (int q = 0; q < kIdsPerLane; ++q) {
+            const int k = base + q * 32 + lane;
+            t[q] = (k >= lo && k < hi) ? tokens[k] : -1;
         }
-        float* dst = dE + static_cast<int64_t>(id) * a.H + static_cast<int64_t>(cv) * kVec;
-        float4 d0 = *reinterpret_cast<float4*>(dst), d1 = *reinterpret_cast<float4*>(dst + 4);
-        d0.x = fmaf(a.coef, acc[0], d0.x); d0.y = fmaf(a.coef, acc[1], d0.y);
-        d0.z = fmaf(a.coef, acc[2], d0.z); d0.w = fmaf(a.coef, acc[3], d0.w);
-        d1.x = fmaf(a.coef, acc[4], d1.x); d1.y = fmaf(a.coef, acc[5], d1.y);
-        d1.z = fmaf(a.coef, acc[6], d1.z); d1.w = fmaf(a.coef, acc[7], d1.w);
-        *reinterpret_cast<float4*>(dst) = d0;
-        *reinterpret_cast<float4*>(dst + 4) = d1;
+        uint32_t my = 0;
+#pragma unroll
+        for (int q = 0; q < kIdsPerLane; ++q) my |= static_cast<uint32_t>(t[q] == w) << q;
+        return my;
+    };
+    for (int base = 0; base < j; base += kIdStep)  // an earlier token with id w?
+        if (__ballot_sync(0xffffffffu, matches(base, 0, j) != 0)) return;
+    for (int cv = lane; cv < a.nvr; cv += 32) {
+        prefetch_l2(dE + static_cast<int64_t>(w) * a.H + static_cast<int64_t>(cv) * kVec);
+        prefetch_l2(dy + static_cast<int64_t>(j) * a.H + static_cast<int64_t>(cv) * kVec);
+    }
+    const int first = j - j % kIdStep;
+    int end = a.T;  // after the first pass: one past the id's last token
+    for (int cb = 0; cb < a.nvr; cb += 32 * kOwnerBlk) {
+        float acc[kOwnerBlk][kVec];
+#pragma unroll
+        for (int b = 0; b < kOwnerBlk; ++b)
+#pragma unroll
+            for (int q = 0; q < kVec; ++q) acc[b][q] = 0.f;
+        int last = j;
+        for (int base = first; base < end; base += kIdStep) {
+            const uint32_t my = matches(base, j, end);
+            if (!__ballot_sync(0xffffffffu, my != 0)) continue;
+#pragma unroll 1
+            for (int ld = 0; ld < kIdsPerLane; ++ld) {  // warp-uniform: loads, then lanes, in order
+                uint32_t lanes = __ballot_sync(0xffffffffu, (my >> ld) & 1u);
+                while (lanes) {
+                    const int64_t i = base + ld * 32 + __ffs(lanes) - 1;
+                    lanes &= lanes - 1;
+                    last = static_cast<int>(i);
+                    Raw8<T> g[kOwnerBlk];
+                    uint32_t bits[kOwnerBlk];
+#pragma unroll
+                    for (int b = 0; b < kOwnerBlk; ++b) {
+                        const int cv = cb + b * 32 + lane;
+                        bits[b] = 0u;
+                        if (cv < a.nvr) {
+                            const int64_t e = i * a.H + static_cast<int64_t>(cv) * kVec;
+                            g[b] = load8<T>(dy + e);
+                            bits[b] = mask[e >> 3];
+                        }
+                    }
+#pragma unroll
+                    for (int b = 0; b < kOwnerBlk; ++b) {
+                        if (cb + b * 32 + lane >= a.nvr) continue;
+                        float f[kVec];
+                        unpack(g[b], f);
+#pragma unroll
+                        for (int q = 0; q < kVec; ++q)
+                            if ((bits[b] >> q) & 1u) acc[b][q] += f[q];
+                    }
+                }
+            }
+        }
+        end = last + 1;  // later passes stop at the id's last token
+#pragma unroll
+        for (int b = 0; b < kOwnerBlk; ++b) {
+            const int cv = cb + b * 32 + lane;
+            if (cv >= a.nvr) continue;
+            float* dst = dE + static_cast<int64_t>(w) * a.H + static_cast<int64_t>(cv) * kVec;
+            float4 d0 = *reinterpret_cast<float4*>(dst), d1 = *reinterpret_cast<float4*>(dst + 4);
+            d0.x = fmaf(a.coef, acc[b][0], d0.x); d0.y = fmaf(a.coef, acc[b][1], d0.y);
+            d0.z = fmaf(a.coef, acc[b][2], d0.z); d0.w = fmaf(a.coef, acc[b][3], d0.w);
+            d1.x = fmaf(a.coef, acc[b][4], d1.x); d1.y = fmaf(a.coef, acc[b][5], d1.y);
+            d1.z = fmaf(a.coef, acc[b][6], d1.z); d1.w = fmaf(a.coef, acc[b][7], d1.w);
+            *reinterpret_cast<float4*>(dst) = d0;
+            *reinterpret_cast<float4*>(dst + 4) = d1;
+        }
     }
 }
 
@@ -364,35 +303,19 @@ cudaError_t launch_embedding_bwd_atomic(DType dt, float* dE, const void* dy, con
 
 cudaError_t launch_embedding_bwd(DType dt, float* dE, const void* dy, const uint8_t* mask,
                                  const int32_t* tokens, int64_t T, int64_t H, int64_t vocab,
-                                 float coef, uint64_t* sorted, cudaStream_t st) {
-    int n2 = 1;
-    while (n2 < T) n2 <<= 1;
-    cudaError_t e;
-    if (n2 <= kRegSortMax) {
-        // n2/4 threads, at least one warp (padding keys fill the rest)
-        const int n2r = std::max(n2, 32 * kRegKeys);
-        e = launch_pdl(emb_sort_reg_kernel, dim3(1), dim3(n2r / kRegKeys), 0, st, sorted, tokens,
-                       static_cast<int>(T), n2r, vocab);
-    } else {
-        const size_t smem = static_cast<size_t>(n2) * sizeof(uint64_t);
-        e = cudaFuncSetAttribute(emb_sort_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        e = launch_pdl(emb_sort_kernel, dim3(1), dim3(kSortThreads), smem, st, sorted, tokens,
-                       static_cast<int>(T), n2, vocab);
-    }
-    if (e != cudaSuccess) return e;
+                                 float coef, cudaStream_t st) {
     EmbBwdArgs a;
     a.T = static_cast<int>(T);
     a.nvr = static_cast<int>(H / kVec);
     a.H = H;
+    a.vocab = vocab;
     a.coef = coef;
     const dim3 grid(static_cast<unsigned>((T * 32 + kThreads - 1) / kThreads));
     if (dt == DType::F16)
-        return launch_pdl(emb_accum_kernel<__half>, grid, dim3(kThreads), 0, st, dE,
-                          static_cast<const __half*>(dy), mask, sorted, a);
-    return launch_pdl(emb_accum_kernel<float>, grid, dim3(kThreads), 0, st, dE,
-                      static_cast<const float*>(dy), mask, sorted, a);
+        return launch_pdl(emb_owner_kernel<__half>, grid, dim3(kThreads), 0, st, dE,
+                          static_cast<const __half*>(dy), mask, tokens, a);
+    return launch_pdl(emb_owner_kernel<float>, grid, dim3(kThreads), 0, st, dE,
+                      static_cast<const float*>(dy), mask, tokens, a);
 }
 
 }  // namespace ls

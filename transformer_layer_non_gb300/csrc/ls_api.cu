@@ -905,7 +905,8 @@ ls_status ls_embedding_fwd(ls_dtype dtype, void* y, uint32_t* mask_bits, const i
 }
 
 size_t ls_embedding_workspace_bytes(int64_t tokens) {
-    return tokens > 0 ? static_cast<size_t>(tokens) * sizeof(uint64_t) : 0;
+    (void)tokens;  // the deterministic backward needs no scratch
+    return 0;
 }
 
 ls_status ls_embedding_bwd(ls_dtype dtype, float* d_token_table, const void* dy,
@@ -946,25 +947,21 @@ ls_status ls_embedding_bwd(ls_dtype dtype, float* d_token_table, const void* dy,
     LS_TRY(check_ptr(d_token_table, "d_token_table", true));
     LS_TRY(check_ptr(dy, "dy", true));
     LS_TRY(check_ptr(mask_bits, "mask_bits", true));
-    LS_TRY(check_ptr(workspace, "workspace", true));
     if (!tokens) return fail(LS_ERR_INVALID_ARGUMENT, "tokens is NULL");
     if (reinterpret_cast<uintptr_t>(tokens) & 3u)
         return fail(LS_ERR_MISALIGNED, "tokens is not 4-byte aligned");
-    if (workspace_bytes < ls_embedding_workspace_bytes(T))
-        return fail(LS_ERR_WORKSPACE_TOO_SMALL, "ls_embedding_bwd: workspace of %zu bytes, need %zu",
-                    workspace_bytes, ls_embedding_workspace_bytes(T));
+    (void)workspace;  // none needed (ls_embedding_workspace_bytes is 0)
+    (void)workspace_bytes;
     const size_t es = elem_size(dt);
-    const Span outs[] = {{"d_token_table", d_token_table, static_cast<size_t>(vocab * hidden) * 4},
-                         {"workspace", workspace, ls_embedding_workspace_bytes(T)}};
+    const Span outs[] = {{"d_token_table", d_token_table, static_cast<size_t>(vocab * hidden) * 4}};
     const Span ins[] = {{"dy", dy, static_cast<size_t>(T * hidden) * es},
                         {"mask_bits", mask_bits, mask_bytes(T, hidden)},
                         {"tokens", tokens, static_cast<size_t>(T) * 4}};
-    LS_TRY(check_overlaps(outs, 2, ins, 3));
+    LS_TRY(check_overlaps(outs, 1, ins, 3));
     const float coef = static_cast<float>(static_cast<double>(scale) * rng.scale);
     return from_cuda(ls::launch_embedding_bwd(dt, d_token_table, dy,
                                               reinterpret_cast<const uint8_t*>(mask_bits), tokens,
                                               T, hidden, vocab, coef,
-                                              static_cast<uint64_t*>(workspace),
                                               static_cast<cudaStream_t>(stream)),
                      "ls_embedding_bwd launch");
 }

@@ -49,6 +49,12 @@ __host__ __device__ __forceinline__ uint32_t fmod_(uint32_t n, const FastDiv& f)
 // 8-element vectors.  Raw8<T> keeps the loaded bits (4 registers for FP16,
 // 8 for FP32) so that many loads can be in flight before any conversion.
 // ---------------------------------------------------------------------------
+// Asks L2 to fetch the line holding p (a valid global address); no register
+// is written, so the later load finds the line in L2.
+__device__ __forceinline__ void prefetch_l2(const void* p) {
+    asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
+}
+
 template <typename T> struct Raw8;
 template <> struct Raw8<__half> { uint4 v; };
 template <> struct Raw8<float> { float4 a, b; };

@@ -82,8 +82,9 @@ cudaError_t launch_qkv_bwd(DType dt, void* dqkv, float* partial, const void* dou
                            int64_t seq, int64_t heads, int64_t d, cudaStream_t s);
 
 // Embedding layer: gather + dropout forward; deterministic scatter-add
-// backward into an FP32 dE (one CTA sorts the batch's ids into `sorted`,
-// 8 bytes per token, at most kEmbeddingMaxTokens tokens per call).
+// backward into an FP32 dE (the warp of each id's first token adds the id's
+// rows in index order; each warp scans the earlier ids, so the work grows with
+// the square of the tokens: at most kEmbeddingMaxTokens per call).
 constexpr int64_t kEmbeddingMaxTokens = 16384;
 cudaError_t launch_embedding_fwd(DType dt, void* y, uint8_t* mask, const int32_t* tokens,
                                  const void* E, const void* P, int64_t batch, int64_t seq,
@@ -91,7 +92,7 @@ cudaError_t launch_embedding_fwd(DType dt, void* y, uint8_t* mask, const int32_t
                                  cudaStream_t st);
 cudaError_t launch_embedding_bwd(DType dt, float* dE, const void* dy, const uint8_t* mask,
                                  const int32_t* tokens, int64_t T, int64_t H, int64_t vocab,
-                                 float coef, uint64_t* sorted, cudaStream_t st);
+                                 float coef, cudaStream_t st);
 cudaError_t launch_embedding_bwd_atomic(DType dt, float* dE, const void* dy, const uint8_t* mask,
                                         const int32_t* tokens, int64_t T, int64_t H,
                                         int64_t vocab, float coef, cudaStream_t st);

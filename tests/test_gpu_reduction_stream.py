@@ -180,3 +180,23 @@ def test_reset_while_pending_is_refused(ref):
     finally:
         ls_ops.set_reduction_stream(None)
     torch.cuda.synchronize()
+
+
+def test_noalloc_entry_never_forks(ref):
+    # The allocation-free LayerNorm backward keeps its partial sums in one
+    # library-owned scratch, so it reduces on the caller's stream even with a
+    # reduction stream set: the gradients are ready without a join.
+    d, want = ref
+    side = torch.cuda.Stream()
+    o = _outputs()
+    ls_ops.set_reduction_stream(side)
+    try:
+        ls_ops.ls_layernorm_bwd_noalloc(o["ln_dx"], o["dgamma"], o["dbeta"], d["ln_dy"],
+                                        d["ln_x"], d["gamma"], d["mean"], d["rstd"])
+        ls_ops.set_reduction_stream(None)  # nothing pending: accepted
+    finally:
+        ls_ops.set_reduction_stream(None)
+    torch.cuda.synchronize()
+    got = _bits(o)
+    for k in ("ln_dx", "dgamma", "dbeta"):
+        np.testing.assert_array_equal(got[k], want[k], k)

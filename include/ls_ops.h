@@ -129,7 +129,9 @@ size_t ls_colreduce_workspace_bytes(int64_t rows, int64_t cols);
  * (rs, 18 CUDA events of the current device, up to 16 pending reductions) is
  * per host thread.  Errors: LS_ERR_INVALID_ARGUMENT if reductions are pending
  * (join first); LS_ERR_CUDA if the events cannot be created.
- * ls_layernorm_bwd_noalloc never forks. */
+ * ls_layernorm_bwd_noalloc follows the reduction stream too; its built-in
+ * scratch is ordered like a workspace (a later call waits for the pending
+ * reduction that reads it). */
 ls_status ls_set_reduction_stream(void* reduce_stream);
 
 /* Makes stream wait for every reduction forked since the last join (no-op if

@@ -9,7 +9,7 @@ import numpy as np
 import pytest
 
 from tests.gpu_util import dev, require_gpu
-from transformer_layer_non_gb300 import ls_ops, synth
+from transformer_layer_non_gb300 import ls_ops
 
 torch = pytest.importorskip("torch")
 pytestmark = pytest.mark.gpu
@@ -182,21 +182,23 @@ def test_reset_while_pending_is_refused(ref):
     torch.cuda.synchronize()
 
 
-def test_noalloc_entry_never_forks(ref):
-    # The allocation-free LayerNorm backward keeps its partial sums in one
-    # library-owned scratch, so it reduces on the caller's stream even with a
-    # reduction stream set: the gradients are ready without a join.
+def test_noalloc_entry_follows_the_reduction_stream(ref):
+    # The allocation-free LayerNorm backward forks like ls_layernorm_bwd; its
+    # one built-in scratch is tracked as the pending reduction's workspace, so
+    # a second call right after the first waits for the first reduction.
     d, want = ref
     side = torch.cuda.Stream()
-    o = _outputs()
+    outs = [_outputs(), _outputs()]
     ls_ops.set_reduction_stream(side)
     try:
-        ls_ops.ls_layernorm_bwd_noalloc(o["ln_dx"], o["dgamma"], o["dbeta"], d["ln_dy"],
-                                        d["ln_x"], d["gamma"], d["mean"], d["rstd"])
-        ls_ops.set_reduction_stream(None)  # nothing pending: accepted
+        for o in outs:
+            ls_ops.ls_layernorm_bwd_noalloc(o["ln_dx"], o["dgamma"], o["dbeta"], d["ln_dy"],
+                                            d["ln_x"], d["gamma"], d["mean"], d["rstd"])
+        ls_ops.join_reductions()
     finally:
         ls_ops.set_reduction_stream(None)
     torch.cuda.synchronize()
-    got = _bits(o)
-    for k in ("ln_dx", "dgamma", "dbeta"):
-        np.testing.assert_array_equal(got[k], want[k], k)
+    for o in outs:
+        got = _bits(o)
+        for k in ("ln_dx", "dgamma", "dbeta"):
+            np.testing.assert_array_equal(got[k], want[k], k)

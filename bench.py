@@ -61,7 +61,8 @@ def parse_args():
     ap.add_argument("--details", default=None, help="also write a per-op JSON report here")
     ap.add_argument("--profile-op", default=None,
                     help="run the layer once, then only this operator ('all': every operator "
-                         "in layer order) inside the NVTX range 'profile' (for ncu --nvtx "
+                         "in layer order; softmax_long_fwd / softmax_long_bwd: rows of 65536 "
+                         "keys) inside the NVTX range 'profile' (for ncu --nvtx "
                          "--nvtx-include profile/); no timing")
     ap.add_argument("--profile-launches", type=int, default=2)
     ap.add_argument("--reductions", default="side", choices=["side", "inline"],
@@ -810,6 +811,47 @@ def run_ours(args):
     return 0
 
 
+LONG_PROFILE_K_LEN = 65536  # two-pass softmax rows, 2^26 elements (128 MB of FP16)
+
+
+def run_profile_long_softmax(args):
+    """--profile-op softmax_long_fwd|softmax_long_bwd: rows of 65536 keys (the
+    two-pass kernels), 2^26 elements with random valid lengths, the operator
+    called --profile-launches times inside the NVTX range 'profile'."""
+    import torch
+
+    from transformer_layer_non_gb300 import accounting, ls_ops, synth
+    from transformer_layer_non_gb300.ncu_report import kernels_sha
+
+    ls_ops.load()
+    dev = torch.device("cuda", 0)
+    x, dy, kl = synth.sweep_inputs(LONG_PROFILE_K_LEN, args.seed, SWEEP_LONG_ELEMENTS)
+    b, h, q, k = x.shape
+    t = {"x": torch.from_numpy(x).to(dev), "dy": torch.from_numpy(dy).to(dev),
+         "kl": torch.from_numpy(kl).to(dev)}
+    t["y"] = torch.empty_like(t["x"])
+    t["dx"] = torch.empty_like(t["x"])
+    ls_ops.ls_softmax_fwd(t["y"], t["x"], t["kl"], False)
+    torch.cuda.synchronize()
+    fwd = args.profile_op == "softmax_long_fwd"
+    nbytes = (accounting.softmax_fwd_bytes if fwd else accounting.softmax_bwd_bytes)(
+        b, h, q, k, 2, kl, False)
+    torch.cuda.nvtx.range_push("profile")
+    for _ in range(args.profile_launches):
+        if fwd:
+            ls_ops.ls_softmax_fwd(t["y"], t["x"], t["kl"], False)
+        else:
+            ls_ops.ls_softmax_bwd(t["dx"], t["y"], t["dy"], t["kl"], False)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    print(json.dumps({"profile_op": args.profile_op,
+                      "workload": f"softmax rows of {LONG_PROFILE_K_LEN} keys, 2^26 elements",
+                      "kernels_sha": kernels_sha(), "launches_per_op": args.profile_launches,
+                      "launch_order": [args.profile_op] * args.profile_launches,
+                      "algorithmic_bytes": {args.profile_op: int(nbytes)}}))
+    return 0
+
+
 def run_profile_op(args):
     """One eager pass of the whole layer (so backward inputs exist), then, inside
     the NVTX range 'profile', --profile-launches calls of one operator, or of
@@ -819,6 +861,8 @@ def run_profile_op(args):
 
     from transformer_layer_non_gb300 import ls_ops, synth
 
+    if args.profile_op in ("softmax_long_fwd", "softmax_long_bwd"):
+        return run_profile_long_softmax(args)
     ls_ops.load()
     step = LayerStep(synth.LAYERS[args.workload], args.seed, torch.device("cuda", 0))
     ops = step.ops()

@@ -121,7 +121,7 @@ def test_sweep_every_element(k_len):
     ((2, 2, 8, 8192), False), ((1, 2, 3, 16384), True), ((3, 2, 5, 24), True),
     ((2, 3, 7, 40), False), ((2, 1, 9, 264), True), ((1, 1, 300, 1032), True),
     ((2, 2, 16, 8), True), ((1, 2, 3, 16392), True), ((2, 1, 2, 65536), False),
-    ((1, 1, 2, 262144), True), ((2, 1, 3, 14344), False)])
+    ((1, 1, 2, 262144), True), ((2, 1, 3, 14344), False), ((1, 1, 2, 1 << 20), False)])
 def test_odd_lengths_and_masks(dtype, shape, causal):
     # k_len classes between the sweep points, q_len != k_len with the causal
     # diagonal, and key lengths that are 0, negative, 1, or past k_len.

@@ -62,7 +62,8 @@ def test_sweep_row_lengths(k_len):
 @pytest.mark.parametrize("dtype", ["f16", "f32"])
 @pytest.mark.parametrize("shape,causal", [((2, 3, 5, 24), False), ((1, 2, 7, 136), True),
                                           ((2, 2, 33, 40), True), ((1, 1, 3, 2056), False),
-                                          ((1, 1, 3, 65544), True), ((2, 1, 2, 16400), False)])
+                                          ((1, 1, 3, 65544), True), ((2, 1, 2, 16400), False),
+                                          ((1, 1, 2, 1 << 20), True)])
 def test_odd_shapes_and_masks(dtype, shape, causal):
     require_gpu()
     b = shape[0]

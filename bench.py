@@ -49,7 +49,7 @@ SWEEP_LONG_ELEMENTS = 1 << 26
 def parse_args():
     ap = argparse.ArgumentParser(description=__doc__, formatter_class=argparse.RawTextHelpFormatter)
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=10000)
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["transformer-base", "bert-base", "gpt2-large", "tiny"])
@@ -430,7 +430,8 @@ def ncu_traffic(kernel_key, workload):
 # ---------------------------------------------------------------------------
 def oracle_sample_step(layer, frac, seed=0):
     """Build a bounded sample of the layer (a fraction of its rows and of its
-    (batch, head) score slices) and return (run, algorithmic_bytes)."""
+    (batch, head) score slices, at least 8 rows and one slice) and return
+    (run, algorithmic_bytes, row fraction, description)."""
     import numpy as np
 
     import oracle
@@ -440,15 +441,17 @@ def oracle_sample_step(layer, frac, seed=0):
     T, H, F = L.tokens, L.hidden, L.ffn
     d = synth.layer_inputs(L, seed)
     rows = max(8, int(round(T * frac)))
-    nb = max(1, int(round(L.batch * frac)))
+    nsl = max(1, int(round(L.batch * L.heads * frac)))  # (batch, head) score slices
     es = 2 if L.dtype == "f16" else 4
     f64 = lambda a: np.ascontiguousarray(a, dtype=np.float64)  # noqa: E731
     s = {k: f64(v) for k, v in d.items() if k not in ("scores", "scores_dy", "key_len")}
     s = {k: (v[:rows] if v.ndim == 2 else v) for k, v in s.items()}
-    sc = f64(d["scores"][:nb])
-    sdy = f64(d["scores_dy"][:nb])
+    # Slices as a [nsl, 1, Lq, Lk] batch, each with its batch element's key length.
+    sq = (L.batch * L.heads, 1, L.seq, L.seq)
+    sc = f64(d["scores"].reshape(sq)[:nsl])
+    sdy = f64(d["scores_dy"].reshape(sq)[:nsl])
     kl = d.get("key_len")
-    kl = None if kl is None else kl[:nb]
+    kl = None if kl is None else np.ascontiguousarray(np.repeat(kl, L.heads)[:nsl])
     p, eps = L.p, 1e-5
 
     def run():
@@ -465,9 +468,9 @@ def oracle_sample_step(layer, frac, seed=0):
         oracle.bias_dropout_residual_bwd(s["attn_dout"], m1, p)
         oracle.softmax_bwd(pr, sdy, kl, L.causal)
 
-    b = accounting.layer_step_bytes(rows, H, F, nb, L.heads, L.seq, es, kl, L.causal)
-    sample = (f"{rows} of {T} token rows and {nb} of {L.batch} batch elements' score "
-              f"tensors of {L.name}, every operator forward and backward")
+    b = accounting.layer_step_bytes(rows, H, F, nsl, 1, L.seq, es, kl, L.causal)
+    sample = (f"{rows} of {T} token rows and {nsl} of {L.batch * L.heads} (batch, head) "
+              f"score slices of {L.name}, every operator forward and backward")
     return run, sum(b.values()), rows / T, sample
 
 
@@ -529,7 +532,9 @@ def run_reference(args):
     from transformer_layer_non_gb300 import synth
 
     layer = synth.LAYERS[args.workload]
-    per_step = max(0.5, min(2.0, 90.0 / (args.steps + args.warmup)))
+    # Each step a sample sized so that the whole run takes about 90 s (at most
+    # 2 s a step; one score slice, a few ms, is the smallest sample).
+    per_step = min(2.0, 90.0 / (args.steps + args.warmup))
     run, nbytes, frac, sample = calibrated_oracle(layer, per_step, args.seed)
     for _ in range(args.warmup):
         run()

@@ -234,9 +234,9 @@ ls_status ls_layernorm_bwd_noalloc(ls_dtype dtype, void* dx, void* dgamma, void*
  * j <= q + k_len - q_len.  On valid entries y = exp(x - m) / sum(exp(x - m)),
  * m = max of the valid x; masked entries are written as exactly 0 and are
  * not read; a row with no valid key is all zeros.  No 1/sqrt(d) scaling is
- * applied (the score GEMM applies it).  k_len <= 2^20; rows of up to 16384
- * keys are held on chip and read once, longer rows are read twice (an online
- * maximum-and-sum pass, then the output pass).  y may be x. */
+ * applied (the score GEMM applies it).  k_len <= 2^20; rows of up to 4096
+ * keys (backward: 16384) are held on chip and read once, longer rows are read
+ * twice (an online maximum-and-sum pass, then the output pass).  y may be x. */
 ls_status ls_softmax_fwd(ls_dtype dtype, void* y, const void* x, int64_t batch, int64_t heads,
                          int64_t q_len, int64_t k_len, const int32_t* key_len, int causal,
                          void* stream);

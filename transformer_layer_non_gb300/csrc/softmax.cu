@@ -14,7 +14,7 @@
 //   nvec > 128        a CTA per row (4 or 8 warps), partial results of the two
 //                     reductions through shared memory.
 //   nvec > 2048       a CTA per row that reads the row twice: an online
-//   (fwd: > 1792)     (maximum, sum) pass, then the output pass.
+//   (fwd: > 512)      (maximum, sum) pass, then the output pass.
 // Masked keys are never loaded: a lane loads a vector only if it holds at
 // least one valid key; masked outputs are written as exact zeros.
 #include <math.h>
@@ -645,8 +645,12 @@ softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
 // epilogue).  Backward: the first pass sums y*g, the second writes dx.  The
 // row's second read comes from L2 (a row is at most 2 MB).
 // ----------------------------------------------------------------------------
+// CTA sizes: the forward takes 256 threads for rows of up to 32768 keys (four
+// rows in flight per SM hide its two phases better: 0.76 against 0.52 of the
+// copy bandwidth at 16384 keys) and 512 for longer rows; the backward 512.
 constexpr int kStreamThreads = 512;
-constexpr int kStreamWarps = kStreamThreads / 32;
+constexpr int kStreamThreadsShort = 256;
+constexpr int64_t kStreamShortMaxLen = 32768;
 // Vectors per thread in flight: 64 bytes of either storage type.
 template <typename T>
 constexpr int stream_unroll() { return sizeof(T) == 2 ? 4 : 2; }
@@ -658,24 +662,25 @@ __device__ __forceinline__ void online_merge(float& m, float& l, float m2, float
     m = mm;
 }
 
-// Loads the vectors v0 + u * kStreamThreads (u < U) of a row that
-// hold at least one of its vlen valid elements.
-template <typename T, int U>
+// Loads the vectors v0 + u * THREADS (u < U) of a row that hold at least one
+// of its vlen valid elements.
+template <typename T, int U, int THREADS>
 __device__ __forceinline__ void stream_load(Raw8<T> (&r)[U], const T* row_ptr, int v0,
                                             int vlen) {
 #pragma unroll
     for (int u = 0; u < U; ++u) {
-        const int v = v0 + u * kStreamThreads;
+        const int v = v0 + u * THREADS;
         if (v * kVec < vlen) r[u] = load8<T>(row_ptr + v * kVec);
     }
 }
 
-template <typename T, bool DROP>
-__global__ void __launch_bounds__(kStreamThreads, 2)
+template <typename T, bool DROP, int THREADS>
+__global__ void __launch_bounds__(THREADS, 2)
 softmax_fwd_stream_kernel(T* y, const T* x, int k_len, RowMask mk,
                           const __grid_constant__ DropArgs d) {
     constexpr int U = stream_unroll<T>();
-    __shared__ float sm_m[kStreamWarps], sm_l[kStreamWarps];
+    constexpr int kWarps = THREADS / 32;
+    __shared__ float sm_m[kWarps], sm_l[kWarps];
     pdl_enter();
     if (DROP) drop_tail(d);
     const int64_t row = blockIdx.x;
@@ -683,12 +688,12 @@ softmax_fwd_stream_kernel(T* y, const T* x, int k_len, RowMask mk,
     const int nvec = k_len / kVec;
     const int64_t base = row * k_len;
     float m = -INFINITY, l = 0.f;
-    for (int v0 = threadIdx.x; v0 * kVec < vlen; v0 += kStreamThreads * U) {
+    for (int v0 = threadIdx.x; v0 * kVec < vlen; v0 += THREADS * U) {
         Raw8<T> r[U];
-        stream_load<T, U>(r, x + base, v0, vlen);
+        stream_load<T, U, THREADS>(r, x + base, v0, vlen);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int v = v0 + u * kStreamThreads;
+            const int v = v0 + u * THREADS;
             const int cnt = min(vlen - v * kVec, kVec);
             if (cnt <= 0) break;
             float f[kVec];
@@ -715,15 +720,15 @@ softmax_fwd_stream_kernel(T* y, const T* x, int k_len, RowMask mk,
     }
     __syncthreads();
     float M = sm_m[0], L = sm_l[0];
-    for (int w = 1; w < kStreamWarps; ++w) online_merge(M, L, sm_m[w], sm_l[w]);
+    for (int w = 1; w < kWarps; ++w) online_merge(M, L, sm_m[w], sm_l[w]);
     const float ml = M == -INFINITY ? 0.f : M * kLog2e;
     const float inv = L > 0.f ? __fdividef(1.f, L) : 0.f;
-    for (int v0 = threadIdx.x; v0 < nvec; v0 += kStreamThreads * U) {
+    for (int v0 = threadIdx.x; v0 < nvec; v0 += THREADS * U) {
         Raw8<T> r[U];
-        stream_load<T, U>(r, x + base, v0, vlen);
+        stream_load<T, U, THREADS>(r, x + base, v0, vlen);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
-            const int v = v0 + u * kStreamThreads;
+            const int v = v0 + u * THREADS;
             if (v >= nvec) break;
             const int cnt = min(max(vlen - v * kVec, 0), kVec);
             float o[kVec];
@@ -748,7 +753,8 @@ __global__ void __launch_bounds__(kStreamThreads, 2)
 softmax_bwd_stream_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
                           const __grid_constant__ DropArgs d) {
     constexpr int U = stream_unroll<T>();
-    __shared__ float red[kStreamWarps];
+    constexpr int kWarps = kStreamThreads / 32;
+    __shared__ float red[kWarps];
     pdl_enter();
     const int64_t row = blockIdx.x;
     const int vlen = valid_len(row, k_len, mk);
@@ -773,8 +779,8 @@ softmax_bwd_stream_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
     for (int v0 = threadIdx.x; v0 * kVec < vlen; v0 += kStreamThreads * U) {
         Raw8<T> ry[U], rg[U];
         uint32_t mb[U];
-        stream_load<T, U>(ry, y + base, v0, vlen);
-        stream_load<T, U>(rg, dy + base, v0, vlen);
+        stream_load<T, U, kStreamThreads>(ry, y + base, v0, vlen);
+        stream_load<T, U, kStreamThreads>(rg, dy + base, v0, vlen);
         load_bits(mb, v0);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -789,12 +795,12 @@ softmax_bwd_stream_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
                 if (j < cnt) dot = fmaf(yf[j], g[j], dot);
         }
     }
-    dot = cta_sum<kStreamWarps>(dot, red);
+    dot = cta_sum<kWarps>(dot, red);
     for (int v0 = threadIdx.x; v0 < nvec; v0 += kStreamThreads * U) {
         Raw8<T> ry[U], rg[U];
         uint32_t mb[U];
-        stream_load<T, U>(ry, y + base, v0, vlen);
-        stream_load<T, U>(rg, dy + base, v0, vlen);
+        stream_load<T, U, kStreamThreads>(ry, y + base, v0, vlen);
+        stream_load<T, U, kStreamThreads>(rg, dy + base, v0, vlen);
         load_bits(mb, v0);
 #pragma unroll
         for (int u = 0; u < U; ++u) {
@@ -826,13 +832,14 @@ struct SmPlan {
     int64_t grid;
 };
 
-// Longest rows held in registers: 8 warps x 8 vectors x 8 elements.  The
-// forward at 8 vectors per lane needs so many registers that only two CTAs
-// fit on an SM, and measured slower than the two-pass kernel at 16384 keys
-// (the backward is even there), so forward rows past 7 vectors per lane
-// stream.
+// Longest rows held in registers: 8 warps x 8 vectors x 8 elements for the
+// backward.  The forward streams from 4104 keys on: measured on 2^26 FP16
+// elements, the CTA-per-row forward reaches 0.60 of the copy bandwidth at
+// 2048 and 4096 keys (the two-pass kernel 0.29 / 0.46) but 0.57 at 8192
+// (two-pass, 256 threads: 0.67), and at 8 vectors per lane it needs 128
+// registers (0.36 at 16384 keys against 0.76).
 constexpr int64_t kMaxRegisterRowLen = 16384;
-constexpr int64_t kMaxRegisterRowLenFwd = 8 * 32 * 7 * kVec;  // 14336
+constexpr int64_t kMaxRegisterRowLenFwd = 4096;
 
 SmPlan plan_for(int64_t nrows, int64_t k_len, bool fwd) {
     const int nvec = static_cast<int>(k_len / kVec);
@@ -988,9 +995,13 @@ cudaError_t fwd_dispatch(void* y, const void* x, const SoftmaxShape& sh, const D
     const SmPlan p = plan_for(nrows, sh.k_len, true);
     const RowMask m = make_mask(sh);
     if (p.stream)
-        return launch_pdl(softmax_fwd_stream_kernel<T, DROP>, dim3(static_cast<unsigned>(p.grid)),
-                          dim3(kStreamThreads), 0, s, static_cast<T*>(y),
-                          static_cast<const T*>(x), k_len, m, d);
+        return sh.k_len <= kStreamShortMaxLen
+                   ? launch_pdl(softmax_fwd_stream_kernel<T, DROP, kStreamThreadsShort>,
+                                dim3(static_cast<unsigned>(p.grid)), dim3(kStreamThreadsShort), 0,
+                                s, static_cast<T*>(y), static_cast<const T*>(x), k_len, m, d)
+                   : launch_pdl(softmax_fwd_stream_kernel<T, DROP, kStreamThreads>,
+                                dim3(static_cast<unsigned>(p.grid)), dim3(kStreamThreads), 0, s,
+                                static_cast<T*>(y), static_cast<const T*>(x), k_len, m, d);
     if (!p.cta) {
         LS_SM_GROUP_CASES(fwd_group, LS_SM_T_DROP, y, x, nrows, k_len, m, d, p, s)
     } else {

@@ -61,10 +61,12 @@ def parse_args():
     ap.add_argument("--details", default=None, help="also write a per-op JSON report here")
     ap.add_argument("--profile-op", default=None,
                     help="run the layer once, then only this operator ('all': every operator "
-                         "in layer order; softmax_long_fwd / softmax_long_bwd: rows of 65536 "
-                         "keys) inside the NVTX range 'profile' (for ncu --nvtx "
+                         "in layer order; softmax_long_fwd / softmax_long_bwd: rows of "
+                         "--profile-k-len keys) inside the NVTX range 'profile' (for ncu --nvtx "
                          "--nvtx-include profile/); no timing")
     ap.add_argument("--profile-launches", type=int, default=2)
+    ap.add_argument("--profile-k-len", type=int, default=65536,
+                    help="row length of --profile-op softmax_long_fwd/bwd (2^26 elements)")
     ap.add_argument("--reductions", default="side", choices=["side", "inline"],
                     help="layer step: fork the backward column reductions onto a second "
                          "stream (side) or keep them on the step's stream (inline)")
@@ -825,13 +827,11 @@ def run_ours(args):
     return 0
 
 
-LONG_PROFILE_K_LEN = 65536  # two-pass softmax rows, 2^26 elements (128 MB of FP16)
-
-
 def run_profile_long_softmax(args):
-    """--profile-op softmax_long_fwd|softmax_long_bwd: rows of 65536 keys (the
-    two-pass kernels), 2^26 elements with random valid lengths, the operator
-    called --profile-launches times inside the NVTX range 'profile'."""
+    """--profile-op softmax_long_fwd|softmax_long_bwd: rows of --profile-k-len
+    keys (default 65536: the two-pass kernels), 2^26 elements (128 MB of FP16)
+    with random valid lengths, the operator called --profile-launches times
+    inside the NVTX range 'profile'."""
     import torch
 
     from transformer_layer_non_gb300 import accounting, ls_ops, synth
@@ -839,7 +839,8 @@ def run_profile_long_softmax(args):
 
     ls_ops.load()
     dev = torch.device("cuda", 0)
-    x, dy, kl = synth.sweep_inputs(LONG_PROFILE_K_LEN, args.seed, SWEEP_LONG_ELEMENTS)
+    k_len = args.profile_k_len
+    x, dy, kl = synth.sweep_inputs(k_len, args.seed, SWEEP_LONG_ELEMENTS)
     b, h, q, k = x.shape
     t = {"x": torch.from_numpy(x).to(dev), "dy": torch.from_numpy(dy).to(dev),
          "kl": torch.from_numpy(kl).to(dev)}
@@ -859,7 +860,7 @@ def run_profile_long_softmax(args):
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     print(json.dumps({"profile_op": args.profile_op,
-                      "workload": f"softmax rows of {LONG_PROFILE_K_LEN} keys, 2^26 elements",
+                      "workload": f"softmax rows of {k_len} keys, 2^26 elements",
                       "kernels_sha": kernels_sha(), "launches_per_op": args.profile_launches,
                       "launch_order": [args.profile_op] * args.profile_launches,
                       "algorithmic_bytes": {args.profile_op: int(nbytes)}}))

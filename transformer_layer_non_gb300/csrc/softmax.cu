@@ -540,23 +540,43 @@ softmax_fwd_cta_kernel(T* y, const T* x, int k_len, RowMask mk,
         const int v = threadIdx.x + k * NT;
         if (v * kVec < vlen) {
             load8f<T>(x + base + v * kVec, f[k]);
+            if ((v + 1) * kVec <= vlen) {  // a whole vector: no per-element tests
 #pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                if (v * kVec + j < vlen) m = fmaxf(m, f[k][j]);
+                for (int j = 0; j < kVec; ++j) m = fmaxf(m, f[k][j]);
+            } else {
+#pragma unroll
+                for (int j = 0; j < kVec; ++j)
+                    if (v * kVec + j < vlen) m = fmaxf(m, f[k][j]);
+            }
         }
     }
     m = cta_max<WARPS>(m, red);
-    const float ml = m * kLog2e;
+    const float ml = m == -INFINITY ? 0.f : m * kLog2e;  // no valid or all -inf: e = 0
     float s = 0.f;
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = threadIdx.x + k * NT;
+        if ((v + 1) * kVec <= vlen) {  // exponentials two at a time
+            float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            const bool on = v * kVec + j < vlen;
-            const float e = on ? exp2f(fmaf(f[k][j], kLog2e, -ml)) : 0.f;
-            f[k][j] = e;
-            s += e;
+            for (int j = 0; j < kVec; j += 2) {
+                float2 t = fma2(make_float2(f[k][j], f[k][j + 1]), make_float2(kLog2e, kLog2e),
+                                make_float2(-ml, -ml));
+                t.x = exp2_approx(t.x);
+                t.y = exp2_approx(t.y);
+                f[k][j] = t.x;
+                f[k][j + 1] = t.y;
+                acc = add2(acc, t);
+            }
+            s += acc.x + acc.y;
+        } else {
+#pragma unroll
+            for (int j = 0; j < kVec; ++j) {
+                const bool on = v * kVec + j < vlen;
+                const float e = on ? exp2_approx(fmaf(f[k][j], kLog2e, -ml)) : 0.f;
+                f[k][j] = e;
+                s += e;
+            }
         }
     }
     s = cta_sum<WARPS>(s, red);
@@ -567,7 +587,11 @@ softmax_fwd_cta_kernel(T* y, const T* x, int k_len, RowMask mk,
         if (v < nvec) {
             float o[kVec];
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) o[j] = f[k][j] * inv;
+            for (int j = 0; j < kVec; j += 2) {
+                const float2 t = mul2(make_float2(f[k][j], f[k][j + 1]), make_float2(inv, inv));
+                o[j] = t.x;
+                o[j + 1] = t.y;
+            }
             store8f<T>(y + base + v * kVec, o);
             if (DROP) drop_store<T>(o, base, v, vlen, d);
         }
@@ -605,7 +629,9 @@ softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = threadIdx.x + k * NT;
-        if (v * kVec < vlen) {
+        if (!DROP && (v + 1) * kVec <= vlen) {  // a whole vector: no per-element tests
+            dot = dot8_acc(yr[k], dr[k], dot);
+        } else if (v * kVec < vlen) {
             float yf[kVec], df[kVec];
             unpack(yr[k], yf);
             unpack(dr[k], df);
@@ -620,7 +646,18 @@ softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
         const int v = threadIdx.x + k * NT;
         if (v < nvec) {
             float o[kVec];
-            if (v * kVec < vlen) {
+            if (!DROP && (v + 1) * kVec <= vlen) {  // (dy - dot) * y, two at a time
+                float yf[kVec];
+                unpack(yr[k], yf);
+                sub8(dr[k], dot, o);
+#pragma unroll
+                for (int j = 0; j < kVec; j += 2) {
+                    const float2 t = mul2(make_float2(o[j], o[j + 1]),
+                                          make_float2(yf[j], yf[j + 1]));
+                    o[j] = t.x;
+                    o[j + 1] = t.y;
+                }
+            } else if (v * kVec < vlen) {
                 float yf[kVec], df[kVec];
                 unpack(yr[k], yf);
                 unpack(dr[k], df);
@@ -698,6 +735,27 @@ softmax_fwd_stream_kernel(T* y, const T* x, int k_len, RowMask mk,
             if (cnt <= 0) break;
             float f[kVec];
             unpack(r[u], f);
+            if (cnt == kVec) {
+                // a whole vector (every one but the row's last): packed maximum,
+                // exponentials two at a time
+                const float vm = vmax8(r[u]);
+                if (vm > m) {  // rescale the running sum to the new maximum
+                    l *= exp2_approx((m - vm) * kLog2e);
+                    m = vm;
+                }
+                const float ml = m == -INFINITY ? 0.f : m * kLog2e;  // all -inf so far: e = 0
+                float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < kVec; j += 2) {
+                    float2 t = fma2(make_float2(f[j], f[j + 1]), make_float2(kLog2e, kLog2e),
+                                    make_float2(-ml, -ml));
+                    t.x = exp2_approx(t.x);
+                    t.y = exp2_approx(t.y);
+                    acc = add2(acc, t);
+                }
+                l += acc.x + acc.y;
+                continue;
+            }
             float vm = -INFINITY;
 #pragma unroll
             for (int j = 0; j < kVec; ++j) vm = fmaxf(vm, j < cnt ? f[j] : -INFINITY);
@@ -732,7 +790,20 @@ softmax_fwd_stream_kernel(T* y, const T* x, int k_len, RowMask mk,
             if (v >= nvec) break;
             const int cnt = min(max(vlen - v * kVec, 0), kVec);
             float o[kVec];
-            if (cnt > 0) {
+            if (cnt == kVec) {
+                float f[kVec];
+                unpack(r[u], f);
+#pragma unroll
+                for (int j = 0; j < kVec; j += 2) {
+                    float2 t = fma2(make_float2(f[j], f[j + 1]), make_float2(kLog2e, kLog2e),
+                                    make_float2(-ml, -ml));
+                    t.x = exp2_approx(t.x);
+                    t.y = exp2_approx(t.y);
+                    t = mul2(t, make_float2(inv, inv));
+                    o[j] = t.x;
+                    o[j + 1] = t.y;
+                }
+            } else if (cnt > 0) {
                 float f[kVec];
                 unpack(r[u], f);
 #pragma unroll
@@ -787,6 +858,10 @@ softmax_bwd_stream_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
             const int v = v0 + u * kStreamThreads;
             const int cnt = min(vlen - v * kVec, kVec);
             if (cnt <= 0) break;
+            if (!DROP && cnt == kVec) {  // a whole vector: no per-element tests
+                dot = dot8_acc(ry[u], rg[u], dot);
+                continue;
+            }
             float yf[kVec], g[kVec];
             unpack(ry[u], yf);
             grads(rg[u], mb[u], g);
@@ -808,7 +883,18 @@ softmax_bwd_stream_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
             if (v >= nvec) break;
             const int cnt = min(max(vlen - v * kVec, 0), kVec);
             float o[kVec];
-            if (cnt > 0) {
+            if (!DROP && cnt == kVec) {  // a whole vector: (dy - dot) * y, two at a time
+                float yf[kVec];
+                unpack(ry[u], yf);
+                sub8(rg[u], dot, o);
+#pragma unroll
+                for (int j = 0; j < kVec; j += 2) {
+                    const float2 t = mul2(make_float2(o[j], o[j + 1]),
+                                          make_float2(yf[j], yf[j + 1]));
+                    o[j] = t.x;
+                    o[j + 1] = t.y;
+                }
+            } else if (cnt > 0) {
                 float yf[kVec], g[kVec];
                 unpack(ry[u], yf);
                 grads(rg[u], mb[u], g);

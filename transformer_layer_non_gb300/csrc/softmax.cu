@@ -153,6 +153,12 @@ __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y,
         const int v = gl + k * LPR;
         const int cnt = min(max(vlen - v * kVec, 0), kVec);
         unpack(buf.a[k], f[k]);
+        if (LPR == 32 && (k + 1) * LPR * kVec <= vlen) {
+            // the warp's k-th slot lies wholly in the valid prefix (the same
+            // test in every lane): packed maximum, no per-element selects
+            m = fmaxf(m, vmax8(buf.a[k]));
+            continue;
+        }
 #pragma unroll
         for (int j = 0; j < kVec; ++j) {
             f[k][j] = j < cnt ? f[k][j] : -INFINITY;
@@ -161,15 +167,20 @@ __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y,
     }
     m = group_max<LPR>(m);
     const float ml = m == -INFINITY ? 0.f : m * kLog2e;  // empty row: every e is 0
-    float s = 0.f;
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < VPT; ++k)
 #pragma unroll
-        for (int j = 0; j < kVec; ++j) {
-            f[k][j] = exp2_approx(fmaf(f[k][j], kLog2e, -ml));  // -inf -> 0
-            s += f[k][j];
+        for (int j = 0; j < kVec; j += 2) {  // two at a time; -inf -> 0
+            float2 t = fma2(make_float2(f[k][j], f[k][j + 1]), make_float2(kLog2e, kLog2e),
+                            make_float2(-ml, -ml));
+            t.x = exp2_approx(t.x);
+            t.y = exp2_approx(t.y);
+            f[k][j] = t.x;
+            f[k][j + 1] = t.y;
+            acc = add2(acc, t);
         }
-    s = group_sum<LPR>(s);
+    float s = group_sum<LPR>(acc.x + acc.y);
     if (row >= nrows) return;
     const float inv = s > 0.f ? __fdividef(1.f, s) : 0.f;
     const int64_t base = row * k_len;
@@ -179,7 +190,11 @@ __device__ __forceinline__ void sm_fwd_row(const RowBuf<T, LPR, VPT>& buf, T* y,
         if (v < nvec) {
             float o[kVec];
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) o[j] = f[k][j] * inv;  // masked: 0 * inv = +0
+            for (int j = 0; j < kVec; j += 2) {  // masked: 0 * inv = +0
+                const float2 t = mul2(make_float2(f[k][j], f[k][j + 1]), make_float2(inv, inv));
+                o[j] = t.x;
+                o[j + 1] = t.y;
+            }
             store8f<T>(y + base + v * kVec, o);
             if (DROP) drop_store<T>(o, base, v, vlen, d);
         }

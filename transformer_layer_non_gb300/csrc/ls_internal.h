@@ -70,7 +70,7 @@ cudaError_t launch_softmax_dropout_bwd(DType dt, void* dx, const void* y, const 
                                        cudaStream_t s);
 
 constexpr int64_t kMaxRowLen = 16384;          // LayerNorm rows
-constexpr int64_t kMaxSoftmaxRowLen = 1 << 20;  // softmax rows (longer than 16384 stream)
+constexpr int64_t kMaxSoftmaxRowLen = 1 << 20;  // softmax rows (long rows read twice)
 
 // Bias + reshape of Q, K, V: [batch*seq, 3*heads*d] (+ bias) <-> [3, batch,
 // heads, seq, d].  The backward writes one FP32 partial row of the bias

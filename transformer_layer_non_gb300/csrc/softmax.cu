@@ -689,8 +689,8 @@ softmax_bwd_cta_kernel(T* dx, const T* y, const T* dy, int k_len, RowMask mk,
 }
 
 // ----------------------------------------------------------------------------
-// Rows longer than registers hold (k_len > 16384): a CTA per row streams the
-// valid prefix twice.  Forward: the first pass keeps each thread's running
+// Long rows (forward: k_len > 4096, backward: k_len > 16384): a CTA per row
+// streams the valid prefix twice.  Forward: the first pass keeps each thread's running
 // maximum and its rescaled running sum of exponentials -- the online softmax
 // normaliser of "CS336 Lecture 5: GPU", section 6.2 -- and the CTA merges the
 // pairs by the same rule; the second pass writes y (and the dropout
@@ -935,10 +935,10 @@ struct SmPlan {
 
 // Longest rows held in registers: 8 warps x 8 vectors x 8 elements for the
 // backward.  The forward streams from 4104 keys on: measured on 2^26 FP16
-// elements, the CTA-per-row forward reaches 0.60 of the copy bandwidth at
-// 2048 and 4096 keys (the two-pass kernel 0.29 / 0.46) but 0.57 at 8192
-// (two-pass, 256 threads: 0.67), and at 8 vectors per lane it needs 128
-// registers (0.36 at 16384 keys against 0.76).
+// elements, the CTA-per-row forward reaches 0.72 / 0.68 of the copy bandwidth
+// at 2048 / 4096 keys (the two-pass kernel 0.29 / 0.46) but 0.65 / 0.52 at
+// 8192 / 12288 keys (two-pass, 256 threads: 0.69 / 0.75); at 8 vectors per
+// lane it needs 128 registers.
 constexpr int64_t kMaxRegisterRowLen = 16384;
 constexpr int64_t kMaxRegisterRowLenFwd = 4096;
 

@@ -60,9 +60,22 @@ def read_ncu_csv(path):
 
 
 def short_name(kernel: str) -> str:
-    name = re.sub(r"\(.*$", "", kernel)
+    """The kernel's name and template arguments: the return type, the leading
+    namespaces (ncu writes the anonymous one as `unnamed>::`) and the trailing
+    argument list dropped."""
+    name = kernel.strip()
+    if name.endswith(")"):  # the argument list: back to its matching parenthesis
+        depth = 0
+        for i in range(len(name) - 1, -1, -1):
+            if name[i] == ")":
+                depth += 1
+            elif name[i] == "(":
+                depth -= 1
+                if depth == 0:
+                    name = name[:i]
+                    break
     name = re.sub(r"^void\s+", "", name)
-    return re.sub(r"^(\w+>::|\(anonymous namespace\)::|ls::)+", "", name)
+    return re.sub(r"^(\w+>::|<\w+>::|\(anonymous namespace\)::|\w+::)+", "", name)
 
 
 def value(row) -> float:

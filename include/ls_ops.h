@@ -129,9 +129,7 @@ size_t ls_colreduce_workspace_bytes(int64_t rows, int64_t cols);
  * (rs, 18 CUDA events of the current device, up to 16 pending reductions) is
  * per host thread.  Errors: LS_ERR_INVALID_ARGUMENT if reductions are pending
  * (join first); LS_ERR_CUDA if the events cannot be created.
- * ls_layernorm_bwd_noalloc follows the reduction stream too; its built-in
- * scratch is ordered like a workspace (a later call waits for the pending
- * reduction that reads it). */
+ * ls_layernorm_bwd_noalloc keeps its reduction on the caller's stream. */
 ls_status ls_set_reduction_stream(void* reduce_stream);
 
 /* Makes stream wait for every reduction forked since the last join (no-op if
@@ -211,14 +209,22 @@ ls_status ls_layernorm_bwd(ls_dtype dtype, void* dx, void* dgamma, void* dbeta, 
  *  - Every shape with cols <= 3448 fits; wider rows fit only for fewer rows.
  *    A shape whose partial sums need more scratch is rejected with
  *    LS_ERR_UNSUPPORTED_SHAPE before anything is enqueued.
- *  - The first call on a device looks up the array's device address
- *    (cudaGetSymbolAddress) with that device current.  Make that first call
- *    outside any stream capture.
+ *  - Every call looks up the array's device address in the current context
+ *    (cudaGetSymbolAddress; a query, not an allocation).  The array exists
+ *    once per context that has loaded the library, so the address is never
+ *    cached: calls stay correct in a second context on the same device and
+ *    after cudaDeviceReset.  The first call in a context also loads the
+ *    library's device code there; make that first call outside any stream
+ *    capture.
+ *  - The fixed-order reduction of the partial sums always runs on `stream`,
+ *    also while ls_set_reduction_stream is in effect (the scratch is shared
+ *    by every host thread, so a reduction forked onto another stream could
+ *    still be reading it when the next call overwrites it).
  *  - All calls share the one array, which keeps the last call's contents.  A
  *    call overwrites every scratch byte it reads, so nothing has to start at
- *    zero.  Calls that can overlap on the GPU (on different streams, or graphs
- *    replayed concurrently) race on the array and produce wrong dgamma/dbeta:
- *    order them on one stream.
+ *    zero.  Calls ordered on one stream, from any host thread, are safe.
+ *    Calls that can overlap on the GPU (on different streams, or graphs
+ *    replayed concurrently) race on the array and produce wrong dgamma/dbeta.
  * Arguments, layouts, aliasing and errors are otherwise those of
  * ls_layernorm_bwd; with dgamma = dbeta = NULL no scratch is used. */
 #define LS_NOALLOC_SCRATCH_BYTES ((size_t)8 << 20)

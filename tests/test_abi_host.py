@@ -296,3 +296,14 @@ def test_reduction_stream_default_and_empty_join(lib):
     assert lib.ls_set_reduction_stream(None) == ls_ops.LS_OK
     assert lib.ls_join_reductions(None) == ls_ops.LS_OK
     assert lib.ls_join_reductions(A) == ls_ops.LS_OK
+
+
+def test_noalloc_scratch_size_matches_the_header():
+    import re
+
+    from transformer_layer_non_gb300 import ls_ops
+
+    hdr = open(os.path.join(ROOT, "include", "ls_ops.h")).read()
+    m = re.search(r"#define LS_NOALLOC_SCRATCH_BYTES \(\(size_t\)(\d+) << (\d+)\)", hdr)
+    assert m, "LS_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert ls_ops.LS_NOALLOC_SCRATCH_BYTES == int(m.group(1)) << int(m.group(2))

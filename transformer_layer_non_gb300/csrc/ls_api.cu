@@ -102,9 +102,10 @@ cudaError_t guard_workspace(cudaStream_t s, const void* ws, size_t bytes) {
 // Launches a column reduction fn(stream) that reads [ws, ws + bytes): on s,
 // or forked onto the reduction stream after s's work so far.
 template <typename F>
-cudaError_t launch_reduction(cudaStream_t s, const void* ws, size_t bytes, F fn) {
+cudaError_t launch_reduction(cudaStream_t s, const void* ws, size_t bytes, F fn,
+                             bool inline_only = false) {
     ReductionState& r = t_red;
-    if (!r.active) return fn(s);
+    if (!r.active || inline_only) return fn(s);
     int dev = -1;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
@@ -494,6 +495,18 @@ ls_status ls_layernorm_bwd(ls_dtype dtype, void* dx, void* dgamma, void* dbeta, 
                            const void* x, const void* gamma, const float* mean, const float* rstd,
                            int64_t rows, int64_t cols, void* workspace, size_t workspace_bytes,
                            void* stream) {
+    return ls::layernorm_bwd_entry(dtype, dx, dgamma, dbeta, dy, x, gamma, mean, rstd, rows, cols,
+                                   workspace, workspace_bytes, stream, false);
+}
+
+}  // extern "C"
+#pragma GCC visibility pop
+
+ls_status ls::layernorm_bwd_entry(ls_dtype dtype, void* dx, void* dgamma, void* dbeta,
+                                  const void* dy, const void* x, const void* gamma,
+                                  const float* mean, const float* rstd, int64_t rows,
+                                  int64_t cols, void* workspace, size_t workspace_bytes,
+                                  void* stream, bool inline_reduction) {
     ls::DType dt;
     LS_TRY(check_dtype(dtype, &dt));
     LS_TRY(check_shape(rows, cols, ls::kMaxRowLen));
@@ -543,10 +556,13 @@ ls_status ls_layernorm_bwd(ls_dtype dtype, void* dx, void* dgamma, void* dbeta, 
         e = launch_reduction(s, partial, plan.bytes(), [&](cudaStream_t rs) {
             return ls::launch_colreduce(dt, dgamma, dbeta, cols, partial, plan.parts, plan.width,
                                         rs);
-        });
+        }, inline_reduction);
     }
     return from_cuda(e, "ls_layernorm_bwd launch");
 }
+
+#pragma GCC visibility push(default)
+extern "C" {
 
 static ls_status softmax_common(const char* fn, ls_dtype dtype, int64_t batch, int64_t heads,
                                 int64_t q_len, int64_t k_len, const int32_t* key_len,

@@ -7,6 +7,8 @@
 #include <stddef.h>
 #include <stdint.h>
 
+#include "../../include/ls_ops.h"
+
 namespace ls {
 
 enum class DType { F32 = 0, F16 = 1 };
@@ -125,6 +127,14 @@ cudaError_t layernorm_take_device_error(unsigned int* flags);
 
 // Streaming multiprocessors of the current device (queried once per device).
 int sm_count();
+
+// ls_layernorm_bwd with a choice of where the column reduction runs:
+// inline_reduction keeps it on `stream` even when a reduction stream is set
+// (the allocation-free entry point, whose scratch all host threads share).
+ls_status layernorm_bwd_entry(ls_dtype dtype, void* dx, void* dgamma, void* dbeta, const void* dy,
+                              const void* x, const void* gamma, const float* mean,
+                              const float* rstd, int64_t rows, int64_t cols, void* workspace,
+                              size_t workspace_bytes, void* stream, bool inline_reduction);
 
 // Set this host thread's ls_last_error() message (printf-style).
 void set_last_error_message(const char* fmt, ...);

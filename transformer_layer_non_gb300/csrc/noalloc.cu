@@ -12,10 +12,9 @@
 // until the process exits.
 //
 // Nothing here allocates: the array is part of the library's device image,
-// its device address is looked up once per device, and the call then goes
-// through the ordinary ls_layernorm_bwd path with that address as workspace.
-#include <mutex>
-
+// its device address is looked up in the current context on every call, and
+// the call then goes through the ordinary LayerNorm backward path with that
+// address as workspace and its column reduction kept on the caller's stream.
 #include "../../include/ls_ops.h"
 #include "ls_internal.h"
 
@@ -28,26 +27,17 @@ constexpr size_t kNoAllocScratchBytes = LS_NOALLOC_SCRATCH_BYTES;
 // cudaGetSymbolAddress below.
 static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
 
-constexpr int kMaxDevices = 256;
-std::mutex g_setup_mutex;
-void* g_scratch_addr[kMaxDevices] = {};  // per device, set on the first call there
-
-// Device address of the scratch array on the current device (set-up on the
-// first call per device, with that device current).
+// Device address of the scratch array in the current context.  A __device__
+// array exists once per context that has loaded the library's module, so the
+// address belongs to the context, not to the device: it is looked up on every
+// call (a query that allocates nothing), never cached, and so stays right in
+// a second context on the same device and after cudaDeviceReset.
 cudaError_t scratch_address(void** out) {
-    int dev = 0;
-    cudaError_t e = cudaGetDevice(&dev);
+    void* p = nullptr;
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
     if (e != cudaSuccess) return e;
-    if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
-    std::lock_guard<std::mutex> lock(g_setup_mutex);
-    if (g_scratch_addr[dev] == nullptr) {
-        void* p = nullptr;
-        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-        if (e != cudaSuccess) return e;
-        if (p == nullptr) return cudaErrorInvalidSymbol;
-        g_scratch_addr[dev] = p;
-    }
-    *out = g_scratch_addr[dev];
+    if (p == nullptr) return cudaErrorInvalidSymbol;
+    *out = p;
     return cudaSuccess;
 }
 
@@ -61,10 +51,10 @@ extern "C" ls_status ls_layernorm_bwd_noalloc(ls_dtype dtype, void* dx, void* dg
                                               void* stream) {
     const bool param_grads = dgamma != nullptr || dbeta != nullptr;
     // Without parameter gradients, or for an empty batch, no scratch is used;
-    // ls_layernorm_bwd validates the arguments and does the work.
+    // the shared LayerNorm backward path validates the arguments and does the work.
     if (!param_grads || rows == 0)
-        return ls_layernorm_bwd(dtype, dx, dgamma, dbeta, dy, x, gamma, mean, rstd, rows, cols,
-                                nullptr, 0, stream);
+        return ls::layernorm_bwd_entry(dtype, dx, dgamma, dbeta, dy, x, gamma, mean, rstd, rows,
+                                       cols, nullptr, 0, stream, /*inline_reduction=*/true);
     // Reject shapes whose partial sums do not fit, before touching the GPU.
     if (rows > 0 && cols > 0 && cols % 8 == 0 && cols <= ls::kMaxRowLen) {
         const size_t need = ls::layernorm_bwd_plan(rows, cols, dtype == LS_F32 ? 4 : 2).bytes();
@@ -84,7 +74,12 @@ extern "C" ls_status ls_layernorm_bwd_noalloc(ls_dtype dtype, void* dx, void* dg
                                    cudaGetErrorName(e), cudaGetErrorString(e));
         return LS_ERR_CUDA;
     }
-    return ls_layernorm_bwd(dtype, dx, dgamma, dbeta, dy, x, gamma, mean, rstd, rows, cols,
-                            scratch, kNoAllocScratchBytes, stream);
+    // The column reduction stays on `stream` even when a reduction stream is
+    // set: the scratch is shared by every host thread, and a reduction forked
+    // onto another stream would still be reading it when a call from another
+    // thread, ordered only on `stream`, overwrites it.
+    return ls::layernorm_bwd_entry(dtype, dx, dgamma, dbeta, dy, x, gamma, mean, rstd, rows, cols,
+                                   scratch, kNoAllocScratchBytes, stream,
+                                   /*inline_reduction=*/true);
 }
 #pragma GCC visibility pop

@@ -28,6 +28,9 @@ LS_ERR_CUDA = 5
 LS_F32 = 0
 LS_F16 = 1
 
+# Size of the scratch array behind ls_layernorm_bwd_noalloc (include/ls_ops.h).
+LS_NOALLOC_SCRATCH_BYTES = 8 << 20
+
 # Every entry point declared in include/ls_ops.h.
 EXPORTS = (
     "ls_status_string", "ls_last_error", "ls_version", "ls_colreduce_workspace_bytes",

@@ -33,7 +33,10 @@ if ROOT not in sys.path:
 
 METRIC = "achieved HBM GB/s and % of GB300 peak per fused op (fwd+bwd), tokens/s"
 UNIT = "GB/s"
-DEFAULT_WORKLOAD = "bert-base"
+# The headline workload is the largest single-GPU layer configuration; the
+# other layer the target names is measured beside it.
+DEFAULT_WORKLOAD = "gpt2-large"
+DEFAULT_EXTRA_WORKLOADS = "bert-base"
 L2_BYTES = 129e6
 FALLBACK_HBM_GBS = 6800.0
 # GB300's nominal HBM3e bandwidth (vendor figure; context beside the measured
@@ -53,6 +56,11 @@ def parse_args():
     ap.add_argument("--warmup", type=int, default=20)
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD,
                     choices=["transformer-base", "bert-base", "gpt2-large", "tiny"])
+    ap.add_argument("--extra-workloads", default=DEFAULT_EXTRA_WORKLOADS,
+                    help="comma-separated layer workloads measured beside the headline one "
+                         "(each under its own key; '' for none)")
+    ap.add_argument("--no-sweep", dest="with_sweep", action="store_false",
+                    help="skip the softmax row-length sweep (2^22 elements) of the default run")
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -83,6 +91,10 @@ def parse_args():
     a = ap.parse_args()
     if a.warmup < 3:
         ap.error("--warmup must be >= 3")
+    a.extra_workloads = [w for w in a.extra_workloads.split(",") if w]
+    for w in a.extra_workloads:
+        if w not in ("transformer-base", "bert-base", "gpt2-large", "tiny"):
+            ap.error(f"unknown workload {w}")
     return a
 
 
@@ -560,12 +572,11 @@ def run_reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(dt / args.steps * 1e3, 3), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": layer.name, "tokens": layer.tokens, "hidden": layer.hidden,
-                   "ffn": layer.ffn, "heads": layer.heads, "seq_len": layer.seq,
-                   "storage": layer.dtype, "sample_fraction": round(frac, 5)},
+        "config": layer_config(layer),
         "tokens_per_s": round(tokens, 1),
         "cpu_baseline": {"value": round(value, 3), "unit": UNIT, "cores": oracle.num_threads(),
-                         "kind": "oracle", "sample": sample},
+                         "kind": "oracle", "sample": sample,
+                         "sample_fraction": round(frac, 5)},
         "e2e": {"value": round(value, 3), "unit": UNIT, "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
@@ -678,34 +689,78 @@ def fused_op_summary(ops_report, peak):
     return out
 
 
-def run_ours(args):
+def layer_config(layer):
+    """The workload description both arms print as `config` (identical dicts
+    for the same workload)."""
+    return {"workload": layer.name, "tokens": layer.tokens, "batch": layer.batch,
+            "seq_len": layer.seq, "hidden": layer.hidden, "ffn": layer.ffn,
+            "heads": layer.heads, "mask": "causal" if layer.causal else
+            (f"padding U[{layer.pad_lo},{layer.seq}]" if layer.pad_lo else "none"),
+            "dropout_p": layer.p, "storage": layer.dtype}
+
+
+class Floor:
+    """The reference streaming kernel (libls_floor.so): a dependent launch that
+    reads R and writes W bytes with no arithmetic, chained back to back over
+    L2-cold buffers like the operators; its time per launch is the floor each
+    operator is compared with."""
+
+    NEVER = 0xDEADBEEF  # a word the buffers never hold (they are zero-filled)
+
+    def __init__(self):
+        import ctypes
+
+        from transformer_layer_non_gb300 import build as lsbuild
+
+        self.lib = ctypes.CDLL(lsbuild.build_floor())
+        self.lib.lsf_stream.restype = ctypes.c_int
+        self.lib.lsf_stream.argtypes = [ctypes.c_void_p, ctypes.c_void_p, ctypes.c_uint64,
+                                        ctypes.c_uint64, ctypes.c_uint32, ctypes.c_void_p]
+        self.cache = {}
+
+    def us(self, read_bytes, write_bytes, reps=10):
+        import math
+
+        import torch
+
+        rv, wv = int(math.ceil(read_bytes / 16)), int(math.ceil(write_bytes / 16))
+        key = (rv, wv)
+        if key in self.cache:
+            return self.cache[key]
+        fp = 16 * (rv + wv)
+        nsets = max(2, min(48, math.ceil(3 * L2_BYTES / max(fp, 1))))
+        sets = [(torch.zeros(max(rv, 1) * 16, dtype=torch.uint8, device="cuda"),
+                 torch.zeros(max(wv, 1) * 16, dtype=torch.uint8, device="cuda"))
+                for _ in range(nsets)]
+
+        def thunk(src, dst):
+            def f():
+                st = self.lib.lsf_stream(dst.data_ptr(), src.data_ptr(), rv, wv, self.NEVER,
+                                         torch.cuda.current_stream().cuda_stream)
+                if st != 0:
+                    raise RuntimeError(f"lsf_stream failed: cuda error {st}")
+            return f
+
+        g = capture([thunk(src, dst) for src, dst in sets])
+        us = time_graph(g, reps) / nsets * 1e3
+        del g, sets
+        self.cache[key] = us
+        return us
+
+
+def measure_layer(layer, args, device, pg, world, floor, full):
+    """One workload's layer step: the graph-replayed step (headline timing),
+    each operator alone over L2-cold buffer sets, the floor of each operator's
+    bytes, and, when `full`, the end-to-end run through host buffers.  Returns
+    (report, step) on every rank; `report` is complete on rank 0."""
     import torch
 
-    from transformer_layer_non_gb300 import ls_ops, synth
+    from transformer_layer_non_gb300 import accounting
 
-    rank, world, local = dist_env()
-    if not torch.cuda.is_available():
-        print(json.dumps({"error": "no CUDA device"}))
-        return 1
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-    pg = None
-    if world > 1:
-        import torch.distributed as dist
-
-        dist.init_process_group("nccl", device_id=device)
-        pg = dist
-    ls_ops.load()
-    layer = synth.LAYERS[args.workload]
     step = LayerStep(layer, args.seed, device, args.reductions)
     step_bytes = sum(step.bytes.values())
     names = [n for n, _ in step.ops()]
     graph = capture(step.step_thunks())
-
-    sampler = ClockSampler(local)
-    sampler.start()
-    time.sleep(0.3)
-    t_busy0 = time.time()
     for _ in range(args.warmup):
         graph.replay()
     torch.cuda.synchronize()
@@ -725,30 +780,41 @@ def run_ours(args):
     if pg:
         ms = max_over_ranks(ms, pg, device)
     ms_step = ms / args.steps
-    t_busy1 = time.time()
 
     # Per-operator device time: inside the running step (events between the
-    # operators), and each operator alone over L2-cold buffer sets.
+    # operators), and each operator alone over L2-cold buffer sets; beside it
+    # the floor of a plain streaming launch of the same bytes.
     live = in_step_times(step)
     iso = per_op_isolated(step)
     per_op = {n: iso[n]["ms"] for n in names}
+    es = step.esize
+    rw = accounting.layer_step_read_write(layer.tokens, layer.hidden, layer.ffn, layer.batch,
+                                          layer.heads, layer.seq, es, step.key_len_np,
+                                          layer.causal)
+    floor_us = {n: floor.us(*rw[n]) for n in names}
 
-    # End to end through the public API with host buffers: every step copies
-    # every input from pinned host memory and every output back.  Serial (copy
-    # in, compute, copy out) and pipelined over two device buffer sets (step
-    # k+1's inputs go in and step k-1's outputs come out while step k runs).
-    e2e_steps = min(args.steps, 50)
-    host_in = {k: step.t[k].cpu().pin_memory() for k in step.inputs}
-    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
-    d2h = sum(step.t[k].numel() * step.t[k].element_size() for k in step.outputs)
-    e2e_serial_ms = e2e_serial(step, graph, host_in, e2e_steps)
-    e2e_ms = e2e_pipelined(step, host_in, e2e_steps)
-    sampler.stop()
+    e2e = None
+    if full:
+        # End to end through the public API with host buffers: every step copies
+        # every input from pinned host memory and every output back.  Serial
+        # (copy in, compute, copy out) and pipelined over two device buffer sets
+        # (step k+1's inputs go in and step k-1's outputs come out while step k
+        # runs).
+        e2e_steps = min(args.steps, 50)
+        host_in = {k: step.t[k].cpu().pin_memory() for k in step.inputs}
+        h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+        d2h = sum(step.t[k].numel() * step.t[k].element_size() for k in step.outputs)
+        e2e_serial_ms = e2e_serial(step, graph, host_in, e2e_steps)
+        e2e_ms = e2e_pipelined(step, host_in, e2e_steps)
+        e2e = {"value": round(world * step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
+               "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+               "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
+               "copies": "pinned host memory; copy-in, step and copy-out pipelined over two "
+                         "device buffer sets on three streams",
+               "serial_ms_per_step": round(e2e_serial_ms, 4)}
+        del host_in
+    del graph
 
-    if rank != 0:
-        if pg:
-            pg.destroy_process_group()
-        return 0
     peak, peak_kind = load_peaks()
     value = whole_job_gbs(step_bytes, world, ms_step)
     ops_report = {}
@@ -756,12 +822,15 @@ def run_ours(args):
         gbs = step.bytes[n] / (per_op[n] * 1e-3) / 1e9
         ops_report[n] = {"us": round(per_op[n] * 1e3, 2), "bytes": int(step.bytes[n]),
                          "GB/s": round(gbs, 1), "frac": round(gbs / peak, 4),
+                         "floor_us": round(floor_us[n], 2),
+                         "floor_frac": round(step.bytes[n] / (floor_us[n] * 1e-6) / 1e9 / peak, 4),
+                         "of_floor": round(floor_us[n] / (per_op[n] * 1e3), 4),
                          "launches": step.launches[n], "buffer_sets": iso[n]["sets"],
                          "in_step_events_us": round(live[n] * 1e3, 2)}
         if n.startswith("softmax"):
             # as if masked scores were read too: one read and one write per
             # element forward, two reads and one write backward
-            dense = layer.batch * layer.heads * layer.seq * layer.seq * step.esize * (
+            dense = layer.batch * layer.heads * layer.seq * layer.seq * es * (
                 2 if n == "softmax_fwd" else 3)
             ops_report[n]["dense_bytes"] = int(dense)
             ops_report[n]["dense_GB/s"] = round(dense / (per_op[n] * 1e-3) / 1e9, 1)
@@ -771,49 +840,159 @@ def run_ours(args):
                 "achieved": dom["GB/s"], "peak": peak, "unit": "GB/s",
                 "frac": dom["frac"], "traffic": ncu_traffic(dominant, layer.name),
                 "algorithmic_bytes": dom["bytes"], "duration_us": dom["us"],
+                "floor_us": dom["floor_us"],
                 "timing": "CUDA events on the launching stream around back-to-back launches "
                           "of the operator over L2-cold buffer sets",
                 "peak_source": f"{peak_kind} hbm_gbs (copy)"}
-    clocks = sampler.summary(t_busy0, t_busy1)
-    line = {
-        "metric": METRIC, "value": round(value, 2), "unit": UNIT, "n_gpus": world,
-        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms_step, 5),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "fp16-storage/fp32-math" if layer.dtype == "f16" else "f32",
-        "data": "synthetic",
-        "config": {"workload": layer.name, "tokens": layer.tokens, "batch": layer.batch,
-                   "seq_len": layer.seq, "hidden": layer.hidden, "ffn": layer.ffn,
-                   "heads": layer.heads, "mask": "causal" if layer.causal else
-                   (f"padding U[{layer.pad_lo},{layer.seq}]" if layer.pad_lo else "none"),
-                   "dropout_p": layer.p, "storage": layer.dtype,
-                   "l2": f"inputs larger than L2: one step touches "
-                         f"{step.footprint_bytes() / 1e6:.0f} MB of distinct buffers "
-                         f"(L2 {L2_BYTES / 1e6:.0f} MB); no flush",
-                   "graph": "one CUDA graph per step", "parallelism": f"replicas x{world}",
-                   "column_reductions": (
-                       "forked onto a second stream, joined at the end of the step"
-                       if step.side is not None else "inline on the step's stream")},
+    report = {
+        "value": round(value, 2), "ms_per_step": round(ms_step, 5),
         "pct_of_peak": round(value / world / peak * 100, 2),
         "pct_of_nominal_hbm": round(value / world / NOMINAL_HBM_GBS * 100, 2),
-        "nominal_hbm_gbs": NOMINAL_HBM_GBS,
         "tokens_per_s": round(layer.tokens * world / (ms_step * 1e-3), 1),
+        "step_bytes": int(step_bytes),
+        "step_floor_us": round(sum(floor_us.values()), 2),
         "per_op": ops_report,
         "per_fused_op": fused_op_summary(ops_report, peak),
-        "per_op_note": "us: the operator alone, back to back over rotating L2-cold buffer "
-                       "sets (CUDA events); in_step_events_us: between CUDA events recorded "
-                       "around it inside the running step, which also stop the overlap of "
-                       "neighbouring launches and so read higher",
         "sum_per_op_us": round(sum(per_op.values()) * 1e3, 2),
         "sum_in_step_events_us": round(sum(live.values()) * 1e3, 2),
         "roofline": roofline,
-        "e2e": {"value": round(step_bytes / (e2e_ms * 1e-3) / 1e9, 2), "unit": UNIT,
-                "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
-                "ms_per_step": round(e2e_ms, 4), "steps": e2e_steps,
-                "copies": "pinned host memory; copy-in, step and copy-out pipelined over two "
-                          "device buffer sets on three streams",
-                "serial_ms_per_step": round(e2e_serial_ms, 4)},
-        "gpu_launches": int(sum(step.launches.values()) * args.steps),
-        "clocks": clocks,
+        "l2": f"inputs larger than L2: one step touches {step.footprint_bytes() / 1e6:.0f} MB "
+              f"of distinct buffers (L2 {L2_BYTES / 1e6:.0f} MB); no flush",
+        "column_reductions": ("forked onto a second stream, joined at the end of the step"
+                              if step.side is not None else "inline on the step's stream"),
+        "launches_per_step": int(sum(step.launches.values())),
     }
+    if e2e is not None:
+        report["e2e"] = e2e
+    return report, step
+
+
+def sweep_short(floor, seed=0, reps=20):
+    """The pages' softmax row-length sweep (k_len 16..4096 on 2^22 FP16
+    elements, a random valid length per row), forward and backward, each
+    length alone over L2-cold buffer sets, with the floor of its bytes."""
+    import math
+
+    import torch
+
+    from transformer_layer_non_gb300 import accounting, ls_ops, synth
+
+    peak, _ = load_peaks()
+    dev = torch.device("cuda", 0)
+    out = {}
+    for k_len in SWEEP_K_LENS:
+        x, dy, kl = synth.sweep_inputs(k_len, seed)
+        b, h, q, k = x.shape
+        t = {"x": torch.from_numpy(x).to(dev), "dy": torch.from_numpy(dy).to(dev),
+             "kl": torch.from_numpy(kl).to(dev)}
+        t["y"] = torch.empty_like(t["x"])
+        t["dx"] = torch.empty_like(t["x"])
+        ls_ops.ls_softmax_fwd(t["y"], t["x"], t["kl"], False)
+        valid = accounting.softmax_valid_count(b, h, q, k, kl, False)
+        rw = {"fwd": (2 * valid + 4 * b, 2 * x.size), "bwd": (4 * valid + 4 * b, 2 * x.size)}
+        res = {}
+        for d in ("fwd", "bwd"):
+            fp = (2 if d == "fwd" else 3) * x.nbytes
+            nsets = max(2, min(64, math.ceil(3 * L2_BYTES / fp)))
+            sets = [{n: v.clone() for n, v in t.items()} for _ in range(nsets)]
+            if d == "fwd":
+                thunks = [(lambda s=s: ls_ops.ls_softmax_fwd(s["y"], s["x"], s["kl"], False))
+                          for s in sets]
+            else:
+                thunks = [(lambda s=s: ls_ops.ls_softmax_bwd(s["dx"], s["y"], s["dy"], s["kl"],
+                                                            False)) for s in sets]
+            ms = time_graph(capture(thunks), reps) / nsets
+            nbytes = sum(rw[d])
+            gbs = nbytes / (ms * 1e-3) / 1e9
+            fus = floor.us(*rw[d])
+            res[d] = {"us": round(ms * 1e3, 2), "bytes": int(nbytes), "GB/s": round(gbs, 1),
+                      "frac": round(gbs / peak, 4), "floor_us": round(fus, 2),
+                      "of_floor": round(fus / (ms * 1e3), 4)}
+            del sets, thunks
+        out[str(k_len)] = res
+        del t
+    return {"elements": synth.SWEEP_ELEMENTS, "storage": "f16",
+            "valid_len": "U[1, k_len] per row", "k_len": out}
+
+
+def run_ours(args):
+    import torch
+
+    from transformer_layer_non_gb300 import ls_ops, synth
+
+    rank, world, local = dist_env()
+    if not torch.cuda.is_available():
+        print(json.dumps({"error": "no CUDA device"}))
+        return 1
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    pg = None
+    if world > 1:
+        import torch.distributed as dist
+
+        dist.init_process_group("nccl", device_id=device)
+        pg = dist
+    ls_ops.load()
+    floor = Floor()
+    layer = synth.LAYERS[args.workload]
+
+    # nvidia-smi samples over every timed section (the step, each operator
+    # alone, the floors, the other workloads and the sweep).
+    sampler = ClockSampler(local)
+    sampler.start()
+    time.sleep(0.3)
+    t_busy0 = time.time()
+    head, _ = measure_layer(layer, args, device, pg, world, floor, full=True)
+    extra = {}
+    for name in args.extra_workloads:
+        if name and name != layer.name:
+            rep, _ = measure_layer(synth.LAYERS[name], args, device, pg, world, floor,
+                                   full=False)
+            extra[name] = rep
+    sweep = sweep_short(floor, args.seed) if (args.with_sweep and rank == 0) else None
+    torch.cuda.synchronize()
+    t_busy1 = time.time()
+    time.sleep(0.25)
+    sampler.stop()
+
+    if rank != 0:
+        if pg:
+            pg.destroy_process_group()
+        return 0
+    line = {
+        "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": head["ms_per_step"],
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "fp16-storage/fp32-math" if layer.dtype == "f16" else "f32",
+        "data": "synthetic",
+        "config": layer_config(layer),
+        "setup": {"l2": head["l2"], "graph": "one CUDA graph per step",
+                  "parallelism": f"replicas x{world}",
+                  "column_reductions": head["column_reductions"]},
+        "pct_of_peak": head["pct_of_peak"], "pct_of_nominal_hbm": head["pct_of_nominal_hbm"],
+        "nominal_hbm_gbs": NOMINAL_HBM_GBS, "tokens_per_s": head["tokens_per_s"],
+        "step_floor_us": head["step_floor_us"],
+        "per_op": head["per_op"], "per_fused_op": head["per_fused_op"],
+        "per_op_note": "us: the operator alone, back to back over rotating L2-cold buffer "
+                       "sets (CUDA events); floor_us: a plain streaming kernel moving the same "
+                       "read and write bytes with no arithmetic, chained the same way "
+                       "(of_floor = floor_us / us); in_step_events_us: between CUDA events "
+                       "recorded around it inside the running step, which also stop the "
+                       "overlap of neighbouring launches and so read higher",
+        "sum_per_op_us": head["sum_per_op_us"],
+        "sum_in_step_events_us": head["sum_in_step_events_us"],
+        "roofline": head["roofline"],
+        "e2e": head["e2e"],
+        "gpu_launches": int(head["launches_per_step"] * args.steps),
+        "clocks": sampler.summary(t_busy0, t_busy1),
+    }
+    for name, rep in extra.items():
+        line[name] = {k: rep[k] for k in ("value", "ms_per_step", "pct_of_peak",
+                                          "tokens_per_s", "step_floor_us", "per_op",
+                                          "per_fused_op", "sum_per_op_us", "roofline")}
+        line[name]["config"] = layer_config(synth.LAYERS[name])
+    if sweep is not None:
+        line["softmax_sweep"] = sweep
     if not args.no_cpu_baseline and world == 1:
         line["cpu_baseline"] = cpu_baseline(layer, args.cpu_budget)
     elif not args.no_cpu_baseline:

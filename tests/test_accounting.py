@@ -99,3 +99,18 @@ def test_next_operator_bytes_by_hand():
     assert acc.embedding_fwd_bytes(10, 5, 16, 2) == 40 + 320 + 160 + 320 + 20
     assert acc.embedding_bwd_bytes(10, 4, 16, 2) == 40 + 320 + 20 + 2 * 256
 
+
+
+def test_read_write_split_adds_up_to_the_step_bytes():
+    from transformer_layer_non_gb300 import synth
+
+    for L in synth.LAYERS.values():
+        es = 2 if L.dtype == "f16" else 4
+        kl = synth.layer_inputs(L, 0, which={"key_len"}).get("key_len")
+        tot = acc.layer_step_bytes(L.tokens, L.hidden, L.ffn, L.batch, L.heads, L.seq, es,
+                                          kl, L.causal)
+        rw = acc.layer_step_read_write(L.tokens, L.hidden, L.ffn, L.batch, L.heads, L.seq,
+                                              es, kl, L.causal)
+        assert set(rw) == set(tot)
+        for k in tot:
+            assert abs(sum(rw[k]) - tot[k]) <= 1e-6 * tot[k], (L.name, k)

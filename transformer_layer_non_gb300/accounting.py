@@ -179,3 +179,32 @@ def layer_step_bytes(tokens: int, hidden: int, ffn: int, batch: int, heads: int,
         "attn_bdr_bwd": dropout_bwd_bytes(T, H, esize),
         "softmax_bwd": softmax_bwd_bytes(**sm),
     }
+
+
+def layer_step_read_write(tokens: int, hidden: int, ffn: int, batch: int, heads: int, seq: int,
+                          esize: int, key_len=None, causal=False) -> Dict[str, tuple]:
+    """(read bytes, write bytes) of every operator of layer_step_bytes, for a
+    plain streaming copy that moves the same bytes (the floor a dependent
+    launch of that size can reach)."""
+    T, H, F = tokens, hidden, ffn
+    n_h, n_f = T * H, T * F
+    m = MASK_BYTES_PER_ELEM
+    sm = dict(batch=batch, heads=heads, q_len=seq, k_len=seq, key_len=key_len, causal=causal)
+    valid = softmax_valid_count(**sm)
+    dense = batch * heads * seq * seq
+    kl = 4 * batch if key_len is not None else 0
+    rw = {
+        "softmax_fwd": (valid * esize + kl, dense * esize),
+        "attn_bdr_fwd": (2 * n_h * esize + H * esize, n_h * esize + n_h * m),
+        "ln1_fwd": (n_h * esize + 2 * H * esize, n_h * esize + 8 * T),
+        "ffn1_brd_fwd": (n_f * esize + F * esize, n_f * esize + n_f * m),
+        "ffn2_bdr_fwd": (2 * n_h * esize + H * esize, n_h * esize + n_h * m),
+        "ln2_fwd": (n_h * esize + 2 * H * esize, n_h * esize + 8 * T),
+        "ln2_bwd": (2 * n_h * esize + H * esize + 8 * T, n_h * esize + 2 * H * esize),
+        "ffn2_bdr_bwd": (n_h * esize + n_h * m, n_h * esize + H * esize),
+        "ffn1_brd_bwd": (n_f * esize + n_f * m, n_f * esize + F * esize),
+        "ln1_bwd": (2 * n_h * esize + H * esize + 8 * T, n_h * esize + 2 * H * esize),
+        "attn_bdr_bwd": (n_h * esize + n_h * m, n_h * esize + H * esize),
+        "softmax_bwd": (2 * valid * esize + kl, dense * esize),
+    }
+    return {k: (float(r), float(w)) for k, (r, w) in rw.items()}

@@ -22,6 +22,9 @@ CSRC = os.path.join(PKG, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(BUILD, "libls_ops.so")
+# The benchmark's reference streaming kernel (not part of the operator library).
+FLOOR_SRC = os.path.join(PKG, "floor", "stream_floor.cu")
+FLOOR_LIB = os.path.join(BUILD, "libls_floor.so")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ARCH + ["-O3", "-lineinfo", "-std=c++17", "--expt-relaxed-constexpr",
@@ -82,6 +85,22 @@ def build(force: bool = False, verbose: bool = False, ptxas_verbose: bool = Fals
     return LIB
 
 
+def build_floor(force: bool = False) -> str:
+    """Compile the benchmark's reference streaming kernel into libls_floor.so."""
+    if (not force and os.path.exists(FLOOR_LIB)
+            and os.path.getmtime(FLOOR_LIB) >= max(os.path.getmtime(FLOOR_SRC),
+                                                    os.path.getmtime(__file__))):
+        return FLOOR_LIB
+    os.makedirs(BUILD, exist_ok=True)
+    tmp = FLOOR_LIB + f".tmp{os.getpid()}"
+    cmd = [_nvcc(), *NVCC_FLAGS, "-shared", "-cudart", "static", "-o", tmp, FLOOR_SRC]
+    r = subprocess.run(cmd, capture_output=True, text=True)
+    if r.returncode != 0:
+        raise RuntimeError(f"nvcc failed on {FLOOR_SRC}:\n{r.stdout}\n{r.stderr}")
+    os.replace(tmp, FLOOR_LIB)
+    return FLOOR_LIB
+
+
 if __name__ == "__main__":
     ap = argparse.ArgumentParser()
     ap.add_argument("--force", action="store_true")
@@ -89,3 +108,4 @@ if __name__ == "__main__":
     ap.add_argument("--ptxas", action="store_true", help="print -Xptxas -v register/spill report")
     a = ap.parse_args()
     print(build(force=a.force or a.ptxas, verbose=a.verbose, ptxas_verbose=a.ptxas))
+    print(build_floor(force=a.force))

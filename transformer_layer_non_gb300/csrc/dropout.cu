@@ -57,10 +57,11 @@ __device__ __forceinline__ void fwd_load(Raw8<T> (&xr)[U], Raw8<T> (&rr)[U], con
     }
 }
 
-// Keep bits of the U vectors of a chunk; called right after the chunk's loads
-// are issued, so the Philox arithmetic overlaps their latency.
-// With 32-bit indices (the host picks them when every vector index and its
-// counter block 2 * vector index fit in 32 bits) the block's high word is 0.
+// Keep bits of the U vectors of a chunk (bit j of keep[u] decides element j of
+// vector u); called right after the chunk's loads are issued, so the Philox
+// arithmetic overlaps their latency.  The bias+dropout+residual forward keeps
+// only these 8 bits per vector in registers (its two input streams need the
+// occupancy more than fewer integer instructions).
 template <int U, typename I>
 __device__ __forceinline__ void fwd_keep(uint32_t (&keep)[U], I v, I S, I nv,
                                          const FwdArgs& a, const PhiloxSchedule& ks) {
@@ -78,8 +79,9 @@ __device__ __forceinline__ void fwd_keep(uint32_t (&keep)[U], I v, I S, I nv,
     }
 }
 
-template <typename T, bool RELU, int U, typename I>
-__device__ __forceinline__ void fwd_compute(const Raw8<T> (&xr)[U], const Raw8<T> (&rr)[U],
+// bias + dropout + residual on the U vectors of a chunk.
+template <typename T, int U, typename I>
+__device__ __forceinline__ void bdr_compute(const Raw8<T> (&xr)[U], const Raw8<T> (&rr)[U],
                                             const uint32_t (&kp)[U], T* out, uint8_t* mask,
                                             const T* __restrict__ bias, I v, uint32_t cv, I S,
                                             I nv, const FwdArgs& a) {
@@ -87,38 +89,125 @@ __device__ __forceinline__ void fwd_compute(const Raw8<T> (&xr)[U], const Raw8<T
     for (int u = 0; u < U; ++u) {
         const I vu = v + u * S;
         if (vu >= nv) break;
-        float b[kVec], z[kVec], o[kVec];
+        float b[kVec], z[kVec], o[kVec], rf[kVec];
         load8f<T>(bias + static_cast<size_t>(cv) * kVec, b);
         add8(xr[u], b, z);  // z = x + bias, exact conversion of x folded in
+        unpack(rr[u], rf);
         const uint32_t keep = kp[u];
-        uint32_t bits;
-        if (RELU) {
-            bits = 0;
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const bool on = (z[j] > 0.f) && ((keep >> j) & 1u);
-                bits |= on ? (1u << j) : 0u;
-                o[j] = on ? z[j] * a.scale : 0.f;
-            }
-        } else {
-            float rf[kVec];
-            unpack(rr[u], rf);
-#pragma unroll
-            for (int j = 0; j < kVec; ++j)
-                o[j] = ((keep >> j) & 1u) ? rf[j] + z[j] * a.scale : rf[j];
-            bits = keep;
-        }
+        for (int j = 0; j < kVec; ++j)
+            o[j] = ((keep >> j) & 1u) ? rf[j] + z[j] * a.scale : rf[j];
         store8f<T>(out + static_cast<size_t>(vu) * kVec, o);
-        if (mask) mask[vu] = static_cast<uint8_t>(bits);
+        if (mask) mask[vu] = static_cast<uint8_t>(keep);
         cv += a.step_col;
         if (cv >= a.nvr) cv -= a.nvr;
     }
 }
 
-template <typename T, bool RELU, int U, typename I>
+// Philox words of the U vectors of a chunk (8 per vector: word j decides
+// element j); called right after the chunk's loads are issued, so the Philox
+// arithmetic overlaps their latency.  With 32-bit indices (the host picks them
+// when every vector index and its counter block 2 * vector index fit in 32
+// bits) the block's high word is 0.
+template <int U, typename I>
+__device__ __forceinline__ void fwd_words(uint4 (&wa)[U], uint4 (&wb)[U], I v, I S, I nv,
+                                          const FwdArgs& a, const PhiloxSchedule& ks) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const I vu = v + u * S;
+        if (vu < nv) {
+            uint32_t lo, hi;
+            if (sizeof(I) == 4) {
+                lo = static_cast<uint32_t>(vu) * 2u;
+                hi = 0u;
+            } else {
+                const uint64_t blk = static_cast<uint64_t>(vu) * 2u;
+                lo = static_cast<uint32_t>(blk);
+                hi = static_cast<uint32_t>(blk >> 32);
+            }
+            wa[u] = philox4x32_10(make_uint4(lo, hi, a.off_lo, a.off_hi), ks);
+            // lo is even, so lo + 1 never carries into hi.
+            wb[u] = philox4x32_10(make_uint4(lo + 1u, hi, a.off_lo, a.off_hi), ks);
+        }
+    }
+}
+
+// One element of the bias+ReLU+dropout epilogue, as predicated selects (FSEL
+// runs on the FMA pipes; only the two compares use the integer ALU, which the
+// Philox rounds already load): with keep = (w >= thr),
+//   on = keep && z > 0;  o = on ? zs : 0;  bit = on,
+// the bit returned as the float 2^j or 0, to be summed exactly.
+__device__ __forceinline__ void brd_elem(uint32_t w, uint32_t thr, float z, float zs, float pow2j,
+                                         float& o, float& bit) {
+    asm("{\n\t.reg .pred p, q;\n\t"
+        "setp.hs.u32 p, %2, %3;\n\t"
+        "setp.gt.and.f32 q, %4, 0f00000000, p;\n\t"
+        "selp.f32 %0, %5, 0f00000000, q;\n\t"
+        "selp.f32 %1, %6, 0f00000000, q;\n\t}"
+        : "=f"(o), "=f"(bit)
+        : "r"(w), "r"(thr), "f"(z), "f"(zs), "f"(pow2j));
+}
+// 2^23 plus the sum of the bits' values 2^j (j < 8) is exact in FP32 and its
+// low byte is the mask byte: the byte store takes it from the float's bits.
+constexpr float kMaskMagic = 8388608.0f;
+
+// Bias of column vector cv in FP32: from the CTA's shared-memory copy when the
+// row fits there (SMEMB), else loaded and converted.
+template <typename T, bool SMEMB>
+__device__ __forceinline__ void bias8(const float* bsm, const T* __restrict__ bias, uint32_t cv,
+                                      float (&b)[kVec]) {
+    if (SMEMB) {
+        const float4 b0 = *reinterpret_cast<const float4*>(bsm + cv * kVec);
+        const float4 b1 = *reinterpret_cast<const float4*>(bsm + cv * kVec + 4);
+        b[0] = b0.x; b[1] = b0.y; b[2] = b0.z; b[3] = b0.w;
+        b[4] = b1.x; b[5] = b1.y; b[6] = b1.z; b[7] = b1.w;
+    } else {
+        load8f<T>(bias + static_cast<size_t>(cv) * kVec, b);
+    }
+}
+
+template <typename T, bool SMEMB, int U, typename I>
+__device__ __forceinline__ void brd_compute(const Raw8<T> (&xr)[U], const uint4 (&wa)[U],
+                                            const uint4 (&wb)[U], T* out,
+                                            uint8_t* mask, const float* bsm,
+                                            const T* __restrict__ bias, I v, uint32_t cv, I S,
+                                            I nv, const FwdArgs& a) {
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        const I vu = v + u * S;
+        if (vu >= nv) break;
+        float b[kVec], z[kVec], o[kVec], bit[kVec];
+        bias8<T, SMEMB>(bsm, bias, cv, b);
+        add8(xr[u], b, z);  // z = x + bias, exact conversion of x folded in
+        const uint32_t w[kVec] = {wa[u].x, wa[u].y, wa[u].z, wa[u].w,
+                                  wb[u].x, wb[u].y, wb[u].z, wb[u].w};
+#pragma unroll
+        for (int j = 0; j < kVec; j += 2) {
+            const float2 zs = mul2(make_float2(z[j], z[j + 1]), make_float2(a.scale, a.scale));
+            brd_elem(w[j], a.thr, z[j], zs.x, static_cast<float>(1u << j), o[j], bit[j]);
+            brd_elem(w[j + 1], a.thr, z[j + 1], zs.y, static_cast<float>(1u << (j + 1)), o[j + 1],
+                     bit[j + 1]);
+        }
+        store8f<T>(out + static_cast<size_t>(vu) * kVec, o);
+        if (mask) {
+            const float m = ((kMaskMagic + bit[0]) + (bit[1] + bit[2])) +
+                            ((bit[3] + bit[4]) + (bit[5] + (bit[6] + bit[7])));
+            mask[vu] = static_cast<uint8_t>(__float_as_uint(m));
+        }
+        cv += a.step_col;
+        if (cv >= a.nvr) cv -= a.nvr;
+    }
+}
+
+// bias + dropout + residual: a chunk's loads are issued, its keep bits drawn
+// while they are in flight, then it is computed and stored.  (Measured on
+// GB300, two register buffers per thread gain nothing here: five CTAs per SM
+// keep enough loads in flight, and the Philox work fits under the two input
+// streams' memory time.)
+template <typename T, int U, typename I>
 __global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 5 : 2)
-dropout_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias,
-                   const T* residual, const __grid_constant__ FwdArgs a) {
+bdr_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias, const T* residual,
+               const __grid_constant__ FwdArgs a) {
     const PhiloxSchedule& ks = a.ks;
     pdl_enter();
     const I nv = static_cast<I>(a.nv);
@@ -126,27 +215,90 @@ dropout_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias
     const I gw = blockIdx.x + static_cast<I>(threadIdx.x >> 5) * gridDim.x;
     I v = gw * 32 + (threadIdx.x & 31);
     uint32_t cv = static_cast<uint32_t>(v % a.nvr);
-    // (U rounds) mod nvr, from the per-round step.
-    uint32_t stepU = 0;
+    uint32_t stepU = 0;  // (U rounds) mod nvr, from the per-round step
 #pragma unroll
     for (int u = 0; u < U; ++u) {
         stepU += a.step_col;
         if (stepU >= a.nvr) stepU -= a.nvr;
     }
-    // One chunk of U rounds at a time: its loads are issued, its keep bits are
-    // drawn while they are in flight, then it is computed and stored.  (Measured
-    // on GB300, two register buffers per thread gain nothing here: the Philox
-    // arithmetic, not memory latency, sets the pace, and five CTAs per SM keep
-    // enough loads in flight.)
     Raw8<T> xa[U], ra[U];
     uint32_t ka[U];
     while (v < nv) {
-        fwd_load<T, RELU, U>(xa, ra, x, residual, v, S, nv);
+        fwd_load<T, false, U>(xa, ra, x, residual, v, S, nv);
         fwd_keep<U>(ka, v, S, nv, a, ks);
-        fwd_compute<T, RELU, U>(xa, ra, ka, out, mask, bias, v, cv, S, nv, a);
+        bdr_compute<T, U>(xa, ra, ka, out, mask, bias, v, cv, S, nv, a);
         v += U * S;
         cv += stepU;
         if (cv >= a.nvr) cv -= a.nvr;
+    }
+    // Bytes of the last mask word past the last element are defined as 0.
+    if (mask && a.mask_tail_bytes > 0 && blockIdx.x == 0 && threadIdx.x == 0)
+        for (int k = 0; k < a.mask_tail_bytes; ++k) mask[a.nv + k] = 0;
+}
+
+// Largest row whose bias the bias+ReLU+dropout forward keeps in shared memory
+// as FP32 (32 KB).
+constexpr int64_t kFwdSmemBiasMaxCols = 8192;
+
+// bias + ReLU + dropout, software-pipelined over two register buffers: while
+// chunk k is computed and stored, chunk k+1's loads are in flight, and its
+// Philox words are drawn right after, before it is needed.  The Philox and
+// select work of this operator is a large part of its time, so it runs under
+// the next chunk's memory latency instead of after it.  Measured on GB300 at
+// BERT-base / GPT-2-large FFN widths: 14.1 / 23.0 us against 15.6 / 25.1 us for
+// the unpipelined kernel with integer keep masks; two vectors per chunk at
+// three CTAs per SM beat one vector at four, and a non-persistent grid (one
+// chunk per thread) is slower (15.8 / 24.3 us).
+template <typename T, bool SMEMB, int U, typename I>
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 3 : 2)
+brd_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias,
+               const __grid_constant__ FwdArgs a) {
+    extern __shared__ __align__(16) float bsm[];  // [cols] FP32 bias when SMEMB
+    const PhiloxSchedule& ks = a.ks;
+    pdl_enter();
+    if (SMEMB) {
+        for (uint32_t c = threadIdx.x; c < a.nvr; c += kThreads) {
+            float b[kVec];
+            load8f<T>(bias + static_cast<size_t>(c) * kVec, b);
+            float4* d = reinterpret_cast<float4*>(bsm + c * kVec);
+            d[0] = make_float4(b[0], b[1], b[2], b[3]);
+            d[1] = make_float4(b[4], b[5], b[6], b[7]);
+        }
+        __syncthreads();
+    }
+    const I nv = static_cast<I>(a.nv);
+    const I S = static_cast<I>(gridDim.x) * kThreads;  // vectors per round
+    const I gw = blockIdx.x + static_cast<I>(threadIdx.x >> 5) * gridDim.x;
+    I v = gw * 32 + (threadIdx.x & 31);
+    uint32_t cv = static_cast<uint32_t>(v % a.nvr);
+    uint32_t stepU = 0;  // (U rounds) mod nvr, from the per-round step
+#pragma unroll
+    for (int u = 0; u < U; ++u) {
+        stepU += a.step_col;
+        if (stepU >= a.nvr) stepU -= a.nvr;
+    }
+    Raw8<T> xa[U], xb[U], unused[U];
+    uint4 wa[U], wb[U];
+    if (v < nv) {
+        fwd_load<T, true, U>(xa, unused, x, nullptr, v, S, nv);
+        fwd_words<U>(wa, wb, v, S, nv, a, ks);
+    }
+    while (v < nv) {
+        const I v1 = v + U * S;
+        fwd_load<T, true, U>(xb, unused, x, nullptr, v1, S, nv);
+        brd_compute<T, SMEMB, U>(xa, wa, wb, out, mask, bsm, bias, v, cv, S, nv, a);
+        cv += stepU;
+        if (cv >= a.nvr) cv -= a.nvr;
+        if (v1 >= nv) break;
+        fwd_words<U>(wa, wb, v1, S, nv, a, ks);
+        const I v2 = v1 + U * S;
+        fwd_load<T, true, U>(xa, unused, x, nullptr, v2, S, nv);
+        brd_compute<T, SMEMB, U>(xb, wa, wb, out, mask, bsm, bias, v1, cv, S, nv, a);
+        cv += stepU;
+        if (cv >= a.nvr) cv -= a.nvr;
+        if (v2 >= nv) break;
+        fwd_words<U>(wa, wb, v2, S, nv, a, ks);
+        v = v2;
     }
     // Bytes of the last mask word past the last element are defined as 0.
     if (mask && a.mask_tail_bytes > 0 && blockIdx.x == 0 && threadIdx.x == 0)
@@ -329,17 +481,13 @@ int occupancy(K kernel, int threads, size_t smem) {
 }
 
 constexpr int kFwdU = 2;
+// bias + ReLU + dropout: vectors per thread per chunk (two chunks in flight).
+constexpr int kBrdU = 2;
 
-template <typename T, bool RELU>
-cudaError_t fwd_impl(void* out, uint8_t* mask, const void* x, const void* bias,
-                     const void* residual, int64_t rows, int64_t cols, const DropoutRng& rng,
-                     cudaStream_t s) {
-    static const int occ = occupancy(dropout_fwd_kernel<T, RELU, kFwdU, uint64_t>, kThreads, 0);
+FwdArgs fwd_args(int64_t rows, int64_t cols, const DropoutRng& rng, int64_t grid) {
     FwdArgs a;
     a.nv = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols) / kVec;
     a.nvr = static_cast<uint32_t>(cols / kVec);
-    const int64_t want = static_cast<int64_t>((a.nv + kThreads * kFwdU - 1) / (kThreads * kFwdU));
-    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, int64_t{sm_count()} * occ));
     a.step_col = static_cast<uint32_t>((static_cast<uint64_t>(grid) * kThreads) % a.nvr);
     a.thr = rng.thr;
     a.scale = rng.scale;
@@ -347,16 +495,53 @@ cudaError_t fwd_impl(void* out, uint8_t* mask, const void* x, const void* bias,
     a.off_lo = static_cast<uint32_t>(rng.offset);
     a.off_hi = static_cast<uint32_t>(rng.offset >> 32);
     a.mask_tail_bytes = static_cast<int>(((a.nv + 3) / 4) * 4 - a.nv);
-    // 32-bit indices when no index the loop forms (up to nv + (U+1) rounds) and
-    // no counter block (2 * index) reaches 2^32.
-    const bool narrow =
-        a.nv + static_cast<uint64_t>(kFwdU + 1) * static_cast<uint64_t>(grid) * kThreads <
-        (uint64_t{1} << 31);
-    auto kern = narrow ? dropout_fwd_kernel<T, RELU, kFwdU, uint32_t>
-                       : dropout_fwd_kernel<T, RELU, kFwdU, uint64_t>;
+    return a;
+}
+
+// 32-bit indices when no index the loop forms (up to nv + (U+2) rounds) and no
+// counter block (2 * index) reaches 2^32.
+bool narrow_index(uint64_t nv, int64_t grid) {
+    return nv + static_cast<uint64_t>(kFwdU + 2) * static_cast<uint64_t>(grid) * kThreads <
+           (uint64_t{1} << 31);
+}
+
+template <typename T>
+cudaError_t bdr_fwd_impl(void* out, uint8_t* mask, const void* x, const void* bias,
+                         const void* residual, int64_t rows, int64_t cols, const DropoutRng& rng,
+                         cudaStream_t s) {
+    static const int occ = occupancy(bdr_fwd_kernel<T, kFwdU, uint64_t>, kThreads, 0);
+    const uint64_t nv = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols) / kVec;
+    const int64_t want = static_cast<int64_t>((nv + kThreads * kFwdU - 1) / (kThreads * kFwdU));
+    const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(want, int64_t{sm_count()} * occ));
+    const FwdArgs a = fwd_args(rows, cols, rng, grid);
+    auto kern = narrow_index(a.nv, grid) ? bdr_fwd_kernel<T, kFwdU, uint32_t>
+                                         : bdr_fwd_kernel<T, kFwdU, uint64_t>;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
                       static_cast<T*>(out), mask, static_cast<const T*>(x),
                       static_cast<const T*>(bias), static_cast<const T*>(residual), a);
+}
+
+template <typename T>
+cudaError_t brd_fwd_impl(void* out, uint8_t* mask, const void* x, const void* bias, int64_t rows,
+                         int64_t cols, const DropoutRng& rng, cudaStream_t s) {
+    const bool smemb = cols <= kFwdSmemBiasMaxCols;
+    const size_t smem = smemb ? static_cast<size_t>(cols) * sizeof(float) : 0;
+    static const int occ = occupancy(brd_fwd_kernel<T, false, kBrdU, uint64_t>, kThreads, 0);
+    static const int occ_s = occupancy(brd_fwd_kernel<T, true, kBrdU, uint64_t>, kThreads,
+                                       kFwdSmemBiasMaxCols * sizeof(float));
+    const uint64_t nv = static_cast<uint64_t>(rows) * static_cast<uint64_t>(cols) / kVec;
+    const int64_t want = static_cast<int64_t>((nv + kThreads * kBrdU - 1) / (kThreads * kBrdU));
+    const int64_t grid = std::max<int64_t>(
+        1, std::min<int64_t>(want, int64_t{sm_count()} * (smemb ? occ_s : occ)));
+    const FwdArgs a = fwd_args(rows, cols, rng, grid);
+    const bool narrow = narrow_index(a.nv, grid);
+    auto kern = smemb ? (narrow ? brd_fwd_kernel<T, true, kBrdU, uint32_t>
+                                : brd_fwd_kernel<T, true, kBrdU, uint64_t>)
+                      : (narrow ? brd_fwd_kernel<T, false, kBrdU, uint32_t>
+                                : brd_fwd_kernel<T, false, kBrdU, uint64_t>);
+    return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), smem, s,
+                      static_cast<T*>(out), mask, static_cast<const T*>(x),
+                      static_cast<const T*>(bias), a);
 }
 
 template <typename T>
@@ -414,10 +599,10 @@ cudaError_t launch_dropout_fwd(DType dt, bool relu, void* out, uint8_t* mask, co
                                const void* bias, const void* residual, int64_t rows, int64_t cols,
                                const DropoutRng& rng, cudaStream_t s) {
     if (dt == DType::F16)
-        return relu ? fwd_impl<__half, true>(out, mask, x, bias, residual, rows, cols, rng, s)
-                    : fwd_impl<__half, false>(out, mask, x, bias, residual, rows, cols, rng, s);
-    return relu ? fwd_impl<float, true>(out, mask, x, bias, residual, rows, cols, rng, s)
-                : fwd_impl<float, false>(out, mask, x, bias, residual, rows, cols, rng, s);
+        return relu ? brd_fwd_impl<__half>(out, mask, x, bias, rows, cols, rng, s)
+                    : bdr_fwd_impl<__half>(out, mask, x, bias, residual, rows, cols, rng, s);
+    return relu ? brd_fwd_impl<float>(out, mask, x, bias, rows, cols, rng, s)
+                : bdr_fwd_impl<float>(out, mask, x, bias, residual, rows, cols, rng, s);
 }
 
 cudaError_t launch_dropout_bwd(DType dt, void* dx, float* partial, const void* dout,

@@ -42,6 +42,20 @@ __device__ __forceinline__ void ln_fwd_load(Raw8<T> (&xr)[VPT], const T* x, int6
     }
 }
 
+// Element 0 of a vector as FP32.
+__device__ __forceinline__ float first_elem(const Raw8<__half>& r) {
+    return __low2float(*reinterpret_cast<const __half2*>(&r.v.x));
+}
+__device__ __forceinline__ float first_elem(const Raw8<float>& r) { return r.a.x; }
+
+// One row of the forward.  The differences d = x - K from the row's first
+// element K are formed once (FP16 converts exactly, folded into the subtract)
+// and kept in registers for both passes; the sums and the output use packed
+// FP32 pairs.  Each result is the FP32 operation on the same operands, rounded
+// once, as in the plain form.  gamma/beta are read per row, after the row's
+// loads: measured on GB300, loading every lane's gamma/beta columns when the
+// kernel starts is slower (4.8 against 4.1 us at 4096 x 768), as every warp
+// then asks L2 for the same few lines at the same moment.
 template <typename T, int LPR, int VPT>
 __device__ __forceinline__ void ln_fwd_row(const Raw8<T> (&xr)[VPT], T* y, float* mean,
                                            float* rstd, const T* __restrict__ gamma,
@@ -49,47 +63,46 @@ __device__ __forceinline__ void ln_fwd_row(const Raw8<T> (&xr)[VPT], T* y, float
                                            int cols, float eps, int gl) {
     const bool row_ok = r < rows;
     const int nvec = cols / kVec;
-    float f[VPT][kVec];
-#pragma unroll
-    for (int k = 0; k < VPT; ++k) {
-        if (row_ok && gl + k * LPR < nvec) {
-            unpack(xr[k], f[k]);
-        } else {
-#pragma unroll
-            for (int j = 0; j < kVec; ++j) f[k][j] = 0.f;
-        }
-    }
     // Sums about the row's first element K (held by the group's lane 0):
     // var = mu((x-K)^2) - mu(x-K)^2 is the same identity, without cancellation
     // when |mean| >> std.
-    const float K = __shfl_sync(0xffffffffu, f[0][0], 0, LPR);
-    float2 s = make_float2(0.f, 0.f);
+    const float K = __shfl_sync(0xffffffffu, first_elem(xr[0]), 0, LPR);
+    float d[VPT][kVec];
+    float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         if (row_ok && gl + k * LPR < nvec) {
+            sub8(xr[k], K, d[k]);
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) {
-                const float d = f[k][j] - K;
-                s.x += d;
-                s.y = fmaf(d, d, s.y);
+            for (int j = 0; j < kVec; j += 2) {
+                const float2 dj = make_float2(d[k][j], d[k][j + 1]);
+                sa = add2(sa, dj);
+                sb = fma2(dj, dj, sb);
             }
         }
     }
+    float2 s = make_float2(sa.x + sa.y, sb.x + sb.y);
     s = group_sum2<LPR>(s);  // the single synchronisation
     const float inv_n = 1.f / static_cast<float>(cols);
     const float m1 = s.x * inv_n;
     const float var = fmaxf(fmaf(-m1, m1, s.y * inv_n), 0.f);
     const float rs = rsqrtf(var + eps);
     if (!row_ok) return;
+    const float2 m2 = make_float2(-m1, -m1), r2 = make_float2(rs, rs);
 #pragma unroll
     for (int k = 0; k < VPT; ++k) {
         const int v = gl + k * LPR;
         if (v < nvec) {
-            float g[kVec], b[kVec], o[kVec];
+            float o[kVec], g[kVec], b[kVec];
             load8f<T>(gamma + v * kVec, g);
             load8f<T>(beta + v * kVec, b);
 #pragma unroll
-            for (int j = 0; j < kVec; ++j) o[j] = fmaf((f[k][j] - K - m1) * rs, g[j], b[j]);
+            for (int j = 0; j < kVec; j += 2) {
+                float2 t = mul2(add2(make_float2(d[k][j], d[k][j + 1]), m2), r2);
+                t = fma2(t, make_float2(g[j], g[j + 1]), make_float2(b[j], b[j + 1]));
+                o[j] = t.x;
+                o[j + 1] = t.y;
+            }
             store8f<T>(y + r * cols + v * kVec, o);
         }
     }
@@ -100,7 +113,7 @@ __device__ __forceinline__ void ln_fwd_row(const Raw8<T> (&xr)[VPT], T* y, float
 }
 
 template <typename T, int LPR, int VPT>
-__global__ void __launch_bounds__(kThreads, min_ctas<T>(VPT <= 3 ? 4 : (VPT <= 4 ? 3 : 2)))
+__global__ void __launch_bounds__(kThreads, min_ctas<T>(VPT == 2 ? 3 : (VPT <= 3 ? 4 : (VPT <= 4 ? 3 : 2))))
 ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, const T* x,
                     const T* __restrict__ gamma, const T* __restrict__ beta, int64_t rows,
                     int cols, float eps) {
@@ -111,23 +124,27 @@ ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, co
     const int64_t stride = static_cast<int64_t>(gridDim.x) * RPC;
     int64_t r = static_cast<int64_t>(slot) * gridDim.x + blockIdx.x;
     Raw8<T> xa[VPT], xb[VPT];
+    const T* gs = gamma;
+    const T* bs = beta;
+    ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
     if (VPT > 2) {
         // Wide rows: one buffer (a second would cost occupancy).
-        for (; __any_sync(0xffffffffu, r < rows); r += stride) {
+        while (__any_sync(0xffffffffu, r < rows)) {
+            ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gs, bs, r, rows, cols, eps, gl);
+            r += stride;
+            if (!__any_sync(0xffffffffu, r < rows)) break;
             ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
-            ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gamma, beta, r, rows, cols, eps, gl);
         }
         return;
     }
-    ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
     while (__any_sync(0xffffffffu, r < rows)) {
         const int64_t r1 = r + stride;
         ln_fwd_load<T, LPR, VPT>(xb, x, r1, rows, cols, gl);
-        ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gamma, beta, r, rows, cols, eps, gl);
+        ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gs, bs, r, rows, cols, eps, gl);
         if (!__any_sync(0xffffffffu, r1 < rows)) break;
         r = r1 + stride;
         ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
-        ln_fwd_row<T, LPR, VPT>(xb, y, mean, rstd, gamma, beta, r1, rows, cols, eps, gl);
+        ln_fwd_row<T, LPR, VPT>(xb, y, mean, rstd, gs, bs, r1, rows, cols, eps, gl);
     }
 }
 
@@ -383,39 +400,80 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
         const float mu = mu_of[s], rs = rs_of[s];
         const T* xs = reinterpret_cast<const T*>(ring.stage(s));
         const T* ds = reinterpret_cast<const T*>(ring.stage(s) + row_bytes);
-        float2 sum = make_float2(0.f, 0.f);
+        // g = gamma*dy and xhat = (x - mu)*rstd, formed once per element with the
+        // mixed-precision forms (FP16 operands convert exactly inside them);
+        // kept in registers for the second pass when they fit, else re-formed.
+        constexpr bool kKeep = VPT <= 3;
+        float gk[kKeep ? VPT : 1][kVec], hk[kKeep ? VPT : 1][kVec];
+        float2 sa = make_float2(0.f, 0.f), sb = make_float2(0.f, 0.f);
+        const float2 rs2 = make_float2(rs, rs);
 #pragma unroll
         for (int k2 = 0; k2 < VPT; ++k2) {
             const int v = lane + k2 * 32;
             if (v < nvec) {
-                float xf[kVec], df[kVec], gf[kVec];
-                unpack(load8_smem<T>(xs + v * kVec), xf);
-                unpack(load8_smem<T>(ds + v * kVec), df);
-                unpack(load8_smem<T>(gsm + v * kVec), gf);
+                float g[kVec], h[kVec];
+                mul8(load8_smem<T>(gsm + v * kVec), load8_smem<T>(ds + v * kVec), g);
+                sub8(load8_smem<T>(xs + v * kVec), mu, h);
 #pragma unroll
-                for (int j = 0; j < kVec; ++j) {
-                    const float g = gf[j] * df[j];
-                    sum.x += g;
-                    sum.y = fmaf(g, (xf[j] - mu) * rs, sum.y);
+                for (int j = 0; j < kVec; j += 2) {
+                    const float2 hj = mul2(make_float2(h[j], h[j + 1]), rs2);
+                    const float2 gj = make_float2(g[j], g[j + 1]);
+                    sa = add2(sa, gj);
+                    sb = fma2(gj, hj, sb);
+                    h[j] = hj.x;
+                    h[j + 1] = hj.y;
+                }
+                if (kKeep) {
+#pragma unroll
+                    for (int j = 0; j < kVec; ++j) {
+                        gk[kKeep ? k2 : 0][j] = g[j];
+                        hk[kKeep ? k2 : 0][j] = h[j];
+                    }
                 }
             }
         }
+        float2 sum = make_float2(sa.x + sa.y, sb.x + sb.y);
         sum = group_sum2<32>(sum);  // the single synchronisation
-        const float a_n = sum.x * inv_n, c_n = sum.y * inv_n;
+        const float2 na = make_float2(-sum.x * inv_n, -sum.x * inv_n);
+        const float2 nc = make_float2(-sum.y * inv_n, -sum.y * inv_n);
 #pragma unroll
         for (int k2 = 0; k2 < VPT; ++k2) {
             const int v = lane + k2 * 32;
             if (v < nvec) {
-                float xf[kVec], df[kVec], gf[kVec], o[kVec];
-                unpack(load8_smem<T>(xs + v * kVec), xf);
-                unpack(load8_smem<T>(ds + v * kVec), df);
-                unpack(load8_smem<T>(gsm + v * kVec), gf);
+                const Raw8<T> dr = load8_smem<T>(ds + v * kVec);
+                float g[kVec], h[kVec], df[kVec], o[kVec];
+                if (kKeep) {
 #pragma unroll
-                for (int j = 0; j < kVec; ++j) {
-                    const float xh = (xf[j] - mu) * rs;
-                    o[j] = rs * (gf[j] * df[j] - a_n - xh * c_n);
-                    ag[k2][j] = fmaf(df[j], xh, ag[k2][j]);
-                    ab[k2][j] += df[j];
+                    for (int j = 0; j < kVec; ++j) {
+                        g[j] = gk[kKeep ? k2 : 0][j];
+                        h[j] = hk[kKeep ? k2 : 0][j];
+                    }
+                } else {
+                    mul8(load8_smem<T>(gsm + v * kVec), dr, g);
+                    sub8(load8_smem<T>(xs + v * kVec), mu, h);
+#pragma unroll
+                    for (int j = 0; j < kVec; j += 2) {
+                        const float2 hj = mul2(make_float2(h[j], h[j + 1]), rs2);
+                        h[j] = hj.x;
+                        h[j + 1] = hj.y;
+                    }
+                }
+                unpack(dr, df);
+#pragma unroll
+                for (int j = 0; j < kVec; j += 2) {
+                    // dx = rstd * ((g - A/H) - xhat * C/H)
+                    const float2 hj = make_float2(h[j], h[j + 1]);
+                    const float2 t = fma2(hj, nc, add2(make_float2(g[j], g[j + 1]), na));
+                    const float2 oj = mul2(t, rs2);
+                    o[j] = oj.x;
+                    o[j + 1] = oj.y;
+                    const float2 dj = make_float2(df[j], df[j + 1]);
+                    const float2 agj = fma2(dj, hj, make_float2(ag[k2][j], ag[k2][j + 1]));
+                    const float2 abj = add2(dj, make_float2(ab[k2][j], ab[k2][j + 1]));
+                    ag[k2][j] = agj.x;
+                    ag[k2][j + 1] = agj.y;
+                    ab[k2][j] = abj.x;
+                    ab[k2][j + 1] = abj.y;
                 }
                 store8f<T>(dx + r * cols + v * kVec, o);
             }

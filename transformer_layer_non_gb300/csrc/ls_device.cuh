@@ -196,6 +196,27 @@ __device__ __forceinline__ void sub8(const Raw8<float>& a, float c, float (&t)[8
     for (int j = 0; j < 8; ++j) t[j] -= c;
 }
 
+// t[j] = a[j] * b[j], exact for FP16 operands (their product fits FP32), as
+// fma.rn.f32.f16 with a zero addend.
+__device__ __forceinline__ void mul8(const Raw8<__half>& a, const Raw8<__half>& b, float (&t)[8]) {
+    const uint32_t aw[4] = {a.v.x, a.v.y, a.v.z, a.v.w};
+    const uint32_t bw[4] = {b.v.x, b.v.y, b.v.z, b.v.w};
+#pragma unroll
+    for (int k = 0; k < 4; ++k)
+        asm("{\n\t.reg .f16 al, ah, bl, bh;\n\t"
+            "mov.b32 {al, ah}, %2;\n\tmov.b32 {bl, bh}, %3;\n\t"
+            "fma.rn.f32.f16 %0, al, bl, 0f00000000;\n\tfma.rn.f32.f16 %1, ah, bh, 0f00000000;\n\t}"
+            : "=f"(t[2 * k]), "=f"(t[2 * k + 1])
+            : "r"(aw[k]), "r"(bw[k]));
+}
+__device__ __forceinline__ void mul8(const Raw8<float>& a, const Raw8<float>& b, float (&t)[8]) {
+    float x[8], y[8];
+    unpack(a, x);
+    unpack(b, y);
+#pragma unroll
+    for (int j = 0; j < 8; ++j) t[j] = x[j] * y[j];
+}
+
 // ---------------------------------------------------------------------------
 // Packed FP32 pairs (PTX add/mul/fma .rn.f32x2, sm_100 and later): one
 // instruction does the same operation on two lanes, each rounded as the scalar

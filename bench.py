@@ -73,6 +73,14 @@ def parse_args():
                          "--profile-k-len keys) inside the NVTX range 'profile' (for ncu --nvtx "
                          "--nvtx-include profile/); no timing")
     ap.add_argument("--profile-launches", type=int, default=2)
+    ap.add_argument("--profile-flush-mb", type=int, default=0,
+                    help="--profile-op: end the range with a read of a clean buffer of this "
+                         "many MB (larger than L2), which evicts the launches' dirty lines so "
+                         "that their write-backs are counted inside the range")
+    ap.add_argument("--profile-sets", type=int, default=1,
+                    help="--profile-op: launch the operator once on each of this many cloned "
+                         "buffer sets inside the range (for ncu range replay, so that earlier "
+                         "launches' write-backs from L2 land inside the measured range)")
     ap.add_argument("--profile-k-len", type=int, default=65536,
                     help="row length of --profile-op softmax_long_fwd/bwd (2^26 elements)")
     ap.add_argument("--reductions", default="side", choices=["side", "inline"],
@@ -1069,17 +1077,46 @@ def run_profile_op(args):
         fn()
     torch.cuda.synchronize()
     order = []
+    sets = [None]
+    if args.profile_sets > 1:
+        if len(names) != 1:
+            print(json.dumps({"error": "--profile-sets needs a single --profile-op"}))
+            return 2
+        keys = [k for k in LayerStep.TENSORS[names[0]] if k in step.t]
+        sets = []
+        for _ in range(args.profile_sets):
+            t = dict(step.t)
+            for k in keys:
+                t[k] = step.t[k].clone()
+            sets.append(t)
+        torch.cuda.synchronize()
+    flush = None
+    if args.profile_flush_mb > 0:
+        # Two buffers filled, then both read: the fills' dirty lines are written
+        # back before the range, and L2 holds only clean lines when it starts.
+        nb = args.profile_flush_mb << 20
+        flush = torch.ones(nb // 2, dtype=torch.float16, device="cuda")
+        other = torch.ones(nb // 2, dtype=torch.float16, device="cuda")
+        flush.sum()
+        other.sum()
+        torch.cuda.synchronize()
+        del other
     torch.cuda.nvtx.range_push("profile")
-    for n in names:
-        for _ in range(args.profile_launches):
-            dict(ops)[n]()
-            order += [n] * step.launches[n]
+    for t in sets:
+        set_ops = dict(step.ops(t))
+        for n in names:
+            for _ in range(args.profile_launches):
+                set_ops[n]()
+                order += [n] * step.launches[n]
+    if flush is not None:
+        flush.sum()  # reads the clean buffer, evicting the launches' dirty lines
     torch.cuda.nvtx.range_pop()
     torch.cuda.synchronize()
     from transformer_layer_non_gb300.ncu_report import kernels_sha
 
     print(json.dumps({"profile_op": args.profile_op, "workload": args.workload,
-                      "kernels_sha": kernels_sha(),
+                      "kernels_sha": kernels_sha(), "buffer_sets": len(sets),
+                      "flush_read_bytes": (args.profile_flush_mb << 20) if flush is not None else 0,
                       "launches_per_op": args.profile_launches, "launch_order": order,
                       "algorithmic_bytes": {n: int(step.bytes[n]) for n in names}}))
     return 0

@@ -137,3 +137,30 @@ def test_bench_reads_traffic_only_for_the_current_sources(tmp_path, monkeypatch)
         {"kernels_sha": "0" * 16, "ops": {"bert-base": entry}}))
     assert bench.ncu_traffic("softmax_bwd", "bert-base") is None       # stale sources
     assert os.path.isdir(prof)
+
+
+def test_range_report_subtracts_the_flush_and_divides_by_launches(tmp_path):
+    # Two range captures: 4 launches each, a 512 MB flush read in the range.
+    flush = 512 << 20
+    for tag, op, rd, wr, alg in [("a", "softmax_bwd", 4 * 64e6 + flush, 4 * 51e6, 111e6),
+                                 ("b", "ln2_bwd", 8 * 12.6e6 + flush, 8 * 6.9e6, 18.9e6)]:
+        n = 4 if tag == "a" else 8
+        _csv(tmp_path / f"{tag}.csv", [
+            ("0", "range", "", "", "dram__bytes_read.sum", "byte", f"{rd:.0f}"),
+            ("0", "range", "", "", "dram__bytes_write.sum", "byte", f"{wr:.0f}"),
+            ("0", "range", "", "", "gpu__time_duration.sum", "ns", "1000")])
+        _json_line(tmp_path / f"{tag}.log", {
+            "profile_op": op, "workload": "bert-base", "kernels_sha": "abc", "buffer_sets": n,
+            "launches_per_op": 1, "flush_read_bytes": flush, "launch_order": [op] * n,
+            "algorithmic_bytes": {op: alg}})
+    out, js = tmp_path / "r.md", tmp_path / "t.json"
+    ncu_report.main(["range", "--case", f"x={tmp_path / 'a.csv'},{tmp_path / 'a.log'}",
+                     "--case", f"y={tmp_path / 'b.csv'},{tmp_path / 'b.log'}",
+                     "--command", "cmd", "--out", str(out), "--json", str(js)])
+    d = json.load(open(js))
+    assert d["kernels_sha"] == "abc"
+    e = d["ops"]["bert-base"]["softmax_bwd"]
+    assert e["dram_read_bytes"] == 64000000 and e["dram_write_bytes"] == 51000000
+    e = d["ops"]["bert-base"]["ln2_bwd"]
+    assert e["dram_read_bytes"] == 12600000 and e["dram_write_bytes"] == 6900000
+    assert "| bert-base | softmax_bwd | 4 |" in open(out).read()

@@ -681,11 +681,12 @@ LnPlan plan_for(int64_t rows, int64_t cols, bool bwd, size_t esize) {
     return p;
 }
 
+// Raises the kernel's dynamic shared-memory limit (once per kernel and
+// device) when `bytes` needs more than the default 48 KB.
 template <typename K>
-cudaError_t set_smem(K kernel, size_t bytes) {
+cudaError_t set_smem(K kernel, size_t bytes, int (&done)[kMaxDevices]) {
     if (bytes <= 48 * 1024) return cudaSuccess;
-    return cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                static_cast<int>(bytes));
+    return allow_max_dynamic_smem(kernel, done);
 }
 
 template <typename K>
@@ -728,7 +729,8 @@ cudaError_t bwd_group(void* dx, float* partial, const void* dy, const void* x, c
         if (ln_bwd_uses_tma(cols, sizeof(T))) {
             const size_t smem = ln_tma_smem(cols, sizeof(T));
             auto kern = ln_bwd_tma_kernel<T, VPT>;
-            cudaError_t e = set_smem(kern, smem);
+            static int done[kMaxDevices] = {};
+            cudaError_t e = set_smem(kern, smem, done);
             if (e != cudaSuccess) return e;
             return launch_pdl(kern, dim3(static_cast<unsigned>(p.grid)), dim3(kLnTmaWarps * 32),
                               smem, s, static_cast<T*>(dx), partial, static_cast<const T*>(dy),
@@ -739,7 +741,8 @@ cudaError_t bwd_group(void* dx, float* partial, const void* dy, const void* x, c
     const size_t smem = partial ? static_cast<size_t>(kThreads / LPR) * 2 * cols * sizeof(float)
                                 : 0;
     auto kern = ln_bwd_group_kernel<T, LPR, VPT>;
-    cudaError_t e = set_smem(kern, smem);
+    static int done[kMaxDevices] = {};
+    cudaError_t e = set_smem(kern, smem, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(static_cast<unsigned>(p.grid)), dim3(kThreads), smem, s,
                       static_cast<T*>(dx), partial, static_cast<const T*>(dy),
@@ -753,7 +756,8 @@ cudaError_t bwd_cta(void* dx, float* partial, const void* dy, const void* x, con
                     const LnPlan& p, cudaStream_t s) {
     const size_t smem = partial ? 2 * static_cast<size_t>(cols) * sizeof(float) : 0;
     auto kern = ln_bwd_cta_kernel<T, WARPS, VPT>;
-    cudaError_t e = set_smem(kern, smem);
+    static int done[kMaxDevices] = {};
+    cudaError_t e = set_smem(kern, smem, done);
     if (e != cudaSuccess) return e;
     return launch_pdl(kern, dim3(static_cast<unsigned>(p.grid)), dim3(WARPS * 32), smem, s,
                       static_cast<T*>(dx), partial, static_cast<const T*>(dy),

@@ -381,6 +381,27 @@ __device__ __forceinline__ void pdl_enter() {
     pdl_trigger();
 }
 
+// Lets `kernel` use up to the device's opt-in maximum of dynamic shared
+// memory.  The attribute is set once per kernel and device (`done` is the
+// caller's per-kernel table, indexed by device), not on every launch: setting
+// it is a driver call that stream capture for profiling ranges does not
+// accept, and it costs host time on every eager call.
+constexpr int kMaxDevices = 64;
+template <typename K>
+inline cudaError_t allow_max_dynamic_smem(K kernel, int (&done)[kMaxDevices]) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return e;
+    if (dev >= 0 && dev < kMaxDevices && __atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) return e;
+    int optin = 0;
+    e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    if (e == cudaSuccess)
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+    if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices)
+        __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
+    return e;
+}
+
 template <typename... KArgs, typename... Args>
 inline cudaError_t launch_pdl(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
                               cudaStream_t stream, Args... args) {

@@ -379,6 +379,7 @@ softmax_group_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, R
 // ----------------------------------------------------------------------------
 constexpr int kTmaWarps = 4;
 constexpr int kTmaStages = 2;
+constexpr int kTmaMaxLen = 1024;  // longest row of the warp-per-row path
 
 __host__ __device__ constexpr uint32_t tma_bar_bytes() {
     return ((kTmaWarps * kTmaStages * 8 + 127) / 128) * 128;
@@ -1004,11 +1005,19 @@ cudaError_t tma_launch(T* out, const T* p, const T* q, int64_t nrows, int k_len,
     const size_t stage = static_cast<size_t>(k_len) * sizeof(T) * (BWD ? 2 : 1);
     const size_t smem = tma_bar_bytes() + static_cast<size_t>(kTmaWarps) * kTmaStages * stage;
     if (smem > 48 * 1024) {
-        cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        static int done[kMaxDevices] = {};
+        const cudaError_t e = allow_max_dynamic_smem(kern, done);
         if (e != cudaSuccess) return e;
     }
-    const int occ = occupancy(kern, kTmaWarps * 32, smem);
+    // Resident CTAs for this row length, queried once per length (k_len <= 1024
+    // on this path: 128 lengths) rather than on every launch.
+    static int occ_by_len[kTmaMaxLen / kVec + 1] = {};
+    const int li = k_len / kVec;
+    int occ = li <= kTmaMaxLen / kVec ? __atomic_load_n(&occ_by_len[li], __ATOMIC_RELAXED) : 0;
+    if (occ == 0) {
+        occ = occupancy(kern, kTmaWarps * 32, smem);
+        if (li <= kTmaMaxLen / kVec) __atomic_store_n(&occ_by_len[li], occ, __ATOMIC_RELAXED);
+    }
     const int64_t need = (nrows + kTmaWarps - 1) / kTmaWarps;
     const int64_t grid = std::max<int64_t>(1, std::min<int64_t>(need, int64_t{sm_count()} * occ));
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kTmaWarps * 32), smem, s, out,

@@ -1,6 +1,6 @@
 """Summaries of Nsight Compute output for the layer-step benchmark.
 
-Three reports, each written as a short markdown file (and one JSON file that
+Four reports, each written as a short markdown file (and one JSON file that
 bench.py reads):
 
   launches  ncu CSV of `--metrics gpu__time_duration.sum` over whole layer
@@ -13,6 +13,12 @@ bench.py reads):
             voids the figures.
   full      an `ncu --set full` report (.ncu-rep) -> the counters that say
             what bounds the kernel (DRAM, issue, pipes, stalls, occupancy).
+  range     ncu CSVs of range replay (`--replay-mode range`) over `bench.py
+            --profile-op OP --profile-sets K --profile-flush-mb M`: K launches
+            of one operator on K buffer sets, then a read of a clean M MB buffer
+            that evicts their dirty lines from L2, so that reads AND write-backs
+            are counted -> DRAM bytes per launch (the flush read subtracted)
+            against the algorithmic bytes; also written to the JSON.
 
 Per-launch times under ncu are serialised and cold-cache (ncu flushes the
 caches before every profiled launch): compare shares, not absolutes.  DRAM
@@ -26,6 +32,9 @@ when it ends, since L2 writes back later.
         --out profiles/Y.md --json profiles/ncu_traffic.json
     python -m transformer_layer_non_gb300.ncu_report full --rep R.ncu-rep \
         --command "..." --out profiles/Z.md
+    python -m transformer_layer_non_gb300.ncu_report range \
+        --case bert-base:softmax_bwd=R.csv,plain.log ... --command "..." \
+        --out profiles/W.md --json profiles/ncu_traffic.json
 """
 from __future__ import annotations
 
@@ -209,6 +218,67 @@ def report_traffic(a):
             f.write("\n")
 
 
+def range_case(csv_path, log_path):
+    """(workload, op, launches, read, write, algorithmic, flush) of one range
+    capture: per-launch DRAM read bytes (the flush read subtracted) and write
+    bytes."""
+    rows = read_ncu_csv(csv_path)
+    m = {r["Metric Name"]: value(r) for r in rows}
+    prof = last_json_line(log_path)
+    (op, alg), = prof["algorithmic_bytes"].items()
+    n = prof["buffer_sets"] * prof["launches_per_op"]
+    flush = prof.get("flush_read_bytes", 0)
+    rd = (m["dram__bytes_read.sum"] - flush) / n
+    wr = m["dram__bytes_write.sum"] / n
+    return prof["workload"], op, n, rd, wr, float(alg), flush, prof.get("kernels_sha")
+
+
+def report_range(a):
+    cases = []
+    for spec in a.case:
+        csv_path, log_path = spec.split("=", 1)[1].split(",")
+        cases.append(range_case(csv_path, log_path))
+    shas = {c[7] for c in cases}
+    sha = a.sha or (shas.pop() if len(shas) == 1 else kernels_sha())
+    out = ["# DRAM traffic per operator launch, reads and write-backs (ncu range replay)", "",
+           "Command per case (one GB300; OP, WORKLOAD, K as in the table):", ""]
+    out += ["    " + ln for ln in a.command.splitlines()]
+    out += ["", f"Kernel sources hash: `{sha}`.  Each range holds K launches of the operator "
+            "on K distinct buffer sets, then a read of a clean buffer larger than L2 that "
+            "evicts their dirty lines, so the write-backs land inside the range; the "
+            "flush's own reads are subtracted.  Figures are per operator launch (main "
+            "kernel plus its column reduction, if any).", "",
+            "| workload | operator | K | algorithmic MB | DRAM read MB | DRAM write MB | "
+            "read+write / algorithmic |", "|---|---|---|---|---|---|---|"]
+    js = {}
+    for wl, op, n, rd, wr, alg, _, _ in cases:
+        out.append(f"| {wl} | {op} | {n} | {alg / 1e6:.2f} | {rd / 1e6:.2f} | {wr / 1e6:.2f} | "
+                   f"{(rd + wr) / alg:.3f} |")
+        js.setdefault(wl, {})[op] = {"dram_bytes_per_launch": int(rd + wr),
+                                     "dram_read_bytes": int(rd), "dram_write_bytes": int(wr),
+                                     "algorithmic_bytes": int(alg),
+                                     "method": "range replay, L2 flushed by a read"}
+    if a.note:
+        out += ["", a.note]
+    with open(a.out, "w") as f:
+        f.write("\n".join(out) + "\n")
+    if a.json:
+        d = {}
+        if os.path.exists(a.json):
+            with open(a.json) as f:
+                d = json.load(f)
+            if d.get("kernels_sha") != sha:
+                d = {}
+        d["kernels_sha"] = sha
+        d["note"] = ("DRAM bytes per operator launch from ncu (dram__bytes_read.sum + "
+                     "dram__bytes_write.sum); valid only for the kernel sources of this hash")
+        for wl, ops in js.items():
+            d.setdefault("ops", {}).setdefault(wl, {}).update(ops)
+        with open(a.json, "w") as f:
+            json.dump(d, f, indent=1)
+            f.write("\n")
+
+
 FULL_METRICS = [
     ("gpu__time_duration.sum", "duration"),
     ("launch__grid_size", "grid"),
@@ -288,6 +358,15 @@ def main(argv=None):
     p.add_argument("--sha", default=None, help="kernel sources hash the capture ran on "
                    "(default: the current sources)")
     p.add_argument("--note", default="")
+    p = sub.add_parser("range")
+    p.add_argument("--case", action="append", required=True,
+                   help="LABEL=CSV,LOG: one range capture and the stdout of its bench.py "
+                        "--profile-op command (repeatable)")
+    p.add_argument("--command", required=True)
+    p.add_argument("--out", required=True)
+    p.add_argument("--json", default=None)
+    p.add_argument("--sha", default=None)
+    p.add_argument("--note", default="")
     p = sub.add_parser("full")
     p.add_argument("--rep", required=True)
     p.add_argument("--title", required=True)
@@ -295,7 +374,8 @@ def main(argv=None):
     p.add_argument("--out", required=True)
     p.add_argument("--note", default="")
     a = ap.parse_args(argv)
-    {"launches": report_launches, "traffic": report_traffic, "full": report_full}[a.mode](a)
+    {"launches": report_launches, "traffic": report_traffic, "full": report_full,
+     "range": report_range}[a.mode](a)
 
 
 if __name__ == "__main__":

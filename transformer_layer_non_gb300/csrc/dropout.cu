@@ -210,6 +210,7 @@ bdr_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias, co
                const __grid_constant__ FwdArgs a) {
     const PhiloxSchedule& ks = a.ks;
     pdl_enter();
+    prefetch_params_l2(bias, static_cast<size_t>(a.nvr) * kVec * sizeof(T));
     const I nv = static_cast<I>(a.nv);
     const I S = static_cast<I>(gridDim.x) * kThreads;  // vectors per round
     const I gw = blockIdx.x + static_cast<I>(threadIdx.x >> 5) * gridDim.x;
@@ -256,16 +257,6 @@ brd_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias,
     extern __shared__ __align__(16) float bsm[];  // [cols] FP32 bias when SMEMB
     const PhiloxSchedule& ks = a.ks;
     pdl_enter();
-    if (SMEMB) {
-        for (uint32_t c = threadIdx.x; c < a.nvr; c += kThreads) {
-            float b[kVec];
-            load8f<T>(bias + static_cast<size_t>(c) * kVec, b);
-            float4* d = reinterpret_cast<float4*>(bsm + c * kVec);
-            d[0] = make_float4(b[0], b[1], b[2], b[3]);
-            d[1] = make_float4(b[4], b[5], b[6], b[7]);
-        }
-        __syncthreads();
-    }
     const I nv = static_cast<I>(a.nv);
     const I S = static_cast<I>(gridDim.x) * kThreads;  // vectors per round
     const I gw = blockIdx.x + static_cast<I>(threadIdx.x >> 5) * gridDim.x;
@@ -279,10 +270,20 @@ brd_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias,
     }
     Raw8<T> xa[U], xb[U], unused[U];
     uint4 wa[U], wb[U];
-    if (v < nv) {
-        fwd_load<T, true, U>(xa, unused, x, nullptr, v, S, nv);
-        fwd_words<U>(wa, wb, v, S, nv, a, ks);
+    // The first chunk's loads go out before the bias is staged, so that the
+    // bias's first (cold) read overlaps them instead of preceding them.
+    if (v < nv) fwd_load<T, true, U>(xa, unused, x, nullptr, v, S, nv);
+    if (SMEMB) {
+        for (uint32_t c = threadIdx.x; c < a.nvr; c += kThreads) {
+            float b[kVec];
+            load8f<T>(bias + static_cast<size_t>(c) * kVec, b);
+            float4* d = reinterpret_cast<float4*>(bsm + c * kVec);
+            d[0] = make_float4(b[0], b[1], b[2], b[3]);
+            d[1] = make_float4(b[4], b[5], b[6], b[7]);
+        }
     }
+    if (v < nv) fwd_words<U>(wa, wb, v, S, nv, a, ks);
+    if (SMEMB) __syncthreads();
     while (v < nv) {
         const I v1 = v + U * S;
         fwd_load<T, true, U>(xb, unused, x, nullptr, v1, S, nv);

@@ -127,6 +127,8 @@ ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, co
     const T* gs = gamma;
     const T* bs = beta;
     ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
+    prefetch_params_l2(gamma, static_cast<size_t>(cols) * sizeof(T));
+    prefetch_params_l2(beta, static_cast<size_t>(cols) * sizeof(T));
     if (VPT > 2) {
         // Wide rows: one buffer (a second would cost occupancy).
         while (__any_sync(0xffffffffu, r < rows)) {

@@ -55,6 +55,21 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Prefetch of a small parameter vector (bias, gamma, beta: `bytes` bytes from
+// p) into L2, one request per 128-byte line, by the first CTA only.  Kernels
+// that read such a vector after their rows' loads issue this at their start,
+// so that the other CTAs' reads find the lines in L2 instead of paying a DRAM
+// round trip on the row's critical path.  (Measured on GB300: the same
+// prefetch from every CTA is slower than none -- hundreds of requests for
+// the same lines queue at one L2 slice ahead of the rows' own loads.)
+__device__ __forceinline__ void prefetch_params_l2(const void* p, size_t bytes) {
+    if (blockIdx.x != 0) return;
+    const char* c = static_cast<const char*>(p);
+    for (size_t off = static_cast<size_t>(threadIdx.x) * 128; off < bytes;
+         off += static_cast<size_t>(blockDim.x) * 128)
+        prefetch_l2(c + off);
+}
+
 template <typename T> struct Raw8;
 template <> struct Raw8<__half> { uint4 v; };
 template <> struct Raw8<float> { float4 a, b; };
@@ -395,8 +410,12 @@ inline cudaError_t allow_max_dynamic_smem(K kernel, int (&done)[kMaxDevices]) {
     if (dev >= 0 && dev < kMaxDevices && __atomic_load_n(&done[dev], __ATOMIC_ACQUIRE)) return e;
     int optin = 0;
     e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
+    // The kernel's own static shared memory counts against the same limit.
+    cudaFuncAttributes fa;
+    if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
     if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
+        e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 optin - static_cast<int>(fa.sharedSizeBytes));
     if (e == cudaSuccess && dev >= 0 && dev < kMaxDevices)
         __atomic_store_n(&done[dev], 1, __ATOMIC_RELEASE);
     return e;

@@ -210,7 +210,6 @@ bdr_fwd_kernel(T* out, uint8_t* mask, const T* x, const T* __restrict__ bias, co
                const __grid_constant__ FwdArgs a) {
     const PhiloxSchedule& ks = a.ks;
     pdl_enter();
-    prefetch_params_l2(bias, static_cast<size_t>(a.nvr) * kVec * sizeof(T));
     const I nv = static_cast<I>(a.nv);
     const I S = static_cast<I>(gridDim.x) * kThreads;  // vectors per round
     const I gw = blockIdx.x + static_cast<I>(threadIdx.x >> 5) * gridDim.x;

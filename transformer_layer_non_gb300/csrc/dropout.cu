@@ -9,9 +9,12 @@
 // walks the vectors in rounds: in round k, warp w of CTA b takes the 32
 // consecutive vectors starting at (k * W + b + w * gridDim) * 32, W = all warps.
 // The last, partial round is thus spread over every CTA instead of piling onto
-// a few SMs.  A thread handles U rounds at a time: it issues their loads,
-// draws their keep bits (two Philox calls per vector) while the loads are in
-// flight, then computes in FP32 and stores.
+// a few SMs.  A thread handles U rounds at a time: it issues their loads and
+// draws their Philox words (two Philox calls per vector) while the loads are in
+// flight, then computes in FP32 and stores.  bias+dropout+residual keeps the
+// keep bits packed (one byte per vector, five CTAs per SM); bias+ReLU+dropout
+// is software-pipelined over two register buffers and selects with predicates
+// on the FMA pipes (its Philox work is a large share of its time).
 //
 // Backward layout.  The bias gradient needs column sums, so the backward works
 // on 2-D tiles of 128 rows x 64 columns: lane l of an 8-lane row group owns one

@@ -24,9 +24,11 @@ constexpr int kCtaRowThreshold = 256;  // vectors per row held by one warp at mo
 // ----------------------------------------------------------------------------
 // Forward, group-per-row, persistent.  Row round k gives group slot q of CTA b
 // the row k*stride + q*gridDim + b (stride = all groups), so a partial last
-// round is spread over every CTA.  For rows of up to 2 vectors per lane each
-// group keeps two register buffers: the next row's loads are in flight while
-// the current row is reduced and stored (wider rows keep one buffer).
+// round is spread over every CTA.  Each group keeps two register buffers: the
+// next row's loads are in flight while the current row is reduced and stored,
+// so a group with two rows waits for DRAM once.  At 3 vectors per lane (FP16)
+// and for FP32 rows of 3 or more vectors the second buffer would spill; those
+// keep one buffer (at 768 FP16 columns a 4096-row batch is one row per warp).
 // Loop conditions are warp-uniform (__any_sync) because the groups of one warp
 // reduce with full-warp shuffles.
 // ----------------------------------------------------------------------------
@@ -48,10 +50,23 @@ __device__ __forceinline__ float first_elem(const Raw8<__half>& r) {
 }
 __device__ __forceinline__ float first_elem(const Raw8<float>& r) { return r.a.x; }
 
+// Rows that keep two buffers at 4 or more vectors per lane: the output pass
+// forms d = x - K again from the raw vector instead of keeping d in registers
+// (the same subtract, so the same bits), which keeps the second buffer within
+// the register budget.
+template <typename T, int VPT>
+constexpr bool ln_fwd_double() {
+    return VPT <= 2 || (sizeof(T) == 2 && VPT >= 4);
+}
+template <typename T, int VPT>
+constexpr bool ln_fwd_keep_d() {
+    return VPT <= 3 || !ln_fwd_double<T, VPT>();
+}
+
 // One row of the forward.  The differences d = x - K from the row's first
 // element K are formed once (FP16 converts exactly, folded into the subtract)
-// and kept in registers for both passes; the sums and the output use packed
-// FP32 pairs.  Each result is the FP32 operation on the same operands, rounded
+// and, where the registers allow, kept for both passes; the sums and the
+// output use packed FP32 pairs.  Each result is the FP32 operation on the same operands, rounded
 // once, as in the plain form.  gamma/beta are read per row, after the row's
 // loads: measured on GB300, loading every lane's gamma/beta columns when the
 // kernel starts is slower (4.8 against 4.1 us at 4096 x 768), as every warp
@@ -96,6 +111,7 @@ __device__ __forceinline__ void ln_fwd_row(const Raw8<T> (&xr)[VPT], T* y, float
             float o[kVec], g[kVec], b[kVec];
             load8f<T>(gamma + v * kVec, g);
             load8f<T>(beta + v * kVec, b);
+            if constexpr (!ln_fwd_keep_d<T, VPT>()) sub8(xr[k], K, d[k]);
 #pragma unroll
             for (int j = 0; j < kVec; j += 2) {
                 float2 t = mul2(add2(make_float2(d[k][j], d[k][j + 1]), m2), r2);
@@ -118,35 +134,51 @@ ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, co
                     const T* __restrict__ gamma, const T* __restrict__ beta, int64_t rows,
                     int cols, float eps) {
     constexpr int RPC = kThreads / LPR;
-    pdl_enter();
     const int gl = threadIdx.x % LPR;
     const int slot = threadIdx.x / LPR;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * RPC;
     int64_t r = static_cast<int64_t>(slot) * gridDim.x + blockIdx.x;
-    Raw8<T> xa[VPT], xb[VPT];
+    // Before the wait: the lines of this group's first row (two rows where
+    // the group keeps two buffers) and of gamma/beta, into L2.
+    {
+        const int nvec = cols / kVec;
+#pragma unroll
+        for (int h = 0; h < (ln_fwd_double<T, VPT>() ? 2 : 1); ++h) {
+            const int64_t rr = r + h * stride;
+            if (rr < rows) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) {
+                    const int v = gl + k * LPR;
+                    if (v < nvec) prefetch_l2(x + rr * cols + v * kVec);
+                }
+            }
+        }
+        prefetch_params_l2(gamma, static_cast<size_t>(cols) * sizeof(T));
+        prefetch_params_l2(beta, static_cast<size_t>(cols) * sizeof(T));
+    }
+    pdl_enter();
+    Raw8<T> xa[VPT];
     const T* gs = gamma;
     const T* bs = beta;
     ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
-    prefetch_params_l2(gamma, static_cast<size_t>(cols) * sizeof(T));
-    prefetch_params_l2(beta, static_cast<size_t>(cols) * sizeof(T));
-    if (VPT > 2) {
-        // Wide rows: one buffer (a second would cost occupancy).
+    if constexpr (!ln_fwd_double<T, VPT>()) {
         while (__any_sync(0xffffffffu, r < rows)) {
             ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gs, bs, r, rows, cols, eps, gl);
             r += stride;
             if (!__any_sync(0xffffffffu, r < rows)) break;
             ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
         }
-        return;
-    }
-    while (__any_sync(0xffffffffu, r < rows)) {
-        const int64_t r1 = r + stride;
-        ln_fwd_load<T, LPR, VPT>(xb, x, r1, rows, cols, gl);
-        ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gs, bs, r, rows, cols, eps, gl);
-        if (!__any_sync(0xffffffffu, r1 < rows)) break;
-        r = r1 + stride;
-        ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
-        ln_fwd_row<T, LPR, VPT>(xb, y, mean, rstd, gs, bs, r1, rows, cols, eps, gl);
+    } else {
+        Raw8<T> xb[VPT];
+        while (__any_sync(0xffffffffu, r < rows)) {
+            const int64_t r1 = r + stride;
+            ln_fwd_load<T, LPR, VPT>(xb, x, r1, rows, cols, gl);
+            ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gs, bs, r, rows, cols, eps, gl);
+            if (!__any_sync(0xffffffffu, r1 < rows)) break;
+            r = r1 + stride;
+            ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
+            ln_fwd_row<T, LPR, VPT>(xb, y, mean, rstd, gs, bs, r1, rows, cols, eps, gl);
+        }
     }
 }
 

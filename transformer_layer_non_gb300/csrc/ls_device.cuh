@@ -55,6 +55,17 @@ __device__ __forceinline__ void prefetch_l2(const void* p) {
     asm volatile("prefetch.global.L2 [%0];" ::"l"(p));
 }
 
+// Prefetches issued before griddepcontrol.wait.  Until the wait returns, a
+// kernel must not read memory that the previous grid on the stream may still
+// be writing.  An L2 prefetch reads nothing into the program: it only moves a
+// line into L2, the device's point of coherence, where the previous grid's
+// writes land as well, and the kernel's own loads after the wait see those
+// writes.  So a kernel may prefetch the lines of its first inputs before the
+// wait: while the previous grid drains, their DRAM round trip is under way
+// (measured on GB300: LayerNorm forward at 4096 x 768, 4.08 -> 3.26 us).
+// Addresses must lie inside the input (a prefetch outside an allocation is
+// not an error, but nothing here relies on that).
+
 // Prefetch of a small parameter vector (bias, gamma, beta: `bytes` bytes from
 // p) into L2, one request per 128-byte line, by the first CTA only.  Kernels
 // that read such a vector after their rows' loads issue this at their start,

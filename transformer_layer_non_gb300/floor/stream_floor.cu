@@ -3,9 +3,14 @@
 // src and writes `write_vecs` to dst, one vector per thread, launched the way
 // the operator kernels are (programmatic dependent launch: it waits for its
 // predecessor's completion before its first access and then releases its own
-// successor).  Chained back to back over L2-cold buffers, its time per launch
-// is what a dependent launch moving those bytes costs with no arithmetic at
-// all: the floor each operator's time is compared with.
+// successor).  Like the operator kernels, each thread first prefetches its
+// source line into L2 before the wait (a prefetch is not a read of the
+// predecessor's data: it only moves the line into L2, where the
+// predecessor's writes land too), so the CTAs resident while the predecessor
+// drains have their DRAM round trip under way.  Chained back to back over
+// L2-cold buffers, its time per launch is what a dependent launch moving those
+// bytes costs with no arithmetic at all: the floor each operator's time is
+// compared with.
 #include <cuda_runtime.h>
 #include <stddef.h>
 #include <stdint.h>
@@ -15,9 +20,10 @@ namespace {
 __global__ void __launch_bounds__(256)
 stream_floor_kernel(uint4* __restrict__ dst, const uint4* __restrict__ src, uint64_t read_vecs,
                     uint64_t write_vecs, uint32_t never) {
+    const uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (i < read_vecs) asm volatile("prefetch.global.L2 [%0];" ::"l"(src + i));
     asm volatile("griddepcontrol.wait;" ::: "memory");
     asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
-    const uint64_t i = static_cast<uint64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     uint4 v = make_uint4(0, 0, 0, 0);
     if (i < read_vecs) v = src[i];
     if (i < write_vecs) {

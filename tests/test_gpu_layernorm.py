@@ -102,6 +102,21 @@ def test_many_rows_per_cta_and_ragged_rows():
     check_case(x, g, b, dy, "10007x520")
 
 
+@pytest.mark.parametrize("cols", [1024, 1280, 1536, 1792, 2048])
+def test_wide_rows_two_buffers(cols):
+    # FP16 rows of 4..8 vectors per lane keep two row buffers in the forward
+    # (the second row's loads in flight, x - K formed again in the output
+    # pass); 9001 rows give every warp 2-4 rows, so both buffers are used more
+    # than once, and a ragged last round.
+    require_gpu()
+    shape = (9001, cols)
+    x = synth.normal(3, f"lnd/x{cols}", shape, 0.5, 2.0, "f16")
+    g = synth.normal(3, f"lnd/g{cols}", (cols,), 1.0, 0.1, "f16")
+    b = synth.normal(3, f"lnd/b{cols}", (cols,), 0.0, 0.1, "f16")
+    dy = synth.normal(3, f"lnd/dy{cols}", shape, 0.0, 1.0, "f16")
+    check_case(x, g, b, dy, f"9001x{cols}")
+
+
 def test_large_mean_rows_fp32():
     # Rows with mean 1e4 and unit spread: a naive one-pass variance in FP32
     # loses every digit here; the sums about the first element do not.

@@ -370,6 +370,9 @@ constexpr uint32_t kLnTmaBarBytes = 256;  // 16 warps x 2 stages x 8 bytes
 __host__ __device__ inline size_t ln_tma_gamma_bytes(int cols, size_t esize) {
     return ((static_cast<size_t>(cols) * esize + 127) / 128) * 128;
 }
+// Floats per half-vector array of the end-of-kernel sum: cols/2 plus 16
+// (64 bytes), so that the two halves of a vector map to different banks.
+__host__ __device__ inline int ln_tma_half_stride(int cols) { return cols / 2 + 16; }
 
 template <typename T, int VPT>
 __global__ void __launch_bounds__(kLnTmaWarps * 32, 1)
@@ -392,8 +395,15 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
     // its waiting CTAs do not hold SMs that this grid's CTAs still need.
     pdl_wait();
     const int nvec = cols / kVec;
-    for (int v = threadIdx.x; v < nvec; v += kLnTmaWarps * 32)
-        store8<T>(gsm + v * kVec, load8<T>(gamma + v * kVec));
+    // gamma's loads go out first (its single vector per thread is in flight
+    // while the row copies are issued) and are stored to shared memory after.
+    constexpr int kGammaVecs = (5 * 32 + kLnTmaWarps * 32 - 1) / (kLnTmaWarps * 32);
+    Raw8<T> graw[kGammaVecs];
+#pragma unroll
+    for (int q = 0; q < kGammaVecs; ++q) {
+        const int v = threadIdx.x + q * kLnTmaWarps * 32;
+        if (v < nvec) graw[q] = load8<T>(gamma + v * kVec);
+    }
     const float inv_n = 1.f / static_cast<float>(cols);
     const int64_t base = static_cast<int64_t>(blockIdx.x) * rows_per_cta;
     const int64_t end = std::min<int64_t>(rows, base + rows_per_cta);
@@ -404,14 +414,24 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
         for (int j = 0; j < kVec; ++j) ag[k][j] = ab[k][j] = 0.f;
     uint32_t parity[S] = {0, 0};
     float mu_of[S], rs_of[S];
-#pragma unroll
-    for (int s = 0; s < S; ++s) {
-        const int64_t r = base + warp + s * kLnTmaWarps;
+    // Only the warp's first row is requested now; its second goes out when
+    // the first has landed.  (Measured on GB300 at 4096 x 1280: requesting
+    // both at once makes every CTA's rows land anywhere in the time DRAM needs
+    // for the whole 21 MB, and all reads precede all dx writes; staggered,
+    // the first rows land sooner and the second rows' reads overlap the first
+    // rows' writes: 10.56 -> 9.97 us, 7.43 -> 7.18 at 4096 x 768.)
+    {
+        const int64_t r = base + warp;
         if (r < end) {
-            ring.issue(s, x + r * cols, row_bytes, dy + r * cols, row_bytes, row_bytes);
-            mu_of[s] = mean[r];
-            rs_of[s] = rstd[r];
+            ring.issue(0, x + r * cols, row_bytes, dy + r * cols, row_bytes, row_bytes);
+            mu_of[0] = mean[r];
+            rs_of[0] = rstd[r];
         }
+    }
+#pragma unroll
+    for (int q = 0; q < kGammaVecs; ++q) {
+        const int v = threadIdx.x + q * kLnTmaWarps * 32;
+        if (v < nvec) store8<T>(gsm + v * kVec, graw[q]);
     }
     bool done = false;  // set when the warp's rows are done (or a wait failed)
     __syncthreads();  // gamma staged
@@ -431,6 +451,14 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
             break;
         }
         parity[s] ^= 1u;
+        if (k0 == 0 && s == 0) {
+            const int64_t r1 = base + warp + kLnTmaWarps;
+            if (r1 < end) {
+                ring.issue(1, x + r1 * cols, row_bytes, dy + r1 * cols, row_bytes, row_bytes);
+                mu_of[1] = mean[r1];
+                rs_of[1] = rstd[r1];
+            }
+        }
         const float mu = mu_of[s], rs = rs_of[s];
         const T* xs = reinterpret_cast<const T*>(ring.stage(s));
         const T* ds = reinterpret_cast<const T*>(ring.stage(s) + row_bytes);
@@ -523,28 +551,51 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
     }
     if (partial == nullptr) return;
     // Cross-warp sum of the parameter-gradient partials, in warp order, through
-    // the stage memory (every copy has landed and been read).
+    // the stage memory (every copy has landed and been read).  Each warp's
+    // sums are kept as four arrays of half-vectors -- dgamma elements 0..3 and
+    // 4..7 of every vector, then dbeta's -- so that a warp's 16-byte stores
+    // (lane l: vector l) and the summing threads' 16-byte loads fall on
+    // distinct banks; the padding puts the two halves of a vector on
+    // different banks.  (With whole 8-float vectors the stores were 32 bytes
+    // apart, a two-way conflict on 160 KB at H = 1280.)  The association of
+    // every sum is unchanged: warps 0..15 in order.
     __syncthreads();
-    float* red = reinterpret_cast<float*>(data);  // [8 warps][2*cols]
-    float* mine = red + static_cast<size_t>(warp) * 2 * cols;
+    const int hs = ln_tma_half_stride(cols);  // floats per half-vector array
+    float* red = reinterpret_cast<float*>(data);  // [16 warps][4][hs]
+    float* mine = red + static_cast<size_t>(warp) * 4 * hs;
 #pragma unroll
     for (int k2 = 0; k2 < VPT; ++k2) {
         const int v = lane + k2 * 32;
         if (v < nvec) {
-            float4* pg = reinterpret_cast<float4*>(mine + v * kVec);
-            float4* pb = reinterpret_cast<float4*>(mine + cols + v * kVec);
-            pg[0] = make_float4(ag[k2][0], ag[k2][1], ag[k2][2], ag[k2][3]);
-            pg[1] = make_float4(ag[k2][4], ag[k2][5], ag[k2][6], ag[k2][7]);
-            pb[0] = make_float4(ab[k2][0], ab[k2][1], ab[k2][2], ab[k2][3]);
-            pb[1] = make_float4(ab[k2][4], ab[k2][5], ab[k2][6], ab[k2][7]);
+            *reinterpret_cast<float4*>(mine + 0 * hs + v * 4) =
+                make_float4(ag[k2][0], ag[k2][1], ag[k2][2], ag[k2][3]);
+            *reinterpret_cast<float4*>(mine + 1 * hs + v * 4) =
+                make_float4(ag[k2][4], ag[k2][5], ag[k2][6], ag[k2][7]);
+            *reinterpret_cast<float4*>(mine + 2 * hs + v * 4) =
+                make_float4(ab[k2][0], ab[k2][1], ab[k2][2], ab[k2][3]);
+            *reinterpret_cast<float4*>(mine + 3 * hs + v * 4) =
+                make_float4(ab[k2][4], ab[k2][5], ab[k2][6], ab[k2][7]);
         }
     }
     __syncthreads();
-    for (int c = threadIdx.x; c < 2 * cols; c += kLnTmaWarps * 32) {
-        float t = 0.f;
+    // Group q of four columns: dgamma (q < cols/4) or dbeta, vector v, half h.
+    const int nq = cols / 4;
+    for (int q = threadIdx.x; q < 2 * nq; q += kLnTmaWarps * 32) {
+        const int which = q >= nq ? 1 : 0;
+        const int q2 = q - which * nq;
+        const int v = q2 >> 1, h = q2 & 1;
+        const int off = (which * 2 + h) * hs + v * 4;
+        float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-        for (int w = 0; w < kLnTmaWarps; ++w) t += red[static_cast<size_t>(w) * 2 * cols + c];
-        partial[static_cast<int64_t>(blockIdx.x) * 2 * cols + c] = t;
+        for (int w = 0; w < kLnTmaWarps; ++w) {
+            const float4 p = *reinterpret_cast<const float4*>(red + static_cast<size_t>(w) * 4 * hs + off);
+            t.x += p.x;
+            t.y += p.y;
+            t.z += p.z;
+            t.w += p.w;
+        }
+        *reinterpret_cast<float4*>(partial + static_cast<int64_t>(blockIdx.x) * 2 * cols +
+                                   which * cols + v * kVec + h * 4) = t;
     }
 }
 
@@ -666,8 +717,15 @@ constexpr int64_t kBwdTmaTargetCtas = 152;
 constexpr size_t kLnTmaMaxSmem = 200 * 1024;
 
 size_t ln_tma_smem(int64_t cols, size_t esize) {
+    // The stage memory also holds the end-of-kernel sums (16 warps x 4
+    // half-vector arrays), whichever is larger.
+    const size_t stages =
+        static_cast<size_t>(kLnTmaWarps) * kLnTmaStages * 2 * static_cast<size_t>(cols) * esize;
+    const size_t sums = static_cast<size_t>(kLnTmaWarps) * 4 *
+                        static_cast<size_t>(ln_tma_half_stride(static_cast<int>(cols))) *
+                        sizeof(float);
     return kLnTmaBarBytes + ln_tma_gamma_bytes(static_cast<int>(cols), esize) +
-           static_cast<size_t>(kLnTmaWarps) * kLnTmaStages * 2 * static_cast<size_t>(cols) * esize;
+           (stages > sums ? stages : sums);
 }
 
 // Whether the backward of rows of `cols` elements of `esize` bytes takes the

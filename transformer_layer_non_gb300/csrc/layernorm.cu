@@ -370,9 +370,7 @@ constexpr uint32_t kLnTmaBarBytes = 256;  // 16 warps x 2 stages x 8 bytes
 __host__ __device__ inline size_t ln_tma_gamma_bytes(int cols, size_t esize) {
     return ((static_cast<size_t>(cols) * esize + 127) / 128) * 128;
 }
-// Floats per half-vector array of the end-of-kernel sum: cols/2 plus 16
-// (64 bytes), so that the two halves of a vector map to different banks.
-__host__ __device__ inline int ln_tma_half_stride(int cols) { return cols / 2 + 16; }
+
 
 template <typename T, int VPT>
 __global__ void __launch_bounds__(kLnTmaWarps * 32, 1)
@@ -550,52 +548,55 @@ ln_bwd_tma_kernel(T* dx, float* __restrict__ partial, const T* dy, const T* x,
     }
     }
     if (partial == nullptr) return;
-    // Cross-warp sum of the parameter-gradient partials, in warp order, through
-    // the stage memory (every copy has landed and been read).  Each warp's
-    // sums are kept as four arrays of half-vectors -- dgamma elements 0..3 and
-    // 4..7 of every vector, then dbeta's -- so that a warp's 16-byte stores
-    // (lane l: vector l) and the summing threads' 16-byte loads fall on
-    // distinct banks; the padding puts the two halves of a vector on
-    // different banks.  (With whole 8-float vectors the stores were 32 bytes
-    // apart, a two-way conflict on 160 KB at H = 1280.)  The association of
-    // every sum is unchanged: warps 0..15 in order.
-    __syncthreads();
-    const int hs = ln_tma_half_stride(cols);  // floats per half-vector array
-    float* red = reinterpret_cast<float*>(data);  // [16 warps][4][hs]
-    float* mine = red + static_cast<size_t>(warp) * 4 * hs;
+    // Cross-warp sum of the parameter-gradient partials, in warp order.  Each
+    // warp stores its sums in its own stage memory as soon as its rows are
+    // done (every copy into it has landed and been read), while other warps
+    // still compute: four arrays of half-vectors -- dgamma elements 0..3 and
+    // 4..7 of every vector, then dbeta's -- 8*H bytes, which is the warp's
+    // stage memory at FP16 (twice that at FP32).  A lane's 16-byte stores are
+    // 16 bytes apart, and the summing threads take consecutive vectors of one
+    // array, so neither side has bank conflicts (whole 8-float vectors were
+    // 32 bytes apart: a two-way conflict on 160 KB at H = 1280).  The
+    // association of every sum is unchanged: warps 0..15 in order.
+    const int hc = cols / 2;  // floats per half-vector array
+    const size_t wstride = static_cast<size_t>(S) * stage_bytes / sizeof(float);
+    float* red = reinterpret_cast<float*>(data);  // warp w's arrays at w * wstride
+    __syncwarp();
+    {
+        float* mine = red + static_cast<size_t>(warp) * wstride;
 #pragma unroll
-    for (int k2 = 0; k2 < VPT; ++k2) {
-        const int v = lane + k2 * 32;
-        if (v < nvec) {
-            *reinterpret_cast<float4*>(mine + 0 * hs + v * 4) =
-                make_float4(ag[k2][0], ag[k2][1], ag[k2][2], ag[k2][3]);
-            *reinterpret_cast<float4*>(mine + 1 * hs + v * 4) =
-                make_float4(ag[k2][4], ag[k2][5], ag[k2][6], ag[k2][7]);
-            *reinterpret_cast<float4*>(mine + 2 * hs + v * 4) =
-                make_float4(ab[k2][0], ab[k2][1], ab[k2][2], ab[k2][3]);
-            *reinterpret_cast<float4*>(mine + 3 * hs + v * 4) =
-                make_float4(ab[k2][4], ab[k2][5], ab[k2][6], ab[k2][7]);
+        for (int k2 = 0; k2 < VPT; ++k2) {
+            const int v = lane + k2 * 32;
+            if (v < nvec) {
+                *reinterpret_cast<float4*>(mine + 0 * hc + v * 4) =
+                    make_float4(ag[k2][0], ag[k2][1], ag[k2][2], ag[k2][3]);
+                *reinterpret_cast<float4*>(mine + 1 * hc + v * 4) =
+                    make_float4(ag[k2][4], ag[k2][5], ag[k2][6], ag[k2][7]);
+                *reinterpret_cast<float4*>(mine + 2 * hc + v * 4) =
+                    make_float4(ab[k2][0], ab[k2][1], ab[k2][2], ab[k2][3]);
+                *reinterpret_cast<float4*>(mine + 3 * hc + v * 4) =
+                    make_float4(ab[k2][4], ab[k2][5], ab[k2][6], ab[k2][7]);
+            }
         }
     }
     __syncthreads();
-    // Group q of four columns: dgamma (q < cols/4) or dbeta, vector v, half h.
-    const int nq = cols / 4;
-    for (int q = threadIdx.x; q < 2 * nq; q += kLnTmaWarps * 32) {
-        const int which = q >= nq ? 1 : 0;
-        const int q2 = q - which * nq;
-        const int v = q2 >> 1, h = q2 & 1;
-        const int off = (which * 2 + h) * hs + v * 4;
+    // Thread q sums vector v of array a (a = q / nvec: dgamma low/high
+    // half, dbeta low/high half).
+    for (int q = threadIdx.x; q < 4 * nvec; q += kLnTmaWarps * 32) {
+        const int a = q / nvec;
+        const int v = q - a * nvec;
+        const int off = a * hc + v * 4;
         float4 t = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
         for (int w = 0; w < kLnTmaWarps; ++w) {
-            const float4 p = *reinterpret_cast<const float4*>(red + static_cast<size_t>(w) * 4 * hs + off);
+            const float4 p = *reinterpret_cast<const float4*>(red + static_cast<size_t>(w) * wstride + off);
             t.x += p.x;
             t.y += p.y;
             t.z += p.z;
             t.w += p.w;
         }
         *reinterpret_cast<float4*>(partial + static_cast<int64_t>(blockIdx.x) * 2 * cols +
-                                   which * cols + v * kVec + h * 4) = t;
+                                   (a >> 1) * cols + v * kVec + (a & 1) * 4) = t;
     }
 }
 
@@ -717,15 +718,10 @@ constexpr int64_t kBwdTmaTargetCtas = 152;
 constexpr size_t kLnTmaMaxSmem = 200 * 1024;
 
 size_t ln_tma_smem(int64_t cols, size_t esize) {
-    // The stage memory also holds the end-of-kernel sums (16 warps x 4
-    // half-vector arrays), whichever is larger.
-    const size_t stages =
-        static_cast<size_t>(kLnTmaWarps) * kLnTmaStages * 2 * static_cast<size_t>(cols) * esize;
-    const size_t sums = static_cast<size_t>(kLnTmaWarps) * 4 *
-                        static_cast<size_t>(ln_tma_half_stride(static_cast<int>(cols))) *
-                        sizeof(float);
+    // A warp's stage memory (2 stages of x and dy rows, at least 2-byte
+    // elements) also holds its 2*cols FP32 sums at the end.
     return kLnTmaBarBytes + ln_tma_gamma_bytes(static_cast<int>(cols), esize) +
-           (stages > sums ? stages : sums);
+           static_cast<size_t>(kLnTmaWarps) * kLnTmaStages * 2 * static_cast<size_t>(cols) * esize;
 }
 
 // Whether the backward of rows of `cols` elements of `esize` bytes takes the

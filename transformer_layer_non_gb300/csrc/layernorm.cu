@@ -138,20 +138,14 @@ ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, co
     const int slot = threadIdx.x / LPR;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * RPC;
     int64_t r = static_cast<int64_t>(slot) * gridDim.x + blockIdx.x;
-    // Before the wait: the lines of this group's first row (two rows where
-    // the group keeps two buffers) and of gamma/beta, into L2.
+    // Before the wait: the lines of this group's first row and of
+    // gamma/beta, into L2.
     {
         const int nvec = cols / kVec;
 #pragma unroll
-        for (int h = 0; h < (ln_fwd_double<T, VPT>() ? 2 : 1); ++h) {
-            const int64_t rr = r + h * stride;
-            if (rr < rows) {
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) {
-                    const int v = gl + k * LPR;
-                    if (v < nvec) prefetch_l2(x + rr * cols + v * kVec);
-                }
-            }
+        for (int k = 0; k < VPT; ++k) {
+            const int v = gl + k * LPR;
+            if (r < rows && v < nvec) prefetch_l2(x + r * cols + v * kVec);
         }
         prefetch_params_l2(gamma, static_cast<size_t>(cols) * sizeof(T));
         prefetch_params_l2(beta, static_cast<size_t>(cols) * sizeof(T));
@@ -169,9 +163,19 @@ ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, co
             ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
         }
     } else {
+        // The second row is requested once the first has landed, so that the
+        // first rows of all groups arrive sooner (measured on GB300 at 4096
+        // rows: 7.85 -> 7.54 us at H = 2048, 4.20 -> 4.10 at 1024, no change
+        // at 1280).
         Raw8<T> xb[VPT];
+        bool first = true;
         while (__any_sync(0xffffffffu, r < rows)) {
             const int64_t r1 = r + stride;
+            if (first) {
+#pragma unroll
+                for (int k = 0; k < VPT; ++k) after_arrival(xa[k]);
+                first = false;
+            }
             ln_fwd_load<T, LPR, VPT>(xb, x, r1, rows, cols, gl);
             ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gs, bs, r, rows, cols, eps, gl);
             if (!__any_sync(0xffffffffu, r1 < rows)) break;

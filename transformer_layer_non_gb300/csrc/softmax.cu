@@ -322,12 +322,28 @@ __global__ void __launch_bounds__(kThreads, min_ctas<T>((VPT == 1 || (BWD && VPT
 softmax_group_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, RowMask mk,
                      const __grid_constant__ DropArgs d) {
     constexpr int RPC = kThreads / LPR;
-    pdl_enter();
-    if (DROP && !BWD) drop_tail(d);
     const int gl = threadIdx.x % LPR;
     const int slot = threadIdx.x / LPR;
     const int64_t stride = static_cast<int64_t>(gridDim.x) * RPC;
     int64_t r = static_cast<int64_t>(slot) * gridDim.x + blockIdx.x;
+    // Before the wait, when every row (or pair of rows) has its own key
+    // length: the L2 lines of the key lengths of this group's first two rows
+    // (a row's data loads need its valid length first, so without this the
+    // first row pays two DRAM round trips; measured on GB300 on 2^22 elements
+    // with a key length per row: 2-5% at 32..1024 keys).  With one key length
+    // per batch entry every warp would prefetch the same line -- L2 requests
+    // queue at one slice, where plain loads mostly hit in L1 (BERT-base:
+    // softmax forward 17.1 -> 21.5 us) -- so none is prefetched then.  The
+    // rows themselves are not prefetched: their valid length is not known.
+    if (mk.key_len && mk.heads_q.d <= 2 && gl == 0) {
+#pragma unroll
+        for (int h = 0; h < 2; ++h) {
+            const int64_t rr = r + h * stride;
+            if (rr < nrows) prefetch_l2(mk.key_len + fdiv(static_cast<uint32_t>(rr), mk.heads_q));
+        }
+    }
+    pdl_enter();
+    if (DROP && !BWD) drop_tail(d);
     RowBuf<T, LPR, VPT> ba, bb;
     if (VPT > 2) {
         // Wide rows: one buffer (a second would cost occupancy).
@@ -397,10 +413,16 @@ softmax_tma_kernel(T* out, const T* p, const T* q, int64_t nrows, int k_len, Row
     WarpRing<S> ring;
     ring.init(reinterpret_cast<uint64_t*>(smem) + warp * S,
               smem + tma_bar_bytes() + static_cast<size_t>(warp) * S * stage_bytes, stage_bytes);
-    pdl_enter();
     const int nvec = k_len / kVec;
     const int64_t W = static_cast<int64_t>(gridDim.x) * kTmaWarps;
     const int64_t first = static_cast<int64_t>(blockIdx.x) + static_cast<int64_t>(warp) * gridDim.x;
+    // Before the wait: the L2 lines of the key lengths of the warp's first S
+    // rows, when each row (or pair) has its own (as in softmax_group_kernel).
+    if (mk.key_len && mk.heads_q.d <= 2 && lane < S) {
+        const int64_t rr = first + lane * W;
+        if (rr < nrows) prefetch_l2(mk.key_len + fdiv(static_cast<uint32_t>(rr), mk.heads_q));
+    }
+    pdl_enter();
     uint32_t parity[S];
     int vlen_of[S];
 #pragma unroll

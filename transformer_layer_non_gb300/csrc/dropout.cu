@@ -424,7 +424,9 @@ dropout_bwd_kernel(T* dx, float* __restrict__ partial, const T* dout,
                    const uint8_t* __restrict__ mask, const __grid_constant__ BwdArgs a) {
     __shared__ __align__(16) float red[kBwdRps][kBwdColsPerTile];
     const PhiloxSchedule& ks = a.ks;
-    // Before the wait: the first tile's lines, into L2.
+    // Before the wait: the first tile's lines, into L2.  (Only the first:
+    // prefetching both tiles a CTA loads at once was slower, 16.13 against
+    // 15.88 us at 4096 x 5120, measured on GB300.)
     {
         const int lane = threadIdx.x % kBwdLanes;
         const int64_t tile = blockIdx.x;
@@ -450,20 +452,8 @@ dropout_bwd_kernel(T* dx, float* __restrict__ partial, const T* dout,
     Raw8<T> da[kBwdU], db[kBwdU];
     uint32_t ma[kBwdU], mbb[kBwdU];
     bwd_load<T, REGEN>(da, ma, dout, mask, t, a, ks);
-    // The second tile is requested once the first has landed, so that every
-    // CTA's first tile arrives sooner (measured on GB300 at 4096 x 5120:
-    // 16.13 -> 15.88 us; 10.82 -> 10.73 at 3072).
-    bool first = true;
     while (t < a.ntiles) {
         const int64_t t1 = t + gridDim.x;
-        if (first) {
-#pragma unroll
-            for (int u = 0; u < kBwdU; ++u) {
-                after_arrival(da[u]);
-                asm volatile("" ::"r"(ma[u]) : "memory");
-            }
-            first = false;
-        }
         bwd_load<T, REGEN>(db, mbb, dout, mask, t1, a, ks);
         bwd_compute<T, REGEN>(da, ma, dx, partial, red, t, a);
         if (t1 >= a.ntiles) break;

@@ -139,7 +139,9 @@ ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, co
     const int64_t stride = static_cast<int64_t>(gridDim.x) * RPC;
     int64_t r = static_cast<int64_t>(slot) * gridDim.x + blockIdx.x;
     // Before the wait: the lines of this group's first row and of
-    // gamma/beta, into L2.
+    // gamma/beta, into L2.  (Only the first row: prefetching both rows of a
+    // two-buffer group was slower, 7.85 against 7.54 us at 4096 x 2048 and
+    // 4.20 against 4.10 at 1024, measured on GB300.)
     {
         const int nvec = cols / kVec;
 #pragma unroll
@@ -163,19 +165,9 @@ ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, co
             ln_fwd_load<T, LPR, VPT>(xa, x, r, rows, cols, gl);
         }
     } else {
-        // The second row is requested once the first has landed, so that the
-        // first rows of all groups arrive sooner (measured on GB300 at 4096
-        // rows: 7.85 -> 7.54 us at H = 2048, 4.20 -> 4.10 at 1024, no change
-        // at 1280).
         Raw8<T> xb[VPT];
-        bool first = true;
         while (__any_sync(0xffffffffu, r < rows)) {
             const int64_t r1 = r + stride;
-            if (first) {
-#pragma unroll
-                for (int k = 0; k < VPT; ++k) after_arrival(xa[k]);
-                first = false;
-            }
             ln_fwd_load<T, LPR, VPT>(xb, x, r1, rows, cols, gl);
             ln_fwd_row<T, LPR, VPT>(xa, y, mean, rstd, gs, bs, r, rows, cols, eps, gl);
             if (!__any_sync(0xffffffffu, r1 < rows)) break;

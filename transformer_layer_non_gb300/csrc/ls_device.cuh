@@ -85,18 +85,6 @@ template <typename T> struct Raw8;
 template <> struct Raw8<__half> { uint4 v; };
 template <> struct Raw8<float> { float4 a, b; };
 
-// Orders the caller's later memory operations after the arrival of a loaded
-// vector: an empty asm that reads one of its registers (so the load must
-// have completed) and clobbers memory (so no later load or store is moved
-// above it).  Used to request a kernel's second chunk only once its first
-// has landed.
-__device__ __forceinline__ void after_arrival(const Raw8<__half>& r) {
-    asm volatile("" ::"r"(r.v.x) : "memory");
-}
-__device__ __forceinline__ void after_arrival(const Raw8<float>& r) {
-    asm volatile("" ::"f"(r.a.x) : "memory");
-}
-
 // Plain C++ accesses: the compiler schedules them freely but never moves them
 // across the barrier/wait instructions, whose asm carries a memory clobber.
 __device__ __forceinline__ uint4 ld16(const void* p) { return *reinterpret_cast<const uint4*>(p); }

@@ -1294,6 +1294,11 @@ def run_next_ops(args):
     t["emb_dE"] = torch.zeros(ev, H, dtype=torch.float32, device=dev)
     t["emb_ws"] = torch.empty(ls_ops.embedding_workspace_bytes(T), dtype=torch.uint8, device=dev)
     unique = int(torch.unique(t["tokens"]).numel())
+    # Word-frequency-like ids (Zipf, exponent 1.1: the commonest id on ~9% of
+    # the tokens), the case where one id's rows pile up.
+    zipf = (np.random.default_rng(args.seed).zipf(1.1, T) - 1) % ev
+    t["tokens_zipf"] = torch.from_numpy(zipf.astype(np.int32)).to(dev)
+    unique_z = int(np.unique(zipf).size)
     ws = ls_ops.new_workspace([(T, 3 * H)], device=dev)
     p = L.p
     ls_ops.ls_softmax_dropout_fwd(t["y"], t["y_drop"], t["mask"], t["scores"], t["key_len"],
@@ -1330,6 +1335,15 @@ def run_next_ops(args):
             ls_ops.ls_embedding_bwd(c["emb_dE"], c["emb_dy"], c["emb_mask"], c["tokens"], B, S,
                                     emb_s, p, deterministic=False),
             accounting.embedding_bwd_bytes(T, unique, H, es)),
+        "embedding_bwd_zipf": (["emb_dy", "emb_mask", "tokens_zipf", "emb_dE"], lambda c: lambda:
+            ls_ops.ls_embedding_bwd(c["emb_dE"], c["emb_dy"], c["emb_mask"], c["tokens_zipf"],
+                                    B, S, emb_s, p, workspace=c["emb_ws"]),
+            accounting.embedding_bwd_bytes(T, unique_z, H, es)),
+        "embedding_bwd_atomic_zipf": (["emb_dy", "emb_mask", "tokens_zipf", "emb_dE"],
+            lambda c: lambda: ls_ops.ls_embedding_bwd(c["emb_dE"], c["emb_dy"], c["emb_mask"],
+                                                      c["tokens_zipf"], B, S, emb_s, p,
+                                                      deterministic=False),
+            accounting.embedding_bwd_bytes(T, unique_z, H, es)),
         "cross_entropy_fwd": (["logits", "loss", "lse"], lambda c: lambda:
             ls_ops.ls_cross_entropy_fwd(c["loss"], c["lse"], c["logits"], c["target"], 0.1),
             accounting.cross_entropy_fwd_bytes(T, V, es)),

@@ -297,11 +297,14 @@ size_t ls_embedding_workspace_bytes(int64_t tokens);
  *   d_token_table[w] += scale / (1 - p) * sum over tokens i with id w of bit * dy[i]
  * deterministic == 0: the pages' method, float atomic adds (one pass; the
  * order of the additions, so the last bits, vary from run to run; no
- * workspace).  deterministic != 0: the warp of each id's first token adds
- * that id's rows in token order, the same bits on every run (no workspace; at
- * most 16384 tokens per call, calls on one stream accumulate in order; an id
- * that occurs n times costs its warp n row reads one after another).  The
- * position table gets no gradient (the pages' formula has none). */
+ * workspace).  deterministic != 0: the same bits on every run, each table row
+ * updated once, in an order fixed by the ids: an id on at most three tokens
+ * by the warp of its first token, which adds their rows in token order; an id
+ * on four or more by one CTA, whose 16 warps each add the rows of one of 16
+ * equal position slices (from the id's first token on) in token order, the
+ * slice sums then added in slice order.  No workspace; at most 16384 tokens
+ * per call, calls on one stream accumulate in order.  The position table gets
+ * no gradient (the pages' formula has none). */
 ls_status ls_embedding_bwd(ls_dtype dtype, float* d_token_table, const void* dy,
                            const uint32_t* mask_bits, const int32_t* tokens, int64_t batch,
                            int64_t seq, int64_t hidden, int64_t vocab, float scale, float p,

@@ -4,9 +4,10 @@ Backward (a deterministic scatter-add into an FP32 table gradient): within
 the same bound and within the FP32 summation error bound of each row's terms,
 bit-identical from run to run, and accumulated into what the table gradient
 held.  Cases: the layer shapes with
-BERT/GPT-2 vocabularies, a tiny vocabulary (long runs of repeated ids), one
-id on 30% of the tokens, rows wider than one pass of column vectors, ragged
-token counts and ids outside the table."""
+BERT/GPT-2 vocabularies, uniform and word-frequency-like (Zipf) ids, a tiny
+vocabulary (long runs of repeated ids), one id on 30% of the tokens, ids past
+16 bits, the largest token count per call, rows wider than one pass of column
+vectors, ragged token counts and ids outside the table."""
 import numpy as np
 import pytest
 
@@ -23,7 +24,9 @@ P_DROP, SEED, OFF = 0.1, 99, 4
 def _case(B, L, H, V, dtype, seed=0, bad_ids=False, skew=False):
     rng = np.random.default_rng(seed)
     tok = rng.integers(0, V, B * L).astype(np.int32)
-    if skew:  # a padding-like id on 30% of the tokens: one run of ~0.3*B*L rows
+    if skew == "zipf":  # word-frequency-like ids: a few hundred repeats of the commonest
+        tok = ((rng.zipf(1.1, B * L) - 1) % V).astype(np.int32)
+    elif skew:  # a padding-like id on 30% of the tokens: one run of ~0.3*B*L rows
         tok[rng.random(B * L) < 0.3] = 0
     if bad_ids:
         tok[::13] = -1
@@ -41,6 +44,10 @@ def _case(B, L, H, V, dtype, seed=0, bad_ids=False, skew=False):
     (8, 512, 768, 30522, "f16", False, True),   # BERT-base, one id on 30% of the tokens
     (4, 1024, 1280, 50257, "f16", True, False),  # GPT-2-large, some ids outside the table
     (2, 100, 4104, 300, "f32", False, True),    # H past one pass of column vectors per lane
+    (8, 512, 768, 30522, "f16", False, "zipf"),  # BERT-base, word-frequency-like ids
+    (4, 1024, 1280, 50257, "f16", False, "zipf"),  # GPT-2-large, word-frequency-like ids
+    (3, 250, 136, 70000, "f16", True, "zipf"),  # ids past 16 bits
+    (16, 1024, 64, 1000, "f16", False, False),  # the most tokens one call takes, ~16 per id
 ])
 def test_forward_and_backward(B, L, H, V, dtype, bad, skew):
     require_gpu()

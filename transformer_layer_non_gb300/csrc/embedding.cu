@@ -11,9 +11,9 @@
 // Backward: dE[w] += s / (1 - p) * sum over the tokens i with id w of
 // bit * dy[i].  The pages add the rows with atomicAdd, whose order (and so
 // whose rounding) changes from run to run; that is one mode here (vector
-// float atomics, one pass).  The other mode is deterministic: the warp of the
-// first token with each id adds that id's rows in index order and adds the
-// total into dE[w] -- each row of dE has exactly one writer, so no atomics.
+// float atomics, one pass).  The other mode is deterministic: each row of dE
+// is updated once, by one warp or one CTA, with the id's rows added in an
+// order fixed by the ids alone (emb_det_kernel), so no atomics.
 #include "ls_device.cuh"
 #include "ls_internal.h"
 
@@ -87,110 +87,319 @@ struct EmbBwdArgs {
     float coef;  // s / (1 - p)
 };
 
-constexpr int kOwnerBlk = 3;  // column vectors per lane per pass over the matches
-constexpr int kIdsPerLane = 8;
-constexpr int kIdStep = 32 * kIdsPerLane;  // ids a warp compares per ballot
+// Rows in flight per warp in the shared sum of a frequent id (32 registers).
+template <typename T> constexpr int heavy_batch() { return sizeof(T) == 2 ? 8 : 4; }
 
-// Deterministic backward without a sort: one warp per token j.  The warp
-// returns unless j is the first token with its id w; the owner then walks the
-// tokens from j on, and for every token i with id w, in increasing i, adds
-// bit * dy[i] into FP32 registers, and finally adds coef times the sum into
-// dE[w].  Each row of dE has one writer and a fixed order of additions, so the
-// bits are the same on every run.  The ids (which stay in L1) are compared
-// 256 per step, load q of lane l reading id base + 32q + l (each load a
-// coalesced 128 bytes), so a scan over the batch is a short chain of
-// independent loads; the matches are taken load by load and lane by lane,
-// i.e. in increasing index.  Column vectors go kOwnerBlk per lane per pass
-// (one pass for H <= 768); four CTAs per SM keep a whole 4096-token batch
-// resident in one wave.  The owner asks L2 for its dE row and its own dy row
-// before it scans, so those reads overlap the scan.
-template <typename T>
-__global__ void __launch_bounds__(kThreads, min_ctas<T>(4))
-emb_owner_kernel(float* __restrict__ dE, const T* __restrict__ dy,
-                 const uint8_t* __restrict__ mask, const int32_t* __restrict__ tokens,
-                 const __grid_constant__ EmbBwdArgs a) {
-    pdl_enter();
-    const int j = static_cast<int>((static_cast<int64_t>(blockIdx.x) * kThreads + threadIdx.x) >> 5);
-    const int lane = threadIdx.x & 31;
-    if (j >= a.T) return;  // whole warps
-    const int32_t w = tokens[j];
-    if (w < 0 || static_cast<int64_t>(w) >= a.vocab) return;  // no table row: no gradient
-    // This lane's ids of the step at `base`, restricted to [lo, hi), as a bit
-    // mask of matches with w (ids outside the range are never loaded).
-    auto matches = [&](int base, int lo, int hi) {
-        int32_t t[kIdsPerLane];
-#pragma unroll
-        for (int q = 0; q < kIdsPerLane; ++q) {
-            const int k = base + q * 32 + lane;
-            t[q] = (k >= lo && k < hi) ? tokens[k] : -1;
+// Ids as the deterministic backward keeps them in shared memory: 16 bits when
+// every valid id lies below the 0xFFFF sentinel, else 32.  A lane compares
+// IdScan<ID>::kPerLane consecutive ids (one 16-byte shared load), a warp
+// kStep per step.
+template <typename ID> struct IdScan {
+    static constexpr int kPerLane = 16 / static_cast<int>(sizeof(ID));
+    static constexpr int kStep = 32 * kPerLane;
+    static constexpr uint32_t kNone = sizeof(ID) == 2 ? 0xFFFFu : 0xFFFFFFFFu;
+    // Bit k set iff ids[base + kPerLane*lane + k] == w (w < kNone).
+    static __device__ __forceinline__ uint32_t lane_bits(const ID* ids, int base, int lane,
+                                                         uint32_t w) {
+        const uint4 q = *reinterpret_cast<const uint4*>(ids + base + kPerLane * lane);
+        if constexpr (sizeof(ID) == 2) {
+            const uint32_t wp = w | (w << 16);
+            const uint32_t m0 = __vcmpeq2(q.x, wp), m1 = __vcmpeq2(q.y, wp);
+            const uint32_t m2 = __vcmpeq2(q.z, wp), m3 = __vcmpeq2(q.w, wp);
+            return (m0 & 1u) | ((m0 >> 15) & 2u) | ((m1 & 1u) << 2) | ((m1 >> 13) & 8u) |
+                   ((m2 & 1u) << 4) | ((m2 >> 11) & 32u) | ((m3 & 1u) << 6) | ((m3 >> 9) & 128u);
+        } else {
+            return static_cast<uint32_t>(q.x == w) | (static_cast<uint32_t>(q.y == w) << 1) |
+                   (static_cast<uint32_t>(q.z == w) << 2) | (static_cast<uint32_t>(q.w == w) << 3);
         }
-        uint32_t my = 0;
-#pragma unroll
-        for (int q = 0; q < kIdsPerLane; ++q) my |= static_cast<uint32_t>(t[q] == w) << q;
-        return my;
-    };
-    for (int base = 0; base < j; base += kIdStep)  // an earlier token with id w?
-        if (__ballot_sync(0xffffffffu, matches(base, 0, j) != 0)) return;
-    for (int cv = lane; cv < a.nvr; cv += 32) {
-        prefetch_l2(dE + static_cast<int64_t>(w) * a.H + static_cast<int64_t>(cv) * kVec);
-        prefetch_l2(dy + static_cast<int64_t>(j) * a.H + static_cast<int64_t>(cv) * kVec);
     }
-    const int first = j - j % kIdStep;
-    int end = a.T;  // after the first pass: one past the id's last token
-    for (int cb = 0; cb < a.nvr; cb += 32 * kOwnerBlk) {
-        float acc[kOwnerBlk][kVec];
+    static __device__ __forceinline__ uint32_t of(int32_t t, int64_t vocab) {
+        return t >= 0 && static_cast<int64_t>(t) < vocab ? static_cast<uint32_t>(t) : kNone;
+    }
+};
+
+// Bits k of a lane's run of n ids starting at position p0 whose position lies
+// in [lo, hi).
+__device__ __forceinline__ uint32_t range_bits(int p0, int n, int lo, int hi) {
+    const int a = min(max(lo - p0, 0), n), b = min(max(hi - p0, 0), n);
+    return ((1u << b) - 1u) & ~((1u << a) - 1u);
+}
+
+// Warps (tokens) per CTA of the deterministic backward, and the CTAs per SM
+// its registers are sized for: two at 64 registers for FP16 rows (32 warps
+// per SM, so a 4096-token batch is one wave), one at 128 for FP32 rows.
+constexpr int kDetWarps = 16;
+template <typename T> constexpr int det_min_ctas() { return sizeof(T) == 4 ? 1 : 2; }
+
+// Ids on at least this many tokens are summed by a whole CTA.
+constexpr int kFrequent = 4;
+
+// Deterministic backward: dE[w] += coef * sum over the tokens i with id w of
+// bit * dy[i], each row of dE written by one warp or CTA, in an order fixed
+// by the ids alone, so the bits are the same on every run (no atomics).
+//
+// One warp per token, W tokens per CTA; each warp's gradient row and mask
+// bytes are asked of L2 before the dependency wait.  Each CTA copies all T
+// ids into shared memory (padded with a sentinel to whole scan steps) and
+// passes over them once, counting for each of its tokens j with id w the
+// tokens with id w before j (r) and after it, so n = all of them:
+//   - n <= 3: the first of them (r = 0) adds its own row and the later ones,
+//     in token order: dE[w] += coef * (((0 + bit*dy[j]) + bit*dy[i1]) + ...);
+//   - n >= 4 ("frequent"): the token whose rank r equals a hash of w modulo n
+//     hands the id to its CTA.  After the light sums, the CTA takes its
+//     frequent ids one by one: the row's 32-vector column blocks up to W at a
+//     time, the positions [f, T) (f: the id's first token) cut into
+//     NS = W / (blocks taken) equal slices; warp (b, s) sums, in increasing
+//     index, the rows of slice s with id w, column block b (heavy_batch rows
+//     in flight), into S_s, and dE[w] += coef * (((0 + S_0) + S_1) + ...
+//     + S_{NS-1}) through shared memory.
+// The tokens of an id are spread over the batch, so the hash spreads the
+// frequent ids over the CTAs (their first tokens all lie early in the batch).
+// Light sums take NB column vectors per lane per pass.
+template <typename T, typename ID, int NB>
+__global__ void __launch_bounds__(32 * kDetWarps, det_min_ctas<T>())
+emb_det_kernel(float* __restrict__ dE, const T* __restrict__ dy,
+               const uint8_t* __restrict__ mask, const int32_t* __restrict__ tokens,
+               const __grid_constant__ EmbBwdArgs a) {
+    using S = IdScan<ID>;
+    constexpr int W = kDetWarps;
+    constexpr int P = S::kPerLane;
+    constexpr int STEP = S::kStep;
+    constexpr int B = heavy_batch<T>();
+    extern __shared__ __align__(16) unsigned char det_smem[];
+    ID* ids = reinterpret_cast<ID*>(det_smem);  // [Tp]
+    __shared__ int s_first[W];  // first token of the frequent id warp t hands over, or -1
+    __shared__ uint32_t s_tab[256];  // bit t: token t's id has these low 8 bits
+    __shared__ uint32_t s_wid[W];
+    __shared__ int s_rank[W], s_low[W], s_nlater[W], s_next[W][2];
+    __shared__ __align__(16) float s_part[W][32][kVec];
+    __shared__ uint16_t s_list[W][STEP];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ntok = a.T, nvr = a.nvr;
+    const int Tp = (ntok + STEP - 1) / STEP * STEP;
+    const int j = blockIdx.x * W + warp;
+    const bool have = j < ntok;
+    const int64_t rowv = static_cast<int64_t>(j) * nvr;  // first vector of row j
+
+    // Before the dependency wait: this warp's gradient row and mask bytes, and
+    // one line of the ids per CTA (the CTAs together cover them), into L2.
+    if (have) {
+        const char* row = reinterpret_cast<const char*>(dy + rowv * kVec);
+        const int bytes = nvr * kVec * static_cast<int>(sizeof(T));
+        for (int c = lane * 128; c < bytes; c += 32 * 128) prefetch_l2(row + c);
+        if (lane == 31) prefetch_l2(row + bytes - 1);
+        if (lane == 0) prefetch_l2(mask + rowv);
+        if (lane == 1) prefetch_l2(mask + rowv + nvr - 1);
+    }
+    if (threadIdx.x == 0) {
+        const int lines = (ntok + 31) / 32;
+        prefetch_l2(tokens + static_cast<int64_t>(blockIdx.x % lines) * 32);
+    }
+    pdl_enter();
+
+    for (int k = threadIdx.x; k < 256; k += 32 * W) s_tab[k] = 0u;
+    if (threadIdx.x < W) {
+        s_rank[threadIdx.x] = s_nlater[threadIdx.x] = 0;
+        s_low[threadIdx.x] = ntok;
+        s_next[threadIdx.x][0] = s_next[threadIdx.x][1] = 0;
+    }
+    // All ids into shared memory, four per 16-byte load where aligned.
+    int k0 = 0;
+    if ((reinterpret_cast<uintptr_t>(tokens) & 15u) == 0) {
+        const int n4 = ntok >> 2;
+        const int4* t4 = reinterpret_cast<const int4*>(tokens);
+#pragma unroll 2
+        for (int k = threadIdx.x; k < n4; k += 32 * W) {
+            const int4 t = t4[k];
+            const uint32_t x = S::of(t.x, a.vocab), y = S::of(t.y, a.vocab);
+            const uint32_t z = S::of(t.z, a.vocab), u = S::of(t.w, a.vocab);
+            if constexpr (sizeof(ID) == 2)
+                *reinterpret_cast<uint2*>(ids + 4 * k) = make_uint2(x | (y << 16), z | (u << 16));
+            else
+                *reinterpret_cast<uint4*>(ids + 4 * k) = make_uint4(x, y, z, u);
+        }
+        k0 = 4 * n4;
+    }
+#pragma unroll 4
+    for (int k = k0 + threadIdx.x; k < Tp; k += 32 * W)
+        ids[k] = static_cast<ID>(k < ntok ? S::of(tokens[k], a.vocab) : S::kNone);
+    __syncthreads();
+
+    const uint32_t w = have ? static_cast<uint32_t>(ids[j]) : S::kNone;
+    const bool valid = w != S::kNone;
+    if (valid) {  // the dE row into L2 (harmless if this token is not the one to update it)
+        const float* row = dE + static_cast<int64_t>(w) * a.H;
+        for (int c = lane * 32; c < nvr * kVec; c += 32 * 32) prefetch_l2(row + c);
+        if (lane == 31) prefetch_l2(row + nvr * kVec - 1);
+    }
+    // One pass of the CTA over all ids finds the tokens with the CTA's W ids:
+    // s_tab[x & 255] has bit t set if token t's id has those low bits, so an
+    // id is compared in full only on a hit.  For token t it counts the earlier
+    // tokens with its id (s_rank) and the first of them (s_low), and the later
+    // ones (s_nlater), keeping the first two it meets (s_next; their order is
+    // restored below).
+    if (lane == 0) {
+        s_wid[warp] = w;
+        if (valid) atomicOr(&s_tab[w & 255u], 1u << warp);
+    }
+    __syncthreads();
+    for (int k = P * threadIdx.x; k < Tp; k += P * 32 * W) {
+        const uint4 q = *reinterpret_cast<const uint4*>(ids + k);
+        uint32_t x[P];
+        if constexpr (sizeof(ID) == 2) {
+            x[0] = q.x & 0xFFFFu; x[1] = q.x >> 16; x[2] = q.y & 0xFFFFu; x[3] = q.y >> 16;
+            x[4] = q.z & 0xFFFFu; x[5] = q.z >> 16; x[6] = q.w & 0xFFFFu; x[7] = q.w >> 16;
+        } else {
+            x[0] = q.x; x[1] = q.y; x[2] = q.z; x[3] = q.w;
+        }
 #pragma unroll
-        for (int b = 0; b < kOwnerBlk; ++b)
-#pragma unroll
-            for (int q = 0; q < kVec; ++q) acc[b][q] = 0.f;
-        int last = j;
-        for (int base = first; base < end; base += kIdStep) {
-            const uint32_t my = matches(base, j, end);
-            if (!__ballot_sync(0xffffffffu, my != 0)) continue;
-#pragma unroll 1
-            for (int ld = 0; ld < kIdsPerLane; ++ld) {  // warp-uniform: loads, then lanes, in order
-                uint32_t lanes = __ballot_sync(0xffffffffu, (my >> ld) & 1u);
-                while (lanes) {
-                    const int64_t i = base + ld * 32 + __ffs(lanes) - 1;
-                    lanes &= lanes - 1;
-                    last = static_cast<int>(i);
-                    Raw8<T> g[kOwnerBlk];
-                    uint32_t bits[kOwnerBlk];
-#pragma unroll
-                    for (int b = 0; b < kOwnerBlk; ++b) {
-                        const int cv = cb + b * 32 + lane;
-                        bits[b] = 0u;
-                        if (cv < a.nvr) {
-                            const int64_t e = i * a.H + static_cast<int64_t>(cv) * kVec;
-                            g[b] = load8<T>(dy + e);
-                            bits[b] = mask[e >> 3];
-                        }
-                    }
-#pragma unroll
-                    for (int b = 0; b < kOwnerBlk; ++b) {
-                        if (cb + b * 32 + lane >= a.nvr) continue;
-                        float f[kVec];
-                        unpack(g[b], f);
-#pragma unroll
-                        for (int q = 0; q < kVec; ++q)
-                            if ((bits[b] >> q) & 1u) acc[b][q] += f[q];
-                    }
+        for (int i = 0; i < P; ++i) {
+            if (x[i] == S::kNone) continue;
+            for (uint32_t m = s_tab[x[i] & 255u]; m; m &= m - 1) {
+                const int t = __ffs(m) - 1;
+                if (s_wid[t] != x[i]) continue;
+                const int pos = k + i, jt = blockIdx.x * W + t;
+                if (pos < jt) {
+                    atomicAdd(&s_rank[t], 1);
+                    atomicMin(&s_low[t], pos);
+                } else if (pos > jt) {
+                    const int slot = atomicAdd(&s_nlater[t], 1);
+                    if (slot < 2) s_next[t][slot] = pos;
                 }
             }
         }
-        end = last + 1;  // later passes stop at the id's last token
+    }
+    __syncthreads();
+    const int r = s_rank[warp], later = s_nlater[warp];
+    const int first = r > 0 ? s_low[warp] : j;
+    int p1 = s_next[warp][0], p2 = s_next[warp][1];
+    if (later >= 2 && p2 < p1) { const int tmp = p1; p1 = p2; p2 = tmp; }
+    const int n = r + 1 + later;
+    const bool frequent = valid && n >= kFrequent;
+    if (lane == 0)
+        s_first[warp] = frequent && r == static_cast<int>(__umulhi(w * 2654435761u, n)) ? first : -1;
+
+    if (valid && !frequent && r == 0) {
+        const int64_t row1 = static_cast<int64_t>(p1) * nvr, row2 = static_cast<int64_t>(p2) * nvr;
+        for (int cb = 0; cb < nvr; cb += 32 * NB) {
+            Raw8<T> g0[NB];  // the own row's block (in L2 since before the dependency wait)
+            uint32_t b0[NB];
 #pragma unroll
-        for (int b = 0; b < kOwnerBlk; ++b) {
-            const int cv = cb + b * 32 + lane;
-            if (cv >= a.nvr) continue;
-            float* dst = dE + static_cast<int64_t>(w) * a.H + static_cast<int64_t>(cv) * kVec;
-            float4 d0 = *reinterpret_cast<float4*>(dst), d1 = *reinterpret_cast<float4*>(dst + 4);
-            d0.x = fmaf(a.coef, acc[b][0], d0.x); d0.y = fmaf(a.coef, acc[b][1], d0.y);
-            d0.z = fmaf(a.coef, acc[b][2], d0.z); d0.w = fmaf(a.coef, acc[b][3], d0.w);
-            d1.x = fmaf(a.coef, acc[b][4], d1.x); d1.y = fmaf(a.coef, acc[b][5], d1.y);
-            d1.z = fmaf(a.coef, acc[b][6], d1.z); d1.w = fmaf(a.coef, acc[b][7], d1.w);
-            *reinterpret_cast<float4*>(dst) = d0;
-            *reinterpret_cast<float4*>(dst + 4) = d1;
+            for (int b = 0; b < NB; ++b) {
+                const int cv = cb + b * 32 + lane;
+                b0[b] = 0u;
+                if (cv < nvr) {
+                    g0[b] = load8<T>(dy + (rowv + cv) * kVec);
+                    b0[b] = mask[rowv + cv];
+                }
+            }
+#pragma unroll
+            for (int b = 0; b < NB; ++b) {
+                const int cv = cb + b * 32 + lane;
+                if (cv >= nvr) continue;
+                float acc[kVec], f[kVec];
+                unpack(g0[b], f);
+#pragma unroll
+                for (int q = 0; q < kVec; ++q) {
+                    acc[q] = 0.f;
+                    if ((b0[b] >> q) & 1u) acc[q] += f[q];
+                }
+                for (int m = 0; m < later; ++m) {  // at most 2, in token order
+                    const int64_t iv = (m == 0 ? row1 : row2) + cv;
+                    unpack(load8<T>(dy + iv * kVec), f);
+                    const uint32_t bits = mask[iv];
+#pragma unroll
+                    for (int q = 0; q < kVec; ++q)
+                        if ((bits >> q) & 1u) acc[q] += f[q];
+                }
+                float* dst = dE + static_cast<int64_t>(w) * a.H + static_cast<int64_t>(cv) * kVec;
+                float4 d0 = *reinterpret_cast<const float4*>(dst);
+                float4 d1 = *reinterpret_cast<const float4*>(dst + 4);
+                d0.x = fmaf(a.coef, acc[0], d0.x); d0.y = fmaf(a.coef, acc[1], d0.y);
+                d0.z = fmaf(a.coef, acc[2], d0.z); d0.w = fmaf(a.coef, acc[3], d0.w);
+                d1.x = fmaf(a.coef, acc[4], d1.x); d1.y = fmaf(a.coef, acc[5], d1.y);
+                d1.z = fmaf(a.coef, acc[6], d1.z); d1.w = fmaf(a.coef, acc[7], d1.w);
+                *reinterpret_cast<float4*>(dst) = d0;
+                *reinterpret_cast<float4*>(dst + 4) = d1;
+            }
+        }
+    }
+
+    // The frequent ids handed to this CTA, one after another, by all its warps.
+    __syncthreads();
+    const int ncb = (nvr + 31) / 32;  // 32-vector column blocks of a row
+    for (int t = 0; t < W; ++t) {
+        const int f = s_first[t];  // the same in every thread of the CTA
+        if (f < 0) continue;
+        const uint32_t wt = ids[blockIdx.x * W + t];
+        for (int cb0 = 0; cb0 < ncb; cb0 += W) {
+            const int nb = min(ncb - cb0, W);  // column blocks this round
+            const int ns = W / nb;             // slices per block
+            const int bi = warp / ns, si = warp % ns;
+            const bool active = bi < nb;
+            const int cv = (cb0 + bi) * 32 + lane;
+            const int per = (ntok - f + ns - 1) / ns;
+            const int lo = min(ntok, f + si * per), hi = active ? min(ntok, lo + per) : lo;
+            float acc[kVec];
+#pragma unroll
+            for (int q = 0; q < kVec; ++q) acc[q] = 0.f;
+            for (int base = lo - lo % STEP; base < hi; base += STEP) {
+                // This step's matches, in increasing position, listed in s_list.
+                const uint32_t m =
+                    S::lane_bits(ids, base, lane, wt) & range_bits(base + P * lane, P, lo, hi);
+                const uint32_t c = __popc(m);
+                uint32_t incl = c;
+#pragma unroll
+                for (int d = 1; d < 32; d <<= 1) {
+                    const uint32_t o = __shfl_up_sync(0xffffffffu, incl, d);
+                    if (lane >= d) incl += o;
+                }
+                const int total = static_cast<int>(__shfl_sync(0xffffffffu, incl, 31));
+                int slot = static_cast<int>(incl - c);
+                for (uint32_t rb = m; rb; rb &= rb - 1)
+                    s_list[warp][slot++] = static_cast<uint16_t>(P * lane + __ffs(rb) - 1);
+                __syncwarp();
+                for (int q0 = 0; q0 < total; q0 += B) {
+                    Raw8<T> g[B];
+                    uint32_t bits[B];
+#pragma unroll
+                    for (int u = 0; u < B; ++u) {
+                        bits[u] = 0u;
+                        if (q0 + u < total && cv < nvr) {
+                            const int64_t iv =
+                                static_cast<int64_t>(base + s_list[warp][q0 + u]) * nvr + cv;
+                            g[u] = load8<T>(dy + iv * kVec);
+                            bits[u] = mask[iv];
+                        }
+                    }
+#pragma unroll
+                    for (int u = 0; u < B; ++u) {
+                        if (q0 + u >= total || cv >= nvr) continue;
+                        float fv[kVec];
+                        unpack(g[u], fv);
+#pragma unroll
+                        for (int q = 0; q < kVec; ++q)
+                            if ((bits[u] >> q) & 1u) acc[q] += fv[q];
+                    }
+                }
+                __syncwarp();
+            }
+            float4* pp = reinterpret_cast<float4*>(s_part[warp][lane]);
+            pp[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
+            pp[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
+            __syncthreads();
+            for (int q = threadIdx.x; q < nb * 32 * kVec; q += 32 * W) {
+                const int b = q / (32 * kVec), v = (q / kVec) % 32, e = q % kVec;
+                const int vv = (cb0 + b) * 32 + v;
+                if (vv < nvr) {
+                    float sum = 0.f;
+                    for (int s2 = 0; s2 < ns; ++s2) sum += s_part[b * ns + s2][v][e];
+                    float* d = dE + static_cast<int64_t>(wt) * a.H + static_cast<int64_t>(vv) * kVec + e;
+                    *d = fmaf(a.coef, sum, *d);
+                }
+            }
+            __syncthreads();
         }
     }
 }
@@ -301,6 +510,36 @@ cudaError_t launch_embedding_bwd_atomic(DType dt, float* dE, const void* dy, con
     return atomic_impl<float>(dE, dy, mask, tokens, T, H, vocab, coef, st);
 }
 
+namespace {
+
+template <typename T, typename ID, int NB>
+cudaError_t det_launch(float* dE, const void* dy, const uint8_t* mask, const int32_t* tokens,
+                       const EmbBwdArgs& a, cudaStream_t st) {
+    static int done[kMaxDevices] = {};
+    auto kern = emb_det_kernel<T, ID, NB>;
+    constexpr int step = IdScan<ID>::kStep, W = kDetWarps;
+    const size_t smem = static_cast<size_t>((a.T + step - 1) / step * step) * sizeof(ID);
+    if (smem > 16 * 1024) {
+        const cudaError_t e = allow_max_dynamic_smem(kern, done);
+        if (e != cudaSuccess) return e;
+    }
+    const dim3 grid(static_cast<unsigned>((a.T + W - 1) / W));
+    return launch_pdl(kern, grid, dim3(32 * W), smem, st, dE, static_cast<const T*>(dy), mask,
+                      tokens, a);
+}
+
+template <typename T, typename ID>
+cudaError_t det_dispatch(float* dE, const void* dy, const uint8_t* mask, const int32_t* tokens,
+                         const EmbBwdArgs& a, cudaStream_t st) {
+    // Column vectors per lane per pass of a light sum: one pass up to 160
+    // vectors (1280 columns), four per pass beyond.
+    if (a.nvr <= 96) return det_launch<T, ID, 3>(dE, dy, mask, tokens, a, st);
+    if (a.nvr > 128 && a.nvr <= 160) return det_launch<T, ID, 5>(dE, dy, mask, tokens, a, st);
+    return det_launch<T, ID, 4>(dE, dy, mask, tokens, a, st);
+}
+
+}  // namespace
+
 cudaError_t launch_embedding_bwd(DType dt, float* dE, const void* dy, const uint8_t* mask,
                                  const int32_t* tokens, int64_t T, int64_t H, int64_t vocab,
                                  float coef, cudaStream_t st) {
@@ -310,12 +549,12 @@ cudaError_t launch_embedding_bwd(DType dt, float* dE, const void* dy, const uint
     a.H = H;
     a.vocab = vocab;
     a.coef = coef;
-    const dim3 grid(static_cast<unsigned>((T * 32 + kThreads - 1) / kThreads));
+    const bool narrow = vocab <= 0xFFFF;  // every valid id below the 16-bit sentinel
     if (dt == DType::F16)
-        return launch_pdl(emb_owner_kernel<__half>, grid, dim3(kThreads), 0, st, dE,
-                          static_cast<const __half*>(dy), mask, tokens, a);
-    return launch_pdl(emb_owner_kernel<float>, grid, dim3(kThreads), 0, st, dE,
-                      static_cast<const float*>(dy), mask, tokens, a);
+        return narrow ? det_dispatch<__half, uint16_t>(dE, dy, mask, tokens, a, st)
+                      : det_dispatch<__half, uint32_t>(dE, dy, mask, tokens, a, st);
+    return narrow ? det_dispatch<float, uint16_t>(dE, dy, mask, tokens, a, st)
+                  : det_dispatch<float, uint32_t>(dE, dy, mask, tokens, a, st);
 }
 
 }  // namespace ls

@@ -84,9 +84,10 @@ cudaError_t launch_qkv_bwd(DType dt, void* dqkv, float* partial, const void* dou
                            int64_t seq, int64_t heads, int64_t d, cudaStream_t s);
 
 // Embedding layer: gather + dropout forward; deterministic scatter-add
-// backward into an FP32 dE (the warp of each id's first token adds the id's
-// rows in index order; each warp scans the earlier ids, so the work grows with
-// the square of the tokens: at most kEmbeddingMaxTokens per call).
+// backward into an FP32 dE (each id's sum in an order fixed by the ids; every
+// CTA of 16 tokens stages and scans all the ids, so the work grows with the
+// square of the tokens and the ids must fit in shared memory: at most
+// kEmbeddingMaxTokens per call).
 constexpr int64_t kEmbeddingMaxTokens = 16384;
 cudaError_t launch_embedding_fwd(DType dt, void* y, uint8_t* mask, const int32_t* tokens,
                                  const void* E, const void* P, int64_t batch, int64_t seq,

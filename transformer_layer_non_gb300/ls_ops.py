@@ -372,8 +372,8 @@ def embedding_workspace_bytes(tokens: int) -> int:
 def ls_embedding_bwd(d_token_table, dy, mask_bits, tokens, batch: int, seq: int, scale: float,
                      p: float, deterministic: bool = True, workspace=None, stream=None):
     """Adds the token-table gradient (FP32 [vocab, H]) of this batch into
-    d_token_table: deterministically (each id's rows in token order by one
-    warp) or with float atomics.  No workspace is needed."""
+    d_token_table: deterministically (each id's sum in an order fixed by the
+    ids) or with float atomics.  No workspace is needed."""
     vocab, hidden = d_token_table.shape
     _check(load().ls_embedding_bwd(_dtype_code(dy), _ptr(d_token_table), _ptr(dy),
                                    _ptr(mask_bits), _ptr(tokens), batch, seq, hidden, vocab,

@@ -6,8 +6,9 @@ bit-identical from run to run, and accumulated into what the table gradient
 held.  Cases: the layer shapes with
 BERT/GPT-2 vocabularies, uniform and word-frequency-like (Zipf) ids, a tiny
 vocabulary (long runs of repeated ids), one id on 30% of the tokens, ids past
-16 bits, the largest token count per call, rows wider than one pass of column
-vectors, ragged token counts and ids outside the table."""
+16 bits (FP16 and FP32 rows), the largest token count per call (ids spread,
+and all on one id), a single token, no id in the table, rows wider than one
+pass of column vectors, ragged token counts and ids outside the table."""
 import numpy as np
 import pytest
 
@@ -26,6 +27,10 @@ def _case(B, L, H, V, dtype, seed=0, bad_ids=False, skew=False):
     tok = rng.integers(0, V, B * L).astype(np.int32)
     if skew == "zipf":  # word-frequency-like ids: a few hundred repeats of the commonest
         tok = ((rng.zipf(1.1, B * L) - 1) % V).astype(np.int32)
+    elif skew == "one":  # every token on one id
+        tok[:] = V - 1
+    elif skew == "none":  # every id outside the table
+        tok[:] = np.where(rng.random(B * L) < 0.5, -1 - tok, V + tok)
     elif skew:  # a padding-like id on 30% of the tokens: one run of ~0.3*B*L rows
         tok[rng.random(B * L) < 0.3] = 0
     if bad_ids:
@@ -48,6 +53,10 @@ def _case(B, L, H, V, dtype, seed=0, bad_ids=False, skew=False):
     (4, 1024, 1280, 50257, "f16", False, "zipf"),  # GPT-2-large, word-frequency-like ids
     (3, 250, 136, 70000, "f16", True, "zipf"),  # ids past 16 bits
     (16, 1024, 64, 1000, "f16", False, False),  # the most tokens one call takes, ~16 per id
+    (1, 16384, 16, 3, "f16", False, "one"),     # the most tokens, all on one id
+    (1, 1, 8, 3, "f16", False, False),          # one token, one column vector
+    (3, 5, 40, 20, "f16", False, "none"),       # no id in the table: no gradient
+    (2, 300, 72, 90000, "f32", True, "zipf"),   # FP32 rows, ids past 16 bits
 ])
 def test_forward_and_backward(B, L, H, V, dtype, bad, skew):
     require_gpu()

@@ -300,9 +300,10 @@ size_t ls_embedding_workspace_bytes(int64_t tokens);
  * workspace).  deterministic != 0: the same bits on every run, each table row
  * updated once, in an order fixed by the ids: an id on at most three tokens
  * by the warp of its first token, which adds their rows in token order; an id
- * on four or more by one CTA, whose 16 warps each add the rows of one of 16
- * equal position slices (from the id's first token on) in token order, the
- * slice sums then added in slice order.  No workspace; at most 16384 tokens
+ * on four or more one 256-column block at a time, each block by one CTA,
+ * whose 16 warps each add the block's rows of one of 16 equal position
+ * slices (from the id's first token on) in token order, the slice sums then
+ * added in slice order.  No workspace; at most 16384 tokens
  * per call, calls on one stream accumulate in order.  The position table gets
  * no gradient (the pages' formula has none). */
 ls_status ls_embedding_bwd(ls_dtype dtype, float* d_token_table, const void* dy,

@@ -145,16 +145,17 @@ constexpr int kFrequent = 4;
 // tokens with id w before j (r) and after it, so n = all of them:
 //   - n <= 3: the first of them (r = 0) adds its own row and the later ones,
 //     in token order: dE[w] += coef * (((0 + bit*dy[j]) + bit*dy[i1]) + ...);
-//   - n >= 4 ("frequent"): the token whose rank r equals a hash of w modulo n
-//     hands the id to its CTA.  After the light sums, the CTA takes its
-//     frequent ids one by one: the row's 32-vector column blocks up to W at a
-//     time, the positions [f, T) (f: the id's first token) cut into
-//     NS = W / (blocks taken) equal slices; warp (b, s) sums, in increasing
-//     index, the rows of slice s with id w, column block b (heavy_batch rows
-//     in flight), into S_s, and dE[w] += coef * (((0 + S_0) + S_1) + ...
-//     + S_{NS-1}) through shared memory.
+//   - n >= 4 ("frequent"): each 32-vector column block b of the row is an
+//     independent sum, handed to the CTA of the id's token of rank
+//     (h + b) mod n, h a hash of w.  After the light sums, the CTA takes its
+//     blocks one by one: the positions [f, T) (f: the id's first token) cut
+//     into W equal slices, warp s sums, in increasing index, the rows of
+//     slice s with id w (heavy_batch rows in flight) into S_s, and
+//     dE[w][block] += coef * (((0 + S_0) + S_1) + ... + S_{W-1}) through
+//     shared memory.
 // The tokens of an id are spread over the batch, so the hash spreads the
-// frequent ids over the CTAs (their first tokens all lie early in the batch).
+// frequent ids' blocks over the CTAs (their first tokens all lie early in the
+// batch), and an id's blocks over as many CTAs as it has blocks.
 // Light sums take NB column vectors per lane per pass.
 template <typename T, typename ID, int NB>
 __global__ void __launch_bounds__(32 * kDetWarps, det_min_ctas<T>())
@@ -169,9 +170,12 @@ emb_det_kernel(float* __restrict__ dE, const T* __restrict__ dy,
     extern __shared__ __align__(16) unsigned char det_smem[];
     ID* ids = reinterpret_cast<ID*>(det_smem);  // [Tp]
     __shared__ int s_first[W];  // first token of the frequent id warp t hands over, or -1
+    __shared__ int s_blk[W], s_cnt[W];  // its first column block and its token count
     __shared__ uint32_t s_tab[256];  // bit t: token t's id has these low 8 bits
     __shared__ uint32_t s_wid[W];
-    __shared__ int s_rank[W], s_low[W], s_nlater[W], s_next[W][2];
+    // Per counting warp c and token t: earlier / later tokens with t's id, the
+    // first earlier one, and the first two later ones it met.
+    __shared__ int s_rank[W][W], s_low[W][W], s_nlater[W][W], s_next[W][W][2];
     __shared__ __align__(16) float s_part[W][32][kVec];
     __shared__ uint16_t s_list[W][STEP];
 
@@ -199,10 +203,9 @@ emb_det_kernel(float* __restrict__ dE, const T* __restrict__ dy,
     pdl_enter();
 
     for (int k = threadIdx.x; k < 256; k += 32 * W) s_tab[k] = 0u;
-    if (threadIdx.x < W) {
-        s_rank[threadIdx.x] = s_nlater[threadIdx.x] = 0;
-        s_low[threadIdx.x] = ntok;
-        s_next[threadIdx.x][0] = s_next[threadIdx.x][1] = 0;
+    if (lane < W) {
+        s_rank[warp][lane] = s_nlater[warp][lane] = 0;
+        s_low[warp][lane] = ntok;
     }
     // All ids into shared memory, four per 16-byte load where aligned.
     int k0 = 0;
@@ -237,8 +240,10 @@ emb_det_kernel(float* __restrict__ dE, const T* __restrict__ dy,
     // s_tab[x & 255] has bit t set if token t's id has those low bits, so an
     // id is compared in full only on a hit.  For token t it counts the earlier
     // tokens with its id (s_rank) and the first of them (s_low), and the later
-    // ones (s_nlater), keeping the first two it meets (s_next; their order is
-    // restored below).
+    // ones (s_nlater), keeping the first two it meets (s_next).  Each warp
+    // counts into its own row of these arrays -- a frequent id's hundreds of
+    // matches would otherwise queue on one shared-memory word -- and the rows
+    // are combined after the pass (sums and minima: the order does not matter).
     if (lane == 0) {
         s_wid[warp] = w;
         if (valid) atomicOr(&s_tab[w & 255u], 1u << warp);
@@ -261,24 +266,40 @@ emb_det_kernel(float* __restrict__ dE, const T* __restrict__ dy,
                 if (s_wid[t] != x[i]) continue;
                 const int pos = k + i, jt = blockIdx.x * W + t;
                 if (pos < jt) {
-                    atomicAdd(&s_rank[t], 1);
-                    atomicMin(&s_low[t], pos);
+                    atomicAdd(&s_rank[warp][t], 1);
+                    atomicMin(&s_low[warp][t], pos);
                 } else if (pos > jt) {
-                    const int slot = atomicAdd(&s_nlater[t], 1);
-                    if (slot < 2) s_next[t][slot] = pos;
+                    const int slot = atomicAdd(&s_nlater[warp][t], 1);
+                    if (slot < 2) s_next[warp][t][slot] = pos;
                 }
             }
         }
     }
     __syncthreads();
-    const int r = s_rank[warp], later = s_nlater[warp];
-    const int first = r > 0 ? s_low[warp] : j;
-    int p1 = s_next[warp][0], p2 = s_next[warp][1];
-    if (later >= 2 && p2 < p1) { const int tmp = p1; p1 = p2; p2 = tmp; }
+    // Token `warp`'s counts: lane c reads counting warp c's row.  p1 < p2 are
+    // the two smallest later positions (all of them when there are at most two).
+    const int cr = lane < W ? s_rank[lane][warp] : 0;
+    const int cl = lane < W ? s_nlater[lane][warp] : 0;
+    const int r = __reduce_add_sync(0xffffffffu, cr);
+    const int later = __reduce_add_sync(0xffffffffu, cl);
+    const int first = r > 0 ? __reduce_min_sync(0xffffffffu, lane < W ? s_low[lane][warp] : ntok)
+                            : j;
+    const int e0 = cl >= 1 ? s_next[lane][warp][0] : ntok;
+    const int e1 = cl >= 2 ? s_next[lane][warp][1] : ntok;
+    const int p1 = __reduce_min_sync(0xffffffffu, min(e0, e1));
+    const int p2 = __reduce_min_sync(0xffffffffu, min(e0, e1) == p1 ? max(e0, e1) : min(e0, e1));
     const int n = r + 1 + later;
     const bool frequent = valid && n >= kFrequent;
-    if (lane == 0)
-        s_first[warp] = frequent && r == static_cast<int>(__umulhi(w * 2654435761u, n)) ? first : -1;
+    const int ncb = (nvr + 31) / 32;  // 32-vector column blocks of a row
+    if (lane == 0) {
+        // Column block b of a frequent id goes to its token of rank (h + b) mod n,
+        // h a hash of the id: this token takes blocks b0, b0 + n, ...
+        const int h = static_cast<int>(__umulhi(w * 2654435761u, static_cast<uint32_t>(n)));
+        const int b0 = r >= h ? r - h : r - h + n;
+        s_first[warp] = frequent && b0 < ncb ? first : -1;
+        s_blk[warp] = b0;
+        s_cnt[warp] = n;
+    }
 
     if (valid && !frequent && r == 0) {
         const int64_t row1 = static_cast<int64_t>(p1) * nvr, row2 = static_cast<int64_t>(p2) * nvr;
@@ -326,21 +347,17 @@ emb_det_kernel(float* __restrict__ dE, const T* __restrict__ dy,
         }
     }
 
-    // The frequent ids handed to this CTA, one after another, by all its warps.
+    // The column blocks of frequent ids handed to this CTA, one after another,
+    // by all its warps: warp s sums slice s of the positions [f, T).
     __syncthreads();
-    const int ncb = (nvr + 31) / 32;  // 32-vector column blocks of a row
     for (int t = 0; t < W; ++t) {
         const int f = s_first[t];  // the same in every thread of the CTA
         if (f < 0) continue;
         const uint32_t wt = ids[blockIdx.x * W + t];
-        for (int cb0 = 0; cb0 < ncb; cb0 += W) {
-            const int nb = min(ncb - cb0, W);  // column blocks this round
-            const int ns = W / nb;             // slices per block
-            const int bi = warp / ns, si = warp % ns;
-            const bool active = bi < nb;
-            const int cv = (cb0 + bi) * 32 + lane;
-            const int per = (ntok - f + ns - 1) / ns;
-            const int lo = min(ntok, f + si * per), hi = active ? min(ntok, lo + per) : lo;
+        const int per = (ntok - f + W - 1) / W;
+        const int lo = min(ntok, f + warp * per), hi = min(ntok, lo + per);
+        for (int cb = s_blk[t]; cb < ncb; cb += s_cnt[t]) {
+            const int cv = cb * 32 + lane;
             float acc[kVec];
 #pragma unroll
             for (int q = 0; q < kVec; ++q) acc[q] = 0.f;
@@ -389,12 +406,13 @@ emb_det_kernel(float* __restrict__ dE, const T* __restrict__ dy,
             pp[0] = make_float4(acc[0], acc[1], acc[2], acc[3]);
             pp[1] = make_float4(acc[4], acc[5], acc[6], acc[7]);
             __syncthreads();
-            for (int q = threadIdx.x; q < nb * 32 * kVec; q += 32 * W) {
-                const int b = q / (32 * kVec), v = (q / kVec) % 32, e = q % kVec;
-                const int vv = (cb0 + b) * 32 + v;
+            if (threadIdx.x < 32 * kVec) {
+                const int v = threadIdx.x / kVec, e = threadIdx.x % kVec;
+                const int vv = cb * 32 + v;
                 if (vv < nvr) {
                     float sum = 0.f;
-                    for (int s2 = 0; s2 < ns; ++s2) sum += s_part[b * ns + s2][v][e];
+#pragma unroll
+                    for (int s2 = 0; s2 < W; ++s2) sum += s_part[s2][v][e];
                     float* d = dE + static_cast<int64_t>(wt) * a.H + static_cast<int64_t>(vv) * kVec + e;
                     *d = fmaf(a.coef, sum, *d);
                 }

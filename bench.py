@@ -70,8 +70,10 @@ def parse_args():
     ap.add_argument("--profile-op", default=None,
                     help="run the layer once, then only this operator ('all': every operator "
                          "in layer order; softmax_long_fwd / softmax_long_bwd: rows of "
-                         "--profile-k-len keys) inside the NVTX range 'profile' (for ncu --nvtx "
-                         "--nvtx-include profile/); no timing")
+                         "--profile-k-len keys; embedding_bwd / embedding_bwd_zipf: the "
+                         "deterministic embedding backward on uniform / Zipf token ids) inside "
+                         "the NVTX range 'profile' (for ncu --nvtx --nvtx-include profile/); "
+                         "no timing")
     ap.add_argument("--profile-launches", type=int, default=2)
     ap.add_argument("--profile-flush-mb", type=int, default=0,
                     help="--profile-op: end the range with a read of a clean buffer of this "
@@ -1054,6 +1056,54 @@ def run_profile_long_softmax(args):
     return 0
 
 
+def run_profile_embedding(args):
+    """--profile-op embedding_bwd|embedding_bwd_zipf: the deterministic embedding
+    backward at the workload's token count and width, on token ids drawn
+    uniformly or from Zipf(1.1) folded into the vocabulary (as --next-ops
+    draws them), called --profile-launches times inside the NVTX range
+    'profile' after one untimed call."""
+    import numpy as np
+    import torch
+
+    from transformer_layer_non_gb300 import accounting, ls_ops, synth
+    from transformer_layer_non_gb300.ncu_report import kernels_sha
+
+    ls_ops.load()
+    dev = torch.device("cuda", 0)
+    L = synth.LAYERS[args.workload]
+    T, H, B, S = L.tokens, L.hidden, L.batch, L.seq
+    dt = {"f16": torch.float16, "f32": torch.float32}[L.dtype]
+    ev = synth.EMBEDDING_VOCAB[L.name]
+    rng = np.random.default_rng(args.seed)
+    if args.profile_op == "embedding_bwd_zipf":
+        tok = (rng.zipf(1.1, T) - 1) % ev
+    else:
+        tok = rng.integers(0, ev, T)
+    g = torch.Generator(device=dev).manual_seed(args.seed)
+    tokens = torch.from_numpy(tok.astype(np.int32)).to(dev)
+    E = torch.randn(ev, H, generator=g, device=dev).to(dt)
+    P = torch.randn(S, H, generator=g, device=dev).to(dt)
+    y = torch.empty(T, H, dtype=dt, device=dev)
+    mask = torch.empty((T * H + 31) // 32, dtype=torch.int32, device=dev)
+    dy = torch.randn(T, H, generator=g, device=dev).to(dt)
+    dE = torch.zeros(ev, H, dtype=torch.float32, device=dev)
+    s = float(H) ** 0.5
+    ls_ops.ls_embedding_fwd(y, mask, tokens, E, P, B, S, s, L.p, 0, 10)
+    ls_ops.ls_embedding_bwd(dE, dy, mask, tokens, B, S, s, L.p)
+    torch.cuda.synchronize()
+    torch.cuda.nvtx.range_push("profile")
+    for _ in range(args.profile_launches):
+        ls_ops.ls_embedding_bwd(dE, dy, mask, tokens, B, S, s, L.p)
+    torch.cuda.nvtx.range_pop()
+    torch.cuda.synchronize()
+    nbytes = accounting.embedding_bwd_bytes(T, int(np.unique(tok).size), H, dy.element_size())
+    print(json.dumps({"profile_op": args.profile_op, "workload": args.workload,
+                      "kernels_sha": kernels_sha(), "launches_per_op": args.profile_launches,
+                      "launch_order": [args.profile_op] * args.profile_launches,
+                      "algorithmic_bytes": {args.profile_op: int(nbytes)}}))
+    return 0
+
+
 def run_profile_op(args):
     """One eager pass of the whole layer (so backward inputs exist), then, inside
     the NVTX range 'profile', --profile-launches calls of one operator, or of
@@ -1065,6 +1115,8 @@ def run_profile_op(args):
 
     if args.profile_op in ("softmax_long_fwd", "softmax_long_bwd"):
         return run_profile_long_softmax(args)
+    if args.profile_op in ("embedding_bwd", "embedding_bwd_zipf"):
+        return run_profile_embedding(args)
     ls_ops.load()
     step = LayerStep(synth.LAYERS[args.workload], args.seed, torch.device("cuda", 0))
     ops = step.ops()

@@ -129,7 +129,7 @@ __device__ __forceinline__ void ln_fwd_row(const Raw8<T> (&xr)[VPT], T* y, float
 }
 
 template <typename T, int LPR, int VPT>
-__global__ void __launch_bounds__(kThreads, min_ctas<T>(VPT == 2 ? 3 : (VPT <= 3 ? 4 : (VPT <= 4 ? 3 : 2))))
+__global__ void __launch_bounds__(kThreads, min_ctas<T>(VPT == 2 ? 3 : (VPT <= 3 ? 4 : (VPT <= 6 ? 3 : 2))))
 ln_fwd_group_kernel(T* y, float* __restrict__ mean, float* __restrict__ rstd, const T* x,
                     const T* __restrict__ gamma, const T* __restrict__ beta, int64_t rows,
                     int cols, float eps) {

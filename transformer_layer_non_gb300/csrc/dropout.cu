@@ -419,7 +419,7 @@ __device__ __forceinline__ void bwd_compute(const Raw8<T> (&dr)[kBwdU],
 }
 
 template <typename T, bool REGEN>
-__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 3 : 2)
+__global__ void __launch_bounds__(kThreads, sizeof(T) == 2 ? 4 : 2)
 dropout_bwd_kernel(T* dx, float* __restrict__ partial, const T* dout,
                    const uint8_t* __restrict__ mask, const __grid_constant__ BwdArgs a) {
     __shared__ __align__(16) float red[kBwdRps][kBwdColsPerTile];

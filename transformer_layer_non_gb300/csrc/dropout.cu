@@ -331,6 +331,7 @@ struct BwdArgs {
     int64_t rows;
     int cols;
     int nbands;
+    FastDiv by_nbands;  // tile -> (row chunk, column band); tile indices stay below 2^31
     int64_t ntiles;
     int late_trigger;  // CTAs loop over several tiles: release dependents at exit
     uint32_t thr;
@@ -345,8 +346,9 @@ template <typename T, bool REGEN>
 __device__ __forceinline__ void bwd_load(Raw8<T> (&dr)[kBwdU], uint32_t (&mb)[kBwdU],
                                          const T* dout, const uint8_t* mask, int64_t tile,
                                          const BwdArgs& a, const PhiloxSchedule& ks) {
-    const int64_t chunk = tile / a.nbands;
-    const int band = static_cast<int>(tile - chunk * a.nbands);
+    const uint32_t chunk32 = fdiv(static_cast<uint32_t>(tile), a.by_nbands);
+    const int64_t chunk = chunk32;
+    const int band = static_cast<int>(static_cast<uint32_t>(tile) - chunk32 * a.by_nbands.d);
     const int lane = threadIdx.x % kBwdLanes;
     const int c0 = (band * kBwdLanes + lane) * kVec;
     const int64_t r0 = chunk * kBwdRowsPerTile + threadIdx.x / kBwdLanes;
@@ -376,8 +378,9 @@ __device__ __forceinline__ void bwd_compute(const Raw8<T> (&dr)[kBwdU],
                                             const uint32_t (&mb)[kBwdU], T* dx, float* partial,
                                             float (*red)[kBwdColsPerTile], int64_t tile,
                                             const BwdArgs& a) {
-    const int64_t chunk = tile / a.nbands;
-    const int band = static_cast<int>(tile - chunk * a.nbands);
+    const uint32_t chunk32 = fdiv(static_cast<uint32_t>(tile), a.by_nbands);
+    const int64_t chunk = chunk32;
+    const int band = static_cast<int>(static_cast<uint32_t>(tile) - chunk32 * a.by_nbands.d);
     const int lane = threadIdx.x % kBwdLanes;
     const int slot = threadIdx.x / kBwdLanes;
     const int c0 = (band * kBwdLanes + lane) * kVec;
@@ -430,8 +433,9 @@ dropout_bwd_kernel(T* dx, float* __restrict__ partial, const T* dout,
     {
         const int lane = threadIdx.x % kBwdLanes;
         const int64_t tile = blockIdx.x;
-        const int64_t chunk = tile / a.nbands;
-        const int band = static_cast<int>(tile - chunk * a.nbands);
+        const uint32_t chunk32 = fdiv(static_cast<uint32_t>(tile), a.by_nbands);
+        const int64_t chunk = chunk32;
+        const int band = static_cast<int>(static_cast<uint32_t>(tile) - chunk32 * a.by_nbands.d);
         const int c0 = (band * kBwdLanes + lane) * kVec;
         const int64_t r0 = chunk * kBwdRowsPerTile + threadIdx.x / kBwdLanes;
 #pragma unroll
@@ -587,6 +591,7 @@ cudaError_t bwd_impl(void* dx, float* partial, const void* dout, const uint8_t* 
     a.rows = rows;
     a.cols = static_cast<int>(cols);
     a.nbands = static_cast<int>((cols + kBwdColsPerTile - 1) / kBwdColsPerTile);
+    a.by_nbands = make_fastdiv(static_cast<uint32_t>(a.nbands));
     a.ntiles = ((rows + kBwdRowsPerTile - 1) / kBwdRowsPerTile) * a.nbands;
     a.thr = rng.thr;
     a.scale = rng.scale;
@@ -598,6 +603,9 @@ cudaError_t bwd_impl(void* dx, float* partial, const void* dout, const uint8_t* 
     static const int occ_regen = occupancy(dropout_bwd_kernel<T, true>, kThreads, 0);
     const int occ = mask ? occ_mask : occ_regen;
     const int64_t grid = std::min<int64_t>(a.ntiles, int64_t{sm_count()} * occ);
+    // Every tile index the kernel forms (up to ntiles + 2 * grid) is divided
+    // with the 31-bit FastDiv: 2^31 tiles would be 2^44 elements.
+    if (a.ntiles + 2 * grid >= (int64_t{1} << 31)) return cudaErrorInvalidValue;
     a.late_trigger = a.ntiles > grid ? 1 : 0;
     return launch_pdl(kern, dim3(static_cast<unsigned>(grid)), dim3(kThreads), 0, s,
                       static_cast<T*>(dx), partial, static_cast<const T*>(dout), mask, a);
